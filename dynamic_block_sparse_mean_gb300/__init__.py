@@ -1,1 +1,288 @@
-"""GB300-native dynamic block-sparse attention with a mean-pooled block router."""
+"""GB300-native dynamic block-sparse attention with a mean-pooled block router.
+
+A thin binding over libbsa.so (include/bsa.h): it marshals torch tensors'
+device pointers and the current CUDA stream into the C ABI.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU path.
+
+Typical prefill use::
+
+    import dynamic_block_sparse_mean_gb300 as bsa
+    plan = bsa.PrefillPlan(cu_seqlens_host, num_heads=32, num_kv_heads=8, head_dim=128,
+                           block=64, route=bsa.RouteParams(bsa.ROUTE_TOPK, k_max=32))
+    out, lse = plan.run(q, k, v)        # q [H, T, d], k / v [H_kv, T, d] bf16 on cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import BsaError, NUM_BUCKETS, check
+
+ROUTE_TOPK = 0
+ROUTE_THRESHOLD = 1
+
+__all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "PrefillPlan",
+           "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
+           "attention_fwd", "page_summaries", "decode_paged", "check_status", "library_path"]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return _lib.BSA_BF16
+    if dt == torch.float32:
+        return _lib.BSA_FP32
+    raise TypeError(f"unsupported dtype {dt}: bfloat16 or float32")
+
+
+@dataclass
+class RouteParams:
+    mode: int = ROUTE_TOPK
+    k_max: int = 32
+    k_min: int = 0
+    tau_delta: float = 0.0
+    force_sink: bool = False
+
+    def c(self) -> _lib.RouteParams:
+        return _lib.RouteParams(self.mode, self.k_max, self.k_min, self.tau_delta,
+                                1 if self.force_sink else 0)
+
+
+@dataclass
+class PrefillShape:
+    """Shape of a packed batch; cu_seqlens is the device tensor [B + 1] int32."""
+    num_seqs: int
+    total_tokens: int
+    max_seqlen: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block: int
+    dtype: torch.dtype
+    cu_seqlens: torch.Tensor
+
+    @property
+    def max_blocks(self) -> int:
+        return (self.max_seqlen + self.block - 1) // self.block
+
+    @property
+    def num_rows(self) -> int:
+        return self.num_seqs * self.num_kv_heads * self.max_blocks
+
+    def c(self) -> _lib.Shape:
+        return _lib.Shape(self.num_seqs, self.total_tokens, self.max_seqlen, self.num_heads,
+                          self.num_kv_heads, self.head_dim, self.block, self.max_blocks,
+                          _dtype_code(self.dtype), ctypes.c_void_p(self.cu_seqlens.data_ptr()))
+
+    @staticmethod
+    def make(cu_seqlens_host, num_heads, num_kv_heads, head_dim, block, dtype=torch.bfloat16,
+             device="cuda") -> "PrefillShape":
+        cu = np.asarray(cu_seqlens_host, dtype=np.int64)
+        lens = np.diff(cu)
+        return PrefillShape(len(lens), int(cu[-1]), int(lens.max()), num_heads, num_kv_heads,
+                            head_dim, block, dtype,
+                            torch.as_tensor(cu.astype(np.int32), device=device))
+
+
+@dataclass
+class Worklist:
+    row_ptr: torch.Tensor
+    col_idx: torch.Tensor
+    work: torch.Tensor
+    bucket_off: torch.Tensor
+
+
+def check_status(dev_status: torch.Tensor) -> None:
+    """Raise if a kernel recorded a device-side error (synchronises on the tensor)."""
+    code = int(dev_status.item())
+    if code != 0:
+        raise BsaError("device", code)
+
+
+def block_summaries(k: torch.Tensor, shape: PrefillShape, out: torch.Tensor | None = None):
+    """[B, H_kv, N_q, d] fp32 mean key of every block (bsa_block_summaries)."""
+    if out is None:
+        out = torch.empty(shape.num_seqs, shape.num_kv_heads, shape.max_blocks, shape.head_dim,
+                          dtype=torch.float32, device=k.device)
+    s = shape.c()
+    check("bsa_block_summaries", _lib.lib().bsa_block_summaries(ctypes.byref(s), _p(k), _p(out),
+                                                                 _stream()))
+    return out
+
+
+def route_workspace_bytes(shape: PrefillShape, params: RouteParams) -> int:
+    s, p = shape.c(), params.c()
+    return int(_lib.lib().bsa_route_workspace_size(ctypes.byref(s), ctypes.byref(p)))
+
+
+def route(q, C, shape: PrefillShape, params: RouteParams, J=None, counts=None, scores=None,
+          ws=None, dev_status=None):
+    """J [B, H_kv, N_q, k_max] and counts [B, H_kv, N_q] (bsa_route)."""
+    dev = q.device
+    if J is None:
+        J = torch.empty(shape.num_seqs, shape.num_kv_heads, shape.max_blocks, params.k_max,
+                        dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty(shape.num_seqs, shape.num_kv_heads, shape.max_blocks,
+                             dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(256, route_workspace_bytes(shape, params)), dtype=torch.uint8,
+                         device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    s, p = shape.c(), params.c()
+    check("bsa_route", _lib.lib().bsa_route(ctypes.byref(s), ctypes.byref(p), _p(q), _p(C), _p(J),
+                                            _p(counts), _p(scores), _p(dev_status), _p(ws),
+                                            ws.numel(), _stream()))
+    return J, counts
+
+
+def build_worklist(J, counts, shape: PrefillShape, k_max: int, dev_status, wl: Worklist | None = None,
+                   ws=None) -> Worklist:
+    dev = J.device
+    rows = shape.num_rows
+    if wl is None:
+        wl = Worklist(torch.empty(rows + 1, dtype=torch.int32, device=dev),
+                      torch.empty(max(1, rows * k_max), dtype=torch.int32, device=dev),
+                      torch.empty(max(1, rows), dtype=torch.int32, device=dev),
+                      torch.empty(NUM_BUCKETS + 1, dtype=torch.int32, device=dev))
+    s = shape.c()
+    if ws is None:
+        n = int(_lib.lib().bsa_worklist_workspace_size(ctypes.byref(s), k_max))
+        ws = torch.empty(max(256, n), dtype=torch.uint8, device=dev)
+    check("bsa_build_worklist", _lib.lib().bsa_build_worklist(
+        ctypes.byref(s), k_max, _p(J), _p(counts), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work),
+        _p(wl.bucket_off), _p(dev_status), _p(ws), ws.numel(), _stream()))
+    return wl
+
+
+def attention_fwd(q, k, v, wl: Worklist, shape: PrefillShape, dev_status, scale: float = 0.0,
+                  out=None, lse=None, want_lse: bool = True):
+    """O [H, T, d] (q's dtype) and lse [H, T] fp32 on the worklist's tiles."""
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(shape.num_heads, shape.total_tokens, dtype=torch.float32, device=q.device)
+    s = shape.c()
+    check("bsa_attention_fwd", _lib.lib().bsa_attention_fwd(
+        ctypes.byref(s), _p(q), _p(k), _p(v), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work),
+        _p(wl.bucket_off), float(scale), _p(out), _p(lse), _p(dev_status), _stream()))
+    return out, lse
+
+
+class PrefillPlan:
+    """All buffers of one prefill shape, allocated once; run() enqueues the four calls
+    (summaries, route, worklist, attention) on the current stream."""
+
+    def __init__(self, cu_seqlens_host, num_heads: int, num_kv_heads: int, head_dim: int,
+                 block: int, route: RouteParams, dtype=torch.bfloat16, device="cuda",
+                 keep_scores: bool = False):
+        self.shape = PrefillShape.make(cu_seqlens_host, num_heads, num_kv_heads, head_dim, block,
+                                       dtype, device)
+        self.params = route
+        sh, dev = self.shape, device
+        self.C = torch.empty(sh.num_seqs, num_kv_heads, sh.max_blocks, head_dim,
+                             dtype=torch.float32, device=dev)
+        self.J = torch.empty(sh.num_seqs, num_kv_heads, sh.max_blocks, route.k_max,
+                             dtype=torch.int32, device=dev)
+        self.counts = torch.empty(sh.num_seqs, num_kv_heads, sh.max_blocks, dtype=torch.int32,
+                                  device=dev)
+        self.scores = (torch.empty(sh.num_seqs, num_kv_heads, sh.max_blocks, sh.max_blocks,
+                                   dtype=torch.float32, device=dev) if keep_scores else None)
+        self.route_ws = torch.empty(max(256, route_workspace_bytes(sh, route)), dtype=torch.uint8,
+                                    device=dev)
+        rows = sh.num_rows
+        self.wl = Worklist(torch.empty(rows + 1, dtype=torch.int32, device=dev),
+                           torch.empty(max(1, rows * route.k_max), dtype=torch.int32, device=dev),
+                           torch.empty(max(1, rows), dtype=torch.int32, device=dev),
+                           torch.empty(NUM_BUCKETS + 1, dtype=torch.int32, device=dev))
+        s = sh.c()
+        self.wl_ws = torch.empty(max(256, int(_lib.lib().bsa_worklist_workspace_size(
+            ctypes.byref(s), route.k_max))), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(num_heads, sh.total_tokens, head_dim, dtype=dtype, device=dev)
+        self.lse = torch.empty(num_heads, sh.total_tokens, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def route(self, q, k):
+        block_summaries(k, self.shape, out=self.C)
+        route(q, self.C, self.shape, self.params, J=self.J, counts=self.counts,
+              scores=self.scores, ws=self.route_ws, dev_status=self.status)
+        build_worklist(self.J, self.counts, self.shape, self.params.k_max, self.status,
+                       wl=self.wl, ws=self.wl_ws)
+
+    def attend(self, q, k, v, scale: float = 0.0):
+        return attention_fwd(q, k, v, self.wl, self.shape, self.status, scale, out=self.out,
+                             lse=self.lse)
+
+    def run(self, q, k, v, scale: float = 0.0):
+        self.route(q, k)
+        return self.attend(q, k, v, scale)
+
+
+# ---------------------------------------------------------------- decode
+
+
+def _dshape(q, k_cache, block_table, top_k: int) -> _lib.DecodeShape:
+    R, H, d = q.shape
+    P, Hk, page, _ = k_cache.shape
+    return _lib.DecodeShape(R, H, Hk, d, page, block_table.shape[1], P, top_k)
+
+
+def page_summaries(k_cache, block_table, context_lens, out=None):
+    """[P, H_kv, d] fp32 mean key of every referenced page (bsa_page_summaries)."""
+    P, Hk, page, d = k_cache.shape
+    if out is None:
+        out = torch.zeros(P, Hk, d, dtype=torch.float32, device=k_cache.device)
+    s = _lib.DecodeShape(block_table.shape[0], Hk, Hk, d, page, block_table.shape[1], P, 1)
+    check("bsa_page_summaries", _lib.lib().bsa_page_summaries(
+        ctypes.byref(s), _p(k_cache), _p(block_table), _p(context_lens), _p(out), _stream()))
+    return out
+
+
+class DecodePlan:
+    """Buffers for one decode batch shape; run() enqueues bsa_decode_paged."""
+
+    def __init__(self, num_reqs, num_heads, num_kv_heads, head_dim, page_size, max_pages,
+                 num_phys_pages, top_k, device="cuda"):
+        self.cshape = _lib.DecodeShape(num_reqs, num_heads, num_kv_heads, head_dim, page_size,
+                                       max_pages, num_phys_pages, top_k)
+        self.top_k = top_k
+        n = int(_lib.lib().bsa_decode_workspace_size(ctypes.byref(self.cshape)))
+        self.ws = torch.empty(max(256, n), dtype=torch.uint8, device=device)
+        self.out = torch.empty(num_reqs, num_heads, head_dim, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(num_reqs, num_heads, dtype=torch.float32, device=device)
+        self.sel = torch.empty(num_reqs, num_kv_heads, top_k + 1, dtype=torch.int32, device=device)
+        self.sel_counts = torch.empty(num_reqs, num_kv_heads, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, q, k_cache, v_cache, page_summ, block_table, context_lens, scale: float = 0.0):
+        check("bsa_decode_paged", _lib.lib().bsa_decode_paged(
+            ctypes.byref(self.cshape), _p(q), _p(k_cache), _p(v_cache), _p(page_summ),
+            _p(block_table), _p(context_lens), float(scale), _p(self.out), _p(self.lse),
+            _p(self.sel), _p(self.sel_counts), _p(self.status), _p(self.ws), self.ws.numel(),
+            _stream()))
+        return self.out, self.lse, self.sel, self.sel_counts
+
+
+def decode_paged(q, k_cache, v_cache, page_summ, block_table, context_lens, top_k: int = 32,
+                 scale: float = 0.0):
+    R, H, d = q.shape
+    P, Hk, page, _ = k_cache.shape
+    plan = DecodePlan(R, H, Hk, d, page, block_table.shape[1], P, top_k, device=q.device)
+    return plan.run(q, k_cache, v_cache, page_summ, block_table, context_lens, scale)

@@ -1,0 +1,197 @@
+// C ABI of libbsa.so: argument checks, workspace sizing and dispatch to the
+// launchers.  Every entry point validates its arguments before anything is
+// enqueued; nothing here allocates, copies or synchronises.
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsa {
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  static int cache[64] = {0};
+  if (dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+}  // namespace bsa
+
+namespace {
+
+bool shape_ok(const bsa_shape_t *s) {
+  if (s == nullptr || s->cu_seqlens == nullptr) return false;
+  if (s->num_seqs < 1 || s->total_tokens < 1 || s->max_seqlen < 1) return false;
+  if (s->num_heads < 1 || s->num_kv_heads < 1 || s->num_heads % s->num_kv_heads != 0) return false;
+  if (s->block < 1) return false;
+  if (s->max_blocks != (s->max_seqlen + s->block - 1) / s->block) return false;
+  const long long rows = (long long)s->num_seqs * s->num_kv_heads * s->max_blocks;
+  if (rows > (1LL << 30)) return false;
+  return true;
+}
+
+bool shape_supported(const bsa_shape_t *s) {
+  return (s->head_dim == 64 || s->head_dim == 128) && (s->block == 64 || s->block == 128) &&
+         (s->dtype == BSA_BF16 || s->dtype == BSA_FP32);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bsa_status_t launched(cudaError_t e) { return e == cudaSuccess ? BSA_OK : BSA_ERR_LAUNCH; }
+
+bool decode_ok(const bsa_decode_shape_t *s) {
+  return s != nullptr && s->num_reqs >= 1 && s->num_heads >= 1 && s->num_kv_heads >= 1 &&
+         s->num_heads % s->num_kv_heads == 0 && s->max_pages_per_req >= 1 &&
+         s->num_phys_pages >= 1;
+}
+
+bool decode_supported(const bsa_decode_shape_t *s) {
+  const int G = s->num_heads / s->num_kv_heads;
+  return s->head_dim == 128 && s->page_size == 64 && s->top_k >= 1 && s->top_k <= 64 &&
+         (G == 1 || G == 2 || G == 4 || G == 8) && s->max_pages_per_req <= 16384;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bsa_version(void) { return BSA_VERSION; }
+
+const char *bsa_status_string(bsa_status_t s) {
+  switch (s) {
+    case BSA_OK: return "ok";
+    case BSA_ERR_INVALID_ARG: return "invalid argument";
+    case BSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BSA_ERR_WORKSPACE: return "workspace too small";
+    case BSA_ERR_LAUNCH: return "kernel launch failed";
+    case BSA_ERR_INDEX_RANGE: return "index row entry outside [0, r]";
+    case BSA_ERR_INDEX_ORDER: return "index row not strictly increasing";
+    case BSA_ERR_COUNT: return "row count outside [0, k_max]";
+    case BSA_ERR_TIMEOUT: return "bounded barrier wait timed out";
+  }
+  return "unknown status";
+}
+
+bsa_status_t bsa_block_summaries(const bsa_shape_t *shape, const void *K, float *C,
+                                 cudaStream_t stream) {
+  if (!shape_ok(shape) || K == nullptr || C == nullptr) return BSA_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(K) || !aligned16(C)) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_block_summaries(*shape, K, C, stream));
+}
+
+size_t bsa_route_workspace_size(const bsa_shape_t *shape, const bsa_route_params_t *params) {
+  if (!shape_ok(shape) || params == nullptr) return 0;
+  return bsa::route_workspace_bytes(*shape, *params);
+}
+
+bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *params,
+                       const void *Q, const float *C, int32_t *J, int32_t *counts,
+                       float *scores, int32_t *dev_status, void *ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  if (!shape_ok(shape) || params == nullptr || Q == nullptr || C == nullptr || J == nullptr ||
+      counts == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (params->mode != BSA_ROUTE_TOPK && params->mode != BSA_ROUTE_THRESHOLD)
+    return BSA_ERR_INVALID_ARG;
+  if (params->k_max < 1 || params->k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
+  if (params->mode == BSA_ROUTE_THRESHOLD &&
+      (params->k_min < 0 || !(params->tau_delta >= 0.f) || !isfinite(params->tau_delta)))
+    return BSA_ERR_INVALID_ARG;
+  if (params->force_sink && params->k_max < 2) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(C)) return BSA_ERR_INVALID_ARG;
+  const size_t need = bsa::route_workspace_bytes(*shape, *params);
+  if (scores == nullptr && (ws == nullptr || ws_bytes < need)) return BSA_ERR_WORKSPACE;
+  return launched(bsa::launch_route(*shape, *params, Q, C, J, counts, scores, dev_status, ws,
+                                    stream));
+}
+
+size_t bsa_worklist_workspace_size(const bsa_shape_t *shape, int32_t k_max) {
+  if (!shape_ok(shape)) return 0;
+  return bsa::worklist_workspace_bytes(*shape, k_max);
+}
+
+bsa_status_t bsa_build_worklist(const bsa_shape_t *shape, int32_t k_max, const int32_t *J,
+                                const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
+                                int32_t *work, int32_t *bucket_off, int32_t *dev_status,
+                                void *ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!shape_ok(shape) || J == nullptr || counts == nullptr || row_ptr == nullptr ||
+      col_idx == nullptr || work == nullptr || bucket_off == nullptr || dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (k_max < 1 || k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < bsa::worklist_workspace_bytes(*shape, k_max))
+    return BSA_ERR_WORKSPACE;
+  return launched(bsa::launch_worklist(*shape, k_max, J, counts, row_ptr, col_idx, work,
+                                       bucket_off, dev_status, ws, stream));
+}
+
+bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const void *K,
+                               const void *V, const int32_t *row_ptr, const int32_t *col_idx,
+                               const int32_t *work, const int32_t *bucket_off,
+                               float softmax_scale, void *O, float *lse, int32_t *dev_status,
+                               cudaStream_t stream) {
+  if (!shape_ok(shape) || Q == nullptr || K == nullptr || V == nullptr || row_ptr == nullptr ||
+      col_idx == nullptr || work == nullptr || bucket_off == nullptr || O == nullptr ||
+      dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return BSA_ERR_INVALID_ARG;
+  if (!isfinite(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)shape->head_dim);
+  if (shape->dtype == BSA_BF16)
+    return launched(bsa::launch_attention_tc(*shape, Q, K, V, row_ptr, col_idx, work, bucket_off,
+                                             scale, O, lse, dev_status, stream));
+  return launched(bsa::launch_attention_simt_f32(*shape, Q, K, V, row_ptr, col_idx, work,
+                                                 bucket_off, scale, O, lse, stream));
+}
+
+bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_cache,
+                                const int32_t *block_table, const int32_t *context_lens,
+                                float *page_summ, cudaStream_t stream) {
+  if (!decode_ok(shape) || k_cache == nullptr || block_table == nullptr ||
+      context_lens == nullptr || page_summ == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!decode_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(page_summ)) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_page_summaries(*shape, k_cache, block_table, context_lens,
+                                             page_summ, stream));
+}
+
+size_t bsa_decode_workspace_size(const bsa_decode_shape_t *shape) {
+  if (!decode_ok(shape)) return 0;
+  return bsa::decode_workspace_bytes(*shape);
+}
+
+bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
+                              const void *k_cache, const void *v_cache,
+                              const float *page_summ, const int32_t *block_table,
+                              const int32_t *context_lens, float softmax_scale, void *o,
+                              float *lse, int32_t *sel, int32_t *sel_counts,
+                              int32_t *dev_status, void *ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  if (!decode_ok(shape) || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      page_summ == nullptr || block_table == nullptr || context_lens == nullptr ||
+      o == nullptr || sel == nullptr || sel_counts == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!decode_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(page_summ))
+    return BSA_ERR_INVALID_ARG;
+  if (!isfinite(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < bsa::decode_workspace_bytes(*shape)) return BSA_ERR_WORKSPACE;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)shape->head_dim);
+  return launched(bsa::launch_decode(*shape, q, k_cache, v_cache, page_summ, block_table,
+                                     context_lens, scale, o, lse, sel, sel_counts, dev_status, ws,
+                                     stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Host-side launchers implemented in the kernel translation units and called by
+// the argument-checking entry points in api.cu.  Every launcher enqueues on the
+// given stream and returns the launch error, if any.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bsa.h"
+
+namespace bsa {
+
+int num_sms();
+
+// a1 and the decode page summaries (summaries.cu)
+cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
+                                   cudaStream_t st);
+cudaError_t launch_page_summaries(const bsa_decode_shape_t &s, const void *k_cache,
+                                  const int32_t *block_table, const int32_t *context_lens,
+                                  float *page_summ, cudaStream_t st);
+
+// a2 + a3 (route.cu)
+size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &p);
+cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
+                         const float *C, int32_t *J, int32_t *counts, float *scores,
+                         int32_t *dev_status, void *ws, cudaStream_t st);
+
+// a4 (worklist.cu)
+size_t worklist_workspace_bytes(const bsa_shape_t &s, int32_t k_max);
+cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *J,
+                            const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
+                            int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
+                            cudaStream_t st);
+
+// a5, tensor-core BF16 path (attn_tc.cu) and SIMT FP32 path (attn_simt.cu)
+cudaError_t launch_attention_tc(const bsa_shape_t &s, const void *Q, const void *K,
+                                const void *V, const int32_t *row_ptr, const int32_t *col_idx,
+                                const int32_t *work, const int32_t *bucket_off, float scale,
+                                void *O, float *lse, int32_t *dev_status, cudaStream_t st);
+cudaError_t launch_attention_simt_f32(const bsa_shape_t &s, const void *Q, const void *K,
+                                      const void *V, const int32_t *row_ptr,
+                                      const int32_t *col_idx, const int32_t *work,
+                                      const int32_t *bucket_off, float scale, void *O,
+                                      float *lse, cudaStream_t st);
+
+// a6 (decode.cu)
+size_t decode_workspace_bytes(const bsa_decode_shape_t &s);
+cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void *k_cache,
+                          const void *v_cache, const float *page_summ,
+                          const int32_t *block_table, const int32_t *context_lens, float scale,
+                          void *o, float *lse, int32_t *sel, int32_t *sel_counts,
+                          int32_t *dev_status, void *ws, cudaStream_t st);
+
+}  // namespace bsa

@@ -1,0 +1,275 @@
+// a2 + a3: the block router of "2.1 · 粗粒度选择" §2.1.
+//   scores  g[i,h,r,j] = max over the group's query heads and the valid tokens
+//           of block r of q . c_j, j < r (eq.(6), pool = max; unscaled)
+//   select  forced diagonal (+ sink), then top-k or the clamped threshold of
+//           eq.(7); ranking (score desc, index asc); rows deduplicated and
+//           sorted ascending (eq.(1) address order).
+// Scores are fp32 FFMA dot products (fp32-accurate: the selection is compared
+// bit-exactly, up to a 1e-5 tie band, with a float64 oracle).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsa {
+namespace {
+
+constexpr int kTile = 64;     // query rows x summaries per CTA tile
+constexpr int kKc = 32;       // d chunk
+constexpr int kThreads = 256;  // 16 x 16 threads, 4 x 4 outputs each
+
+template <typename T>
+BSA_DEV void load8(const T *p, float *v);
+template <>
+BSA_DEV void load8<uint16_t>(const uint16_t *p, float *v) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = __uint_as_float(w[e] << 16);
+    v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+template <>
+BSA_DEV void load8<float>(const float *p, float *v) {
+  const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// grid (N_q, H_kv, B): one CTA per router row (i, h, r); writes g[r][0 .. r-1].
+template <typename T>
+__global__ void __launch_bounds__(kThreads) route_scores_kernel(
+    const T *__restrict__ Q, const float *__restrict__ C, const int32_t *__restrict__ cu,
+    float *__restrict__ S, int T_tok, int Nq, int Hk, int G, int d, int b) {
+  __shared__ float Qs[kKc][kTile + 4];
+  __shared__ float Cs[kKc][kTile + 4];
+  __shared__ float red[16][kTile];
+  const int r = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+  const int s0 = cu[i], n = cu[i + 1] - s0;
+  const int nb = (n + b - 1) / b;
+  if (r >= nb || r == 0) return;
+  const int nvalid = min(b, n - r * b);       // valid query tokens of block r
+  const int nrows = G * nvalid;                // pooled query rows
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const float *Crow = C + (((size_t)i * Hk + h) * Nq) * d;
+  float *Srow = S + (((size_t)i * Hk + h) * Nq + r) * Nq;
+  // loader mapping: 256 threads x 8 elements = 64 rows x 32 columns
+  const int lrow = threadIdx.x / 4, lk = (threadIdx.x % 4) * 8;
+
+  for (int j0 = 0; j0 < r; j0 += kTile) {
+    float runmax[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int q0 = 0; q0 < nrows; q0 += kTile) {
+      float acc[4][4] = {};
+      for (int k0 = 0; k0 < d; k0 += kKc) {
+        {
+          float v[8];
+          const int rho = q0 + lrow;
+          if (rho < nrows) {
+            const int hq = h * G + rho / nvalid, t = r * b + rho % nvalid;
+            load8<T>(Q + ((size_t)hq * T_tok + s0 + t) * d + k0 + lk, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) Qs[lk + e][lrow] = v[e];
+          const int j = j0 + lrow;
+          if (j < r) {
+            const float4 *cp = reinterpret_cast<const float4 *>(Crow + (size_t)j * d + k0 + lk);
+            const float4 a = __ldg(cp), c = __ldg(cp + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) Cs[lk + e][lrow] = v[e];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kKc; ++k) {
+          const float4 qa = *reinterpret_cast<const float4 *>(&Qs[k][ty * 4]);
+          const float4 ca = *reinterpret_cast<const float4 *>(&Cs[k][tx * 4]);
+          const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
+          const float cv[4] = {ca.x, ca.y, ca.z, ca.w};
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(qv[a], cv[c], acc[a][c]);
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        if (q0 + ty * 4 + a < nrows)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) runmax[c] = fmaxf(runmax[c], acc[a][c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) red[ty][tx * 4 + c] = runmax[c];
+    __syncthreads();
+    if (threadIdx.x < kTile) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int y = 0; y < 16; ++y) m = fmaxf(m, red[y][threadIdx.x]);
+      const int j = j0 + threadIdx.x;
+      if (j < r) Srow[j] = m;
+    }
+    __syncthreads();
+  }
+}
+
+struct Cand {
+  float v;
+  int idx;
+};
+
+BSA_DEV bool better(const Cand &a, const Cand &b) {
+  return a.v > b.v || (a.v == b.v && a.idx < b.idx);
+}
+
+BSA_DEV Cand warp_best(Cand c) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Cand o;
+    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
+    o.idx = __shfl_xor_sync(0xffffffffu, c.idx, off);
+    if (better(o, c)) c = o;
+  }
+  return c;
+}
+
+// One warp per router row: forced blocks, then top-k / eq.(7) threshold, then sort.
+// Dynamic shared memory: N_q floats of scores, N_q bytes of flags, k_max ints.
+__global__ void __launch_bounds__(32) route_select_kernel(
+    const float *__restrict__ S, const int32_t *__restrict__ cu, int32_t *__restrict__ J,
+    int32_t *__restrict__ counts, int Nq, int Hk, int b, int mode, int k_max, int k_min,
+    float tau_delta, int force_sink) {
+  extern __shared__ uint8_t sm[];
+  float *sc = reinterpret_cast<float *>(sm);
+  int32_t *ids = reinterpret_cast<int32_t *>(sm + (size_t)Nq * 4);
+  uint8_t *taken = sm + (size_t)Nq * 4 + (size_t)(k_max + 2) * 4;
+  const int lane = threadIdx.x;
+  const int row = blockIdx.x;
+  const int r = row % Nq, h = (row / Nq) % Hk, i = row / (Nq * Hk);
+  (void)h;
+  const int n = cu[i + 1] - cu[i];
+  const int nb = (n + b - 1) / b;
+  int32_t *Jrow = J + (size_t)row * k_max;
+  if (r >= nb) {
+    for (int e = lane; e < k_max; e += 32) Jrow[e] = -1;
+    if (lane == 0) counts[row] = 0;
+    return;
+  }
+  const float *Srow = S + (size_t)row * Nq;
+  const bool sink = force_sink && r > 0;
+  const int nforced = sink ? 2 : 1;
+  int ncand = 0;
+  for (int j = lane; j < r; j += 32) {
+    const bool is_cand = !(sink && j == 0);
+    sc[j] = Srow[j];
+    taken[j] = is_cand ? 0 : 1;
+    ncand += is_cand ? 1 : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ncand += __shfl_xor_sync(0xffffffffu, ncand, off);
+  __syncwarp();
+
+  int k_dyn;
+  if (mode == BSA_ROUTE_TOPK) {
+    k_dyn = k_max - nforced;
+  } else {
+    float mx = -INFINITY;
+    for (int j = lane; j < r; j += 32)
+      if (!taken[j]) mx = fmaxf(mx, sc[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float tau = mx - tau_delta;
+    int a = 0;
+    for (int j = lane; j < r; j += 32)
+      if (!taken[j] && sc[j] >= tau) ++a;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    const int k_r = min(k_max, min(max(k_min, nforced + a), nforced + ncand));
+    k_dyn = k_r - nforced;
+  }
+  k_dyn = max(0, min(k_dyn, ncand));
+
+  // Local best among this lane's strided candidates.
+  auto local_best = [&]() {
+    Cand c{-INFINITY, 0x7fffffff};
+    for (int j = lane; j < r; j += 32)
+      if (!taken[j]) {
+        const Cand o{sc[j], j};
+        if (c.idx == 0x7fffffff || better(o, c)) c = o;
+      }
+    return c;
+  };
+  Cand mine = local_best();
+  for (int k = 0; k < k_dyn; ++k) {
+    const Cand w = warp_best(mine);
+    if (lane == 0) ids[nforced + k] = w.idx;
+    if ((w.idx & 31) == lane) {
+      taken[w.idx] = 1;
+      mine = local_best();
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    ids[0] = r;
+    if (sink) ids[1] = 0;
+  }
+  __syncwarp();
+  const int cnt = nforced + k_dyn;
+  // Rank sort (ids are distinct) into ascending order.
+  for (int e = lane; e < k_max; e += 32) {
+    if (e < cnt) {
+      const int v = ids[e];
+      int rank = 0;
+      for (int f = 0; f < cnt; ++f) rank += ids[f] < v ? 1 : 0;
+      Jrow[rank] = v;
+    } else {
+      Jrow[e] = -1;
+    }
+  }
+  if (lane == 0) counts[row] = cnt;
+}
+
+}  // namespace
+
+size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &) {
+  return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * s.max_blocks * sizeof(float);
+}
+
+cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
+                         const float *C, int32_t *J, int32_t *counts, float *scores,
+                         int32_t *dev_status, void *ws, cudaStream_t st) {
+  (void)dev_status;
+  float *S = scores != nullptr ? scores : static_cast<float *>(ws);
+  const int G = s.num_heads / s.num_kv_heads;
+  const dim3 grid(s.max_blocks, s.num_kv_heads, s.num_seqs);
+  if (s.dtype == BSA_BF16)
+    route_scores_kernel<uint16_t><<<grid, kThreads, 0, st>>>(
+        static_cast<const uint16_t *>(Q), C, s.cu_seqlens, S, s.total_tokens, s.max_blocks,
+        s.num_kv_heads, G, s.head_dim, s.block);
+  else
+    route_scores_kernel<float><<<grid, kThreads, 0, st>>>(
+        static_cast<const float *>(Q), C, s.cu_seqlens, S, s.total_tokens, s.max_blocks,
+        s.num_kv_heads, G, s.head_dim, s.block);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows = s.num_seqs * s.num_kv_heads * s.max_blocks;
+  const size_t sm = (size_t)s.max_blocks * 5 + (size_t)(p.k_max + 2) * 4 + 16;
+  if (sm > 48 * 1024) {
+    e = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  route_select_kernel<<<rows, 32, sm, st>>>(S, s.cu_seqlens, J, counts, s.max_blocks,
+                                            s.num_kv_heads, s.block, p.mode, p.k_max, p.k_min,
+                                            p.tau_delta, p.force_sink);
+  return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -1,0 +1,127 @@
+// a1: mean-pooled block summaries ("2.1 · 粗粒度选择" §2.1 eq.(6), with the
+// valid-key divisor r_j of eq.(11)), and the same mean over the pages of a paged
+// KV cache.  Both are HBM-bound: every key is read once with 16-byte loads and
+// each CTA writes one d-vector of fp32.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsa {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<uint16_t> {  // 8 bf16
+  static constexpr int kElems = 8;
+  BSA_DEV static void add(const uint4 &v, float *acc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc[2 * e] += __uint_as_float(w[e] << 16);
+      acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+};
+template <>
+struct Vec16<float> {  // 4 fp32
+  static constexpr int kElems = 4;
+  BSA_DEV static void add(const uint4 &v, float *acc) {
+    acc[0] += __uint_as_float(v.x);
+    acc[1] += __uint_as_float(v.y);
+    acc[2] += __uint_as_float(v.z);
+    acc[3] += __uint_as_float(v.w);
+  }
+};
+
+// Mean over `nrows` rows (row stride `stride` elements) of a d-wide slab; the
+// CTA's threads split rows x 16-byte vectors, then reduce through shared memory.
+template <typename T>
+BSA_DEV void block_mean(const T *__restrict__ base, int nrows, long long stride, int d,
+                        float *__restrict__ out, float *red) {
+  constexpr int E = Vec16<T>::kElems;
+  const int vecs = d / E;             // 16-byte vectors per row
+  const int rgroups = kThreads / vecs;
+  const int vec = threadIdx.x % vecs;
+  const int rg = threadIdx.x / vecs;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int row = rg; row < nrows; row += rgroups) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(base + row * stride) + vec);
+    Vec16<T>::add(v, acc);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) red[rg * d + vec * E + e] = acc[e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < d; c += kThreads) {
+    float s = 0.f;
+    for (int g = 0; g < rgroups; ++g) s += red[g * d + c];
+    out[c] = nrows > 0 ? s / (float)nrows : 0.f;
+  }
+}
+
+// grid (N_q, B, H_kv): one CTA per (block j, sequence i, KV head h).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) block_summaries_kernel(
+    const T *__restrict__ K, const int32_t *__restrict__ cu, float *__restrict__ C, int T_tok,
+    int Nq, int Hk, int d, int b) {
+  extern __shared__ float red[];
+  const int j = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
+  const int s0 = cu[i], n = cu[i + 1] - s0;
+  const int lo = j * b;
+  const int nrows = max(0, min(b, n - lo));
+  float *out = C + (((size_t)i * Hk + h) * Nq + j) * d;
+  const T *base = K + ((size_t)h * T_tok + s0 + lo) * d;
+  block_mean<T>(base, nrows, d, d, out, red);
+}
+
+// grid (max_pages_per_req, R, H_kv): one CTA per (logical page p, request, KV head).
+__global__ void __launch_bounds__(kThreads) page_summaries_kernel(
+    const uint16_t *__restrict__ kc, const int32_t *__restrict__ bt,
+    const int32_t *__restrict__ lens, float *__restrict__ ps, int max_pages, int Hk, int page,
+    int d) {
+  extern __shared__ float red[];
+  const int p = blockIdx.x, rho = blockIdx.y, h = blockIdx.z;
+  const int n = lens[rho];
+  const int lo = p * page;
+  if (lo >= n) return;
+  const int nrows = min(page, n - lo);
+  const int phys = bt[(size_t)rho * max_pages + p];
+  const uint16_t *base = kc + (((size_t)phys * Hk + h) * page) * d;
+  block_mean<uint16_t>(base, nrows, d, d, ps + ((size_t)phys * Hk + h) * d, red);
+}
+
+}  // namespace
+
+cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
+                                   cudaStream_t st) {
+  const dim3 grid(s.max_blocks, s.num_seqs, s.num_kv_heads);
+  if (s.dtype == BSA_BF16) {
+    const size_t sm = (size_t)(kThreads / (s.head_dim / 8)) * s.head_dim * sizeof(float);
+    block_summaries_kernel<uint16_t><<<grid, kThreads, sm, st>>>(
+        static_cast<const uint16_t *>(K), s.cu_seqlens, C, s.total_tokens, s.max_blocks,
+        s.num_kv_heads, s.head_dim, s.block);
+  } else {
+    const size_t sm = (size_t)(kThreads / (s.head_dim / 4)) * s.head_dim * sizeof(float);
+    block_summaries_kernel<float><<<grid, kThreads, sm, st>>>(
+        static_cast<const float *>(K), s.cu_seqlens, C, s.total_tokens, s.max_blocks,
+        s.num_kv_heads, s.head_dim, s.block);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_page_summaries(const bsa_decode_shape_t &s, const void *k_cache,
+                                  const int32_t *block_table, const int32_t *context_lens,
+                                  float *page_summ, cudaStream_t st) {
+  const dim3 grid(s.max_pages_per_req, s.num_reqs, s.num_kv_heads);
+  const size_t sm = (size_t)(kThreads / (s.head_dim / 8)) * s.head_dim * sizeof(float);
+  page_summaries_kernel<<<grid, kThreads, sm, st>>>(
+      static_cast<const uint16_t *>(k_cache), block_table, context_lens, page_summ,
+      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -1,0 +1,187 @@
+// a4: J -> CSR worklist ("2.1 · 粗粒度选择" §3.1 index representations: the fixed
+// table J and the CSR row_ptr / col_idx form; PaperTrace 5-1 "从索引输出到工作表":
+// rows grouped into length buckets and handed to one persistent launch).
+//   1. rows kernel   validates each row and records its length (grid-wide)
+//   2. scan kernel   row_ptr by prefix sum, and the work list: a stable counting
+//                    sort of rows by capacity bucket, largest first (one CTA)
+//   3. fill kernel   copies the block ids into col_idx (grid-wide)
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsa {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// Row code: 0 = not a row (past the sequence end); c > 0 = copy c ids from J;
+// -1 = the row holds only its diagonal block (empty row, or a malformed row).
+__global__ void wl_rows_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ counts,
+                               const int32_t *__restrict__ cu, int32_t *__restrict__ code,
+                               int32_t *dev_status, int nrows, int Nq, int Hk, int b, int k_max) {
+  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
+       row += gridDim.x * blockDim.x) {
+    const int r = row % Nq, i = row / (Nq * Hk);
+    const int n = cu[i + 1] - cu[i];
+    const int nb = (n + b - 1) / b;
+    if (r >= nb) {
+      code[row] = 0;
+      continue;
+    }
+    const int c = counts[row];
+    if (c < 0 || c > k_max) {
+      set_status(dev_status, BSA_ERR_COUNT);
+      code[row] = -1;
+      continue;
+    }
+    if (c == 0) {
+      code[row] = -1;
+      continue;
+    }
+    const int32_t *Jr = J + (size_t)row * k_max;
+    int prev = -1, err = 0;
+    for (int e = 0; e < c; ++e) {
+      const int v = Jr[e];
+      if (v < 0 || v > r) {
+        err = BSA_ERR_INDEX_RANGE;
+        break;
+      }
+      if (v <= prev) {
+        err = BSA_ERR_INDEX_ORDER;
+        break;
+      }
+      prev = v;
+    }
+    if (err) set_status(dev_status, err);
+    code[row] = err ? -1 : c;
+  }
+}
+
+BSA_DEV int bucket_of(int len) {  // capacity max(4, pow2 >= len): 256 -> 0, ..., 4 -> 6
+  int cap = 4, s = 6;
+  while (cap < len && s > 0) {
+    cap <<= 1;
+    --s;
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(kScanThreads) wl_scan_kernel(
+    const int32_t *__restrict__ code, int32_t *__restrict__ row_ptr, int32_t *__restrict__ work,
+    int32_t *__restrict__ bucket_off, int nrows) {
+  __shared__ int32_t hist[BSA_NUM_BUCKETS][kScanThreads];
+  __shared__ int32_t lsum[kScanThreads];
+  __shared__ int32_t btot[BSA_NUM_BUCKETS + 1];
+  const int t = threadIdx.x;
+  const int chunk = (nrows + kScanThreads - 1) / kScanThreads;
+  const int lo = min(nrows, t * chunk), hi = min(nrows, lo + chunk);
+  int sum = 0;
+  int h[BSA_NUM_BUCKETS];
+#pragma unroll
+  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) h[s] = 0;
+  for (int row = lo; row < hi; ++row) {
+    const int c = code[row];
+    const int len = c < 0 ? 1 : c;
+    sum += len;
+    if (len > 0) {
+      const int s = bucket_of(len);
+#pragma unroll
+      for (int q = 0; q < BSA_NUM_BUCKETS; ++q) h[q] += (q == s) ? 1 : 0;
+    }
+  }
+  lsum[t] = sum;
+#pragma unroll
+  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) hist[s][t] = h[s];
+  __syncthreads();
+  // Exclusive scans: lengths over threads, and bucket counts over (bucket, thread).
+  if (t == 0) {
+    int acc = 0;
+    for (int k = 0; k < kScanThreads; ++k) {
+      const int v = lsum[k];
+      lsum[k] = acc;
+      acc += v;
+    }
+    row_ptr[nrows] = acc;
+  }
+  if (t >= 32 && t < 32 + BSA_NUM_BUCKETS) {
+    const int s = t - 32;
+    int acc = 0;
+    for (int k = 0; k < kScanThreads; ++k) {
+      const int v = hist[s][k];
+      hist[s][k] = acc;
+      acc += v;
+    }
+    btot[s] = acc;
+  }
+  __syncthreads();
+  if (t == 0) {
+    int acc = 0;
+    for (int s = 0; s < BSA_NUM_BUCKETS; ++s) {
+      bucket_off[s] = acc;
+      const int v = btot[s];
+      btot[s] = acc;
+      acc += v;
+    }
+    bucket_off[BSA_NUM_BUCKETS] = acc;
+  }
+  __syncthreads();
+  int off = lsum[t];
+  int pos[BSA_NUM_BUCKETS];
+#pragma unroll
+  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) pos[s] = btot[s] + hist[s][t];
+  for (int row = lo; row < hi; ++row) {
+    const int c = code[row];
+    const int len = c < 0 ? 1 : c;
+    row_ptr[row] = off;
+    off += len;
+    if (len > 0) {
+      const int s = bucket_of(len);
+#pragma unroll
+      for (int q = 0; q < BSA_NUM_BUCKETS; ++q)
+        if (q == s) work[pos[q]++] = row;
+    }
+  }
+}
+
+__global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ code,
+                               const int32_t *__restrict__ row_ptr, int32_t *__restrict__ col_idx,
+                               int nrows, int Nq, int k_max) {
+  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
+       row += gridDim.x * blockDim.x) {
+    const int c = code[row];
+    if (c == 0) continue;
+    int32_t *out = col_idx + row_ptr[row];
+    if (c < 0) {
+      out[0] = row % Nq;
+      continue;
+    }
+    const int32_t *Jr = J + (size_t)row * k_max;
+    for (int e = 0; e < c; ++e) out[e] = Jr[e];
+  }
+}
+
+}  // namespace
+
+size_t worklist_workspace_bytes(const bsa_shape_t &s, int32_t) {
+  return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * sizeof(int32_t);
+}
+
+cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *J,
+                            const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
+                            int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
+                            cudaStream_t st) {
+  const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
+  int32_t *code = static_cast<int32_t *>(ws);
+  const int blocks = min(4 * num_sms(), (nrows + 255) / 256);
+  wl_rows_kernel<<<max(blocks, 1), 256, 0, st>>>(J, counts, s.cu_seqlens, code, dev_status, nrows,
+                                                 s.max_blocks, s.num_kv_heads, s.block, k_max);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wl_scan_kernel<<<1, kScanThreads, 0, st>>>(code, row_ptr, work, bucket_off, nrows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wl_fill_kernel<<<max(blocks, 1), 256, 0, st>>>(J, code, row_ptr, col_idx, nrows, s.max_blocks,
+                                                 k_max);
+  return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -1,0 +1,237 @@
+/*
+ * bsa.h — C ABI of libbsa.so: dynamic block-sparse attention with a mean-pooled
+ * block router, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the coarse-grained dynamic selection of
+ * "2.1 · 粗粒度选择: 从内容分组到动态稀疏块" (PaperTrace, sparse-attention 2-1),
+ * cited below as [P2], with the worklist / kernel rules of PaperTrace
+ * sparse-attention 5-1 ("从索引输出到工作表", "稀疏 softmax 仍要保持数值一致"),
+ * cited as [P3].
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless it
+ *    is a pointer to one of the descriptor structs below (host memory, read
+ *    during the call only).  The library never frees, retains or reallocates a
+ *    caller buffer and keeps no pointer after the call returns.
+ *  - Every call enqueues its kernels on `stream` and returns without
+ *    synchronising.  Outputs are valid once the caller's stream has passed them.
+ *  - Scratch memory comes from the caller through `ws` / `ws_bytes`, sized by the
+ *    matching *_workspace_size() query; the library itself never allocates
+ *    device memory.
+ *  - Host-detectable errors (null pointers, unsupported sizes, a workspace that
+ *    is too small) return a non-zero status BEFORE anything is enqueued.
+ *  - Device-detected errors (malformed index rows, a bounded wait that ran out)
+ *    are written to the caller's `int32_t *dev_status` (set it to 0 first);
+ *    the first error wins.  The caller reads it after its own synchronisation.
+ *    The outputs of a failing row are then unspecified.  No kernel traps.
+ *  - Layouts are head-major and packed: Q and O are [H, T, d], K and V are
+ *    [H_kv, T, d] with T = sum of the sequence lengths; sequence i owns tokens
+ *    cu_seqlens[i] .. cu_seqlens[i+1]-1.  [P2] section 1 states the same tensors
+ *    as B x H x n x d_h; a fixed-length batch is the case cu_seqlens[i] = i n.
+ *  - Block ids in J, col_idx and sel are sequence-relative logical ids ([P2]
+ *    §2.1 on packed sequences; §3.1 on logical ids mapped by a block table).
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BSA_VERSION 1
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = 1,   /* null pointer, inconsistent sizes          (host) */
+  BSA_ERR_UNSUPPORTED = 2,   /* head_dim / block / dtype / k_max not built (host) */
+  BSA_ERR_WORKSPACE = 3,     /* ws_bytes below the *_workspace_size value  (host) */
+  BSA_ERR_LAUNCH = 4,        /* a kernel launch returned an error          (host) */
+  BSA_ERR_INDEX_RANGE = 16,  /* a J entry outside [0, r]                 (device) */
+  BSA_ERR_INDEX_ORDER = 17,  /* a J row not strictly increasing          (device) */
+  BSA_ERR_COUNT = 18,        /* counts[row] outside [0, k_max]           (device) */
+  BSA_ERR_TIMEOUT = 19       /* a bounded barrier wait ran out           (device) */
+} bsa_status_t;
+
+typedef enum { BSA_BF16 = 0, BSA_FP32 = 1 } bsa_dtype_t;
+
+enum { BSA_ROUTE_TOPK = 0, BSA_ROUTE_THRESHOLD = 1 };
+
+/* Number of capacity buckets of the work list (4, 8, 16, 32, 64, 128, 256). */
+#define BSA_NUM_BUCKETS 7
+/* Largest supported row capacity k_max. */
+#define BSA_MAX_K 256
+
+/* Shape of a packed prefill batch ([P2] section 1, problem statement). */
+typedef struct {
+  int32_t num_seqs;          /* B                                              */
+  int32_t total_tokens;      /* T = cu_seqlens[B]                              */
+  int32_t max_seqlen;        /* max_i n_i                                      */
+  int32_t num_heads;         /* H query heads                                  */
+  int32_t num_kv_heads;      /* H_kv; H % H_kv == 0, G = H / H_kv (GQA)        */
+  int32_t head_dim;          /* d_h: 64 or 128                                 */
+  int32_t block;             /* b = b_q = b_k: 64 or 128                       */
+  int32_t max_blocks;        /* N_q = ceil(max_seqlen / block)                 */
+  bsa_dtype_t dtype;         /* element type of Q, K, V, O                     */
+  const int32_t *cu_seqlens; /* device [B + 1], non-decreasing, cu[0] = 0      */
+} bsa_shape_t;
+
+/* Router parameters ([P2] §2.1 "top-k, threshold and capacity", eq.(7)). */
+typedef struct {
+  int32_t mode;       /* BSA_ROUTE_TOPK or BSA_ROUTE_THRESHOLD                      */
+  int32_t k_max;      /* row capacity of J, forced blocks included; 1 .. BSA_MAX_K  */
+  int32_t k_min;      /* threshold mode: lower clamp of eq.(7)                      */
+  float tau_delta;    /* threshold mode: tau_r = (max candidate score) - tau_delta   */
+  int32_t force_sink; /* non-zero: block 0 is always kept (a global sink block)      */
+} bsa_route_params_t;
+
+/* Paged decode shape ([P2] §2.2 decode; §3.1 paged KV cache and block table). */
+typedef struct {
+  int32_t num_reqs;          /* R requests, one query token each                 */
+  int32_t num_heads;         /* H                                                */
+  int32_t num_kv_heads;      /* H_kv, H % H_kv == 0                              */
+  int32_t head_dim;          /* 128                                              */
+  int32_t page_size;         /* tokens per page = routing block: 64              */
+  int32_t max_pages_per_req; /* columns of block_table                           */
+  int32_t num_phys_pages;    /* P, rows of the caches and of page_summ           */
+  int32_t top_k;             /* dynamic pages per (request, KV head), 1 .. 64    */
+} bsa_decode_shape_t;
+
+/* ---------------------------------------------------------------------------
+ * a1. Block summaries — [P2] §2.1 eq.(6), mean-pooled key summary
+ *     c_j = (1 / r_j) sum of the keys of block j, where r_j is the number of
+ *     keys the block holds (eq.(11)): a partial tail block averages its valid
+ *     keys only, padding never enters ([P2] §4.1).
+ *   K : [H_kv, T, d] of shape->dtype.
+ *   C : [B, H_kv, N_q, d] fp32, written for every block j < ceil(n_i / b);
+ *       entries of blocks past a sequence's end are set to 0.
+ * ------------------------------------------------------------------------- */
+bsa_status_t bsa_block_summaries(const bsa_shape_t *shape, const void *K, float *C,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a2 + a3. Router — [P2] §2.1 eq.(6) scores, eq.(7) selection.
+ *   score g[i,h,r,j] = max over the G query heads of KV head h and over the
+ *   valid query tokens t of block r of  Q[hq, t] . C[i, h, j],  for j < r
+ *   (unscaled; GQA candidates are shared per KV head, [P2] §4).
+ *   Forced blocks: the diagonal r always (the triangle branch of [P2] §2.1),
+ *   block 0 too when force_sink; they are not dynamic candidates.
+ *   TOPK: keep the forced blocks plus the best k_max - |forced| candidates.
+ *   THRESHOLD: tau_r = max candidate score - tau_delta; with A the candidates
+ *   scoring >= tau_r, k_r = min(k_max, max(k_min, |forced| + |A|),
+ *   |forced| + |candidates|); keep forced plus the best k_r - |forced|.
+ *   Ranking is (score descending, block index ascending).  Each row of J is
+ *   deduplicated and sorted ascending ([P2] §1.2 eq.(1) address order).
+ *   Q      : [H, T, d] of shape->dtype.     C : [B, H_kv, N_q, d] fp32.
+ *   J      : [B, H_kv, N_q, k_max] int32, -1 past counts.
+ *   counts : [B, H_kv, N_q] int32; 0 for rows r >= ceil(n_i / b).
+ *   scores : nullable; if given, [B, H_kv, N_q, N_q] fp32 receives g for j < r
+ *            (other entries unspecified) — a debugging output.
+ *   ws     : at least bsa_route_workspace_size() bytes, 256-byte aligned.
+ *   dev_status : see conventions.
+ * ------------------------------------------------------------------------- */
+size_t bsa_route_workspace_size(const bsa_shape_t *shape, const bsa_route_params_t *params);
+bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *params,
+                       const void *Q, const float *C, int32_t *J, int32_t *counts,
+                       float *scores, int32_t *dev_status, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a4. Worklist — [P2] §3.1 index representations (fixed J -> CSR row_ptr /
+ *     col_idx); [P3] "从索引输出到工作表" (length buckets, persistent kernel).
+ *   Validates every row r < ceil(n_i / b): counts in [0, k_max]
+ *   (BSA_ERR_COUNT), entries in [0, r] (BSA_ERR_INDEX_RANGE), strictly
+ *   increasing (BSA_ERR_INDEX_ORDER, which also rejects duplicates: a block
+ *   may enter the softmax only once, [P2] §1.2).  An empty row is replaced by
+ *   its diagonal block {r} ([P3] sparse-softmax section: empty rows fall back to
+ *   the self block).
+ *   row_ptr    : [B * H_kv * N_q + 1] int32, CSR offsets; rows past a
+ *                sequence's end are empty.
+ *   col_idx    : [B * H_kv * N_q * k_max] int32 capacity, CSR block ids.
+ *   work       : [B * H_kv * N_q] int32 capacity: flattened row ids
+ *                (i * H_kv + h) * N_q + r, grouped by capacity bucket, largest
+ *                first (longest rows first), row-id order inside a bucket.
+ *   bucket_off : [BSA_NUM_BUCKETS + 1] int32: rows of capacity 256 >> s occupy
+ *                work[bucket_off[s] .. bucket_off[s+1]); bucket_off[7] is the
+ *                number of rows.  A row's capacity is max(4, next power of 2
+ *                of its length).
+ * ------------------------------------------------------------------------- */
+size_t bsa_worklist_workspace_size(const bsa_shape_t *shape, int32_t k_max);
+bsa_status_t bsa_build_worklist(const bsa_shape_t *shape, int32_t k_max, const int32_t *J,
+                                const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
+                                int32_t *work, int32_t *bucket_off, int32_t *dev_status,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a5. Sparse attention forward — [P2] §1.2 eqs.(1)-(5): for each row listed
+ *   in `work` and every query head of its group, exact S = Q_r K_j^T * scale
+ *   on the selected tiles only (eq.(2)), the causal mask s <= t inside the
+ *   diagonal tile and the tail mask s < n_i applied before the softmax, tiles
+ *   merged with the online-softmax recurrences (3)-(5), O = u / l.
+ *   BF16 runs on the tensor cores (tcgen05, TMEM accumulators); FP32 is a
+ *   SIMT correctness path.
+ *   softmax_scale : <= 0 selects 1 / sqrt(d).
+ *   O   : [H, T, d] of shape->dtype; rows of valid query tokens are written.
+ *   lse : [H, T] fp32 natural-log logsumexp of the scaled scores (nullable).
+ *   row_ptr / col_idx / work / bucket_off : as produced by bsa_build_worklist.
+ * ------------------------------------------------------------------------- */
+bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const void *K,
+                               const void *V, const int32_t *row_ptr, const int32_t *col_idx,
+                               const int32_t *work, const int32_t *bucket_off,
+                               float softmax_scale, void *O, float *lse, int32_t *dev_status,
+                               cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Page summaries for decode — [P2] §3.1 "block summaries are cache state",
+ *   eq.(11): the mean of the keys each page holds.  For request rho and logical
+ *   page p < ceil(len / page_size), page_summ[block_table[rho][p], h, :] =
+ *   mean of the valid keys of that page.  Pages no request references are
+ *   left untouched.
+ *   k_cache     : [P, H_kv, page_size, d] bf16.
+ *   block_table : [R, max_pages_per_req] int32 physical page ids.
+ *   context_lens: [R] int32, 1 .. max_pages_per_req * page_size.
+ *   page_summ   : [P, H_kv, d] fp32.
+ * ------------------------------------------------------------------------- */
+bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_cache,
+                                const int32_t *block_table, const int32_t *context_lens,
+                                float *page_summ, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a6. Paged sparse decode — [P2] §2.2 (decode reads the summaries, O(N_k d_r),
+ *   then only the selected K/V) and §3.1 (the router emits logical page ids
+ *   that the block table maps to physical pages at attention time).
+ *   For request rho (L = ceil(len / page_size) logical pages) and KV head h:
+ *   pages 0 .. L-2 are scored by max over the group's query heads of
+ *   q . page_summ[phys(p), h]; the best top_k (score desc, index asc) plus the
+ *   last page L-1 are kept, ascending, in sel; the softmax (scale, default
+ *   1/sqrt(d)) runs over the valid tokens of the kept pages.
+ *   q        : [R, H, d] bf16.          k_cache, v_cache : [P, H_kv, page, d] bf16.
+ *   page_summ: [P, H_kv, d] fp32.       block_table, context_lens as above.
+ *   o        : [R, H, d] bf16.          lse : [R, H] fp32 (nullable).
+ *   sel      : [R, H_kv, top_k + 1] int32 logical pages, -1 padded.
+ *   sel_counts : [R, H_kv] int32.
+ *   ws       : at least bsa_decode_workspace_size() bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+size_t bsa_decode_workspace_size(const bsa_decode_shape_t *shape);
+bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
+                              const void *k_cache, const void *v_cache,
+                              const float *page_summ, const int32_t *block_table,
+                              const int32_t *context_lens, float softmax_scale, void *o,
+                              float *lse, int32_t *sel, int32_t *sel_counts,
+                              int32_t *dev_status, void *ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *bsa_status_string(bsa_status_t status);
+
+/* BSA_VERSION of the built library. */
+int32_t bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSA_H_ */

@@ -66,6 +66,12 @@ THRESHOLD = 1
 # helpers
 # ----------------------------------------------------------------------------
 
+def _f64(x):
+    """A slice of an input as float64 (inputs may be any array-like that
+    returns real values when indexed; conversion happens per slice)."""
+    return np.asarray(x, dtype=np.float64)
+
+
 def seq_info(cu_seqlens, b: int):
     """(start, length, number of blocks) per sequence; blocks are ceil(n / b)
     ([P2] section 1 opening: N_q = ceil(n / b))."""
@@ -100,7 +106,6 @@ def block_summaries(K, cu_seqlens, b: int):
     block averages its valid keys only and padding never enters ([P2] §4.1).
     Returns C [B, H_kv, N_q, d]; blocks past a sequence's end are zero.
     """
-    K = np.asarray(K, dtype=np.float64)
     Hk, _, d = K.shape
     info = seq_info(cu_seqlens, b)
     Nq = max((nb for _, _, nb in info), default=0)
@@ -108,7 +113,7 @@ def block_summaries(K, cu_seqlens, b: int):
     for i, (s0, n, nb) in enumerate(info):
         for j in range(nb):
             lo, hi = s0 + j * b, s0 + min(n, (j + 1) * b)
-            C[i, :, j, :] = K[:, lo:hi, :].sum(axis=1) / (hi - lo)
+            C[i, :, j, :] = _f64(K[:, lo:hi, :]).sum(axis=1) / (hi - lo)
     return C
 
 
@@ -137,7 +142,6 @@ def route_scores(Q, C, cu_seqlens, b: int, G: int, rows=None):
     block rule; §4.1, a summary never holds keys the query cannot see).
     `rows`, if given, is an iterable of (i, h, r) to compute.
     """
-    Q = np.asarray(Q, dtype=np.float64)
     info = seq_info(cu_seqlens, b)
     B, Hk, Nq, d = C.shape
     g = np.full((B, Hk, Nq, Nq), -np.inf)
@@ -147,7 +151,7 @@ def route_scores(Q, C, cu_seqlens, b: int, G: int, rows=None):
         s0, n, nb = info[i]
         if r == 0 or r >= nb:
             continue
-        qr = Q[h * G:(h + 1) * G, s0 + r * b: s0 + min(n, (r + 1) * b), :].reshape(-1, d)
+        qr = _f64(Q[h * G:(h + 1) * G, s0 + r * b: s0 + min(n, (r + 1) * b), :]).reshape(-1, d)
         g[i, h, r, :r] = (qr @ C[i, h, :r, :].T).max(axis=0)
     return g
 
@@ -264,12 +268,7 @@ def attention_rows(Q, K, V, cu_seqlens, b: int, G: int, J, counts, rows, scale=N
     masks before softmax; §4.1 token-level triangle in the diagonal block), and
     O = softmax(S) V, lse = logsumexp(S) (R-9).
     """
-    Q = np.asarray(Q, dtype=np.float64)
-    K = np.asarray(K, dtype=np.float64)
-    V = np.asarray(V, dtype=np.float64)
     H, T, d = Q.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if O is None:
         O = np.full((H, T, d), np.nan)
     if lse is None:
@@ -279,21 +278,40 @@ def attention_rows(Q, K, V, cu_seqlens, b: int, G: int, J, counts, rows, scale=N
         s0, n, nb = info[i]
         if r >= nb:
             continue
-        cnt = int(counts[i, h, r])
-        mult = block_multiplicity(J[i, h, r, :cnt], nb, r, multiset)
+        Ob, lb = attention_row(Q, K, V, cu_seqlens, b, G, J, counts, (i, h, r), scale, multiset)
         q_lo, q_hi = r * b, min(n, (r + 1) * b)
-        wkey = mult[np.arange(q_hi) // b]
-        allowed = key_mask(q_lo, q_hi, mult, b)
-        Kp, Vp = K[h, s0:s0 + q_hi], V[h, s0:s0 + q_hi]
-        for hq in range(h * G, (h + 1) * G):
-            S = (Q[hq, s0 + q_lo:s0 + q_hi] @ Kp.T) * scale
-            S = np.where(allowed, S, -np.inf)
-            m = S.max(axis=1, keepdims=True)
-            E = wkey[None, :] * np.exp(S - m)
-            l = E.sum(axis=1, keepdims=True)
-            O[hq, s0 + q_lo:s0 + q_hi] = (E @ Vp) / l
-            lse[hq, s0 + q_lo:s0 + q_hi] = (m + np.log(l))[:, 0]
+        O[h * G:(h + 1) * G, s0 + q_lo:s0 + q_hi] = Ob
+        lse[h * G:(h + 1) * G, s0 + q_lo:s0 + q_hi] = lb
     return O, lse
+
+
+def attention_row(Q, K, V, cu_seqlens, b: int, G: int, J, counts, row, scale=None,
+                  multiset: bool = False):
+    """One router row (i, h_kv, r): returns O [G, n_r, d] and lse [G, n_r] for the
+    group's query heads and the n_r valid query tokens of block r (same
+    definition as attention_rows)."""
+    i, h, r = row
+    d = Q.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s0, n, nb = seq_info(cu_seqlens, b)[i]
+    cnt = int(counts[i, h, r])
+    mult = block_multiplicity(J[i, h, r, :cnt], nb, r, multiset)
+    q_lo, q_hi = r * b, min(n, (r + 1) * b)
+    wkey = mult[np.arange(q_hi) // b]
+    allowed = key_mask(q_lo, q_hi, mult, b)
+    Kp, Vp = _f64(K[h, s0:s0 + q_hi]), _f64(V[h, s0:s0 + q_hi])
+    Ob = np.empty((G, q_hi - q_lo, d))
+    lb = np.empty((G, q_hi - q_lo))
+    for g, hq in enumerate(range(h * G, (h + 1) * G)):
+        S = (_f64(Q[hq, s0 + q_lo:s0 + q_hi]) @ Kp.T) * scale
+        S = np.where(allowed, S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        E = wkey[None, :] * np.exp(S - m)
+        l = E.sum(axis=1, keepdims=True)
+        Ob[g] = (E @ Vp) / l
+        lb[g] = (m + np.log(l))[:, 0]
+    return Ob, lb
 
 
 def all_rows(cu_seqlens, b: int, Hk: int):
@@ -303,7 +321,7 @@ def all_rows(cu_seqlens, b: int, Hk: int):
 
 def attention(Q, K, V, cu_seqlens, b: int, G: int, J, counts, scale=None, rows=None,
               multiset: bool = False):
-    Hk = np.asarray(K).shape[0]
+    Hk = K.shape[0]
     if rows is None:
         rows = all_rows(cu_seqlens, b, Hk)
     return attention_rows(Q, K, V, cu_seqlens, b, G, J, counts, rows, scale, multiset)
@@ -393,7 +411,7 @@ def causal_visibility(pos: int, b: int):
 # ----------------------------------------------------------------------------
 
 def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int,
-           scale=None, reqs=None):
+           scale=None, reqs=None, return_scores: bool = False):
     """Paged single-token decode with the same router.
 
     For request rho and KV head h: L = ceil(len / page) logical pages; the
@@ -404,7 +422,8 @@ def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int
     §3.1 paged KV: the router emits monotone logical ids, the block table maps
     them at attention time); softmax over the selected pages' valid tokens.
     Decode cost is reading the summaries plus the selected K/V ([P2] §2.2).
-    Returns o [R, H, d], lse [R, H], sel [R, H_kv, top_k + 1] (-1 padded), counts.
+    Returns o [R, H, d], lse [R, H], sel [R, H_kv, top_k + 1] (-1 padded), counts,
+    and with return_scores a dict {(rho, h): page scores} as a fifth value.
     """
     q = np.asarray(q, dtype=np.float64)
     R, H, d = q.shape
@@ -416,6 +435,7 @@ def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int
     lse = np.full((R, H), np.nan)
     sel = np.full((R, Hk, top_k + 1), -1, dtype=np.int64)
     cnt = np.zeros((R, Hk), dtype=np.int64)
+    scores = {}
     if reqs is None:
         reqs = range(R)
     for rho in reqs:
@@ -423,15 +443,17 @@ def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int
         L = (n + page - 1) // page
         phys = np.asarray(block_table[rho, :L], dtype=np.int64)
         for h in range(Hk):
-            Kl = np.asarray(k_cache[phys, h], dtype=np.float64).reshape(L * page, d)[:n]
-            Vl = np.asarray(v_cache[phys, h], dtype=np.float64).reshape(L * page, d)[:n]
+            Kl = _f64(k_cache[phys, h]).reshape(L * page, d)[:n]
+            Vl = _f64(v_cache[phys, h]).reshape(L * page, d)[:n]
             qg = q[rho, h * G:(h + 1) * G]
             if L > 1:
                 c = Kl[:(L - 1) * page].reshape(L - 1, page, d).mean(axis=1)
                 gsc = (qg @ c.T).max(axis=0)
                 chosen = [int(x) for x in rank_order(gsc, np.arange(L - 1))[:top_k]]
             else:
+                gsc = np.zeros(0)
                 chosen = []
+            scores[(rho, h)] = gsc
             ids = sorted(set(chosen) | {L - 1})
             sel[rho, h, :len(ids)] = ids
             cnt[rho, h] = len(ids)
@@ -442,6 +464,8 @@ def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int
             l = E.sum(axis=1, keepdims=True)
             o[rho, h * G:(h + 1) * G] = (E @ Vl[keys]) / l
             lse[rho, h * G:(h + 1) * G] = (m + np.log(l))[:, 0]
+    if return_scores:
+        return o, lse, sel, cnt, scores
     return o, lse, sel, cnt
 
 

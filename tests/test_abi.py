@@ -1,0 +1,91 @@
+"""The C-ABI library loads, exports every entry point include/bsa.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dynamic_block_sparse_mean_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from dynamic_block_sparse_mean_gb300 import build
+        build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared()
+    for n in ("bsa_block_summaries", "bsa_route", "bsa_build_worklist", "bsa_attention_fwd",
+              "bsa_decode_paged", "bsa_page_summaries", "bsa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(_lib.PROTOTYPES), "binding prototypes cover the header"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.bsa_version() == 1
+    for code in _lib.STATUS_NAMES:
+        assert lib.bsa_status_string(code)
+
+
+def _shape(**kw):
+    base = dict(num_seqs=1, total_tokens=1024, max_seqlen=1024, num_heads=2, num_kv_heads=2,
+                head_dim=64, block=64, max_blocks=16, dtype=0, cu_seqlens=0x1000)
+    base.update(kw)
+    return _lib.Shape(**base)
+
+
+def test_host_side_argument_errors(lib):
+    null = None
+    s = _shape()
+    bad = _shape(cu_seqlens=None)
+    assert lib.bsa_block_summaries(ctypes.byref(bad), ctypes.c_void_p(16), ctypes.c_void_p(16), null) == 1
+    assert lib.bsa_block_summaries(ctypes.byref(s), null, ctypes.c_void_p(16), null) == 1
+    assert lib.bsa_block_summaries(ctypes.byref(_shape(max_blocks=15)), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), null) == 1
+    assert lib.bsa_block_summaries(ctypes.byref(_shape(head_dim=96)), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), null) == 2
+    assert lib.bsa_block_summaries(ctypes.byref(_shape(num_heads=3)), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), null) == 1
+    p = _lib.RouteParams(0, 300, 0, 0.0, 0)
+    args = [ctypes.c_void_p(16)] * 4
+    assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 2
+    p = _lib.RouteParams(0, 4, 0, 0.0, 0)
+    assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 3
+    p = _lib.RouteParams(5, 4, 0, 0.0, 0)
+    assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 1
+    assert lib.bsa_route_workspace_size(ctypes.byref(s), ctypes.byref(p)) == 1 * 2 * 16 * 16 * 4
+    wl = [ctypes.c_void_p(16)] * 7
+    assert lib.bsa_build_worklist(ctypes.byref(s), 4, *wl, null, 0, null) == 3
+    assert lib.bsa_build_worklist(ctypes.byref(s), 0, *wl, null, 0, null) == 2
+    a = [ctypes.c_void_p(16)] * 7
+    assert lib.bsa_attention_fwd(ctypes.byref(s), *a, ctypes.c_float(0.0), ctypes.c_void_p(16),
+                                 null, null, null) == 1          # dev_status missing
+    assert lib.bsa_attention_fwd(ctypes.byref(s), *a, ctypes.c_float(float("nan")),
+                                 ctypes.c_void_p(16), null, ctypes.c_void_p(16), null) == 1
+    ds = _lib.DecodeShape(4, 32, 8, 128, 64, 100, 400, 32)
+    dargs = [ctypes.c_void_p(16)] * 6
+    assert lib.bsa_decode_paged(ctypes.byref(ds), *dargs, ctypes.c_float(0.0), ctypes.c_void_p(16),
+                                null, ctypes.c_void_p(16), ctypes.c_void_p(16), null, null, 0,
+                                null) == 3
+    ds_bad = _lib.DecodeShape(4, 32, 8, 64, 64, 100, 400, 32)
+    assert lib.bsa_decode_paged(ctypes.byref(ds_bad), *dargs, ctypes.c_float(0.0),
+                                ctypes.c_void_p(16), null, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                null, null, 0, null) == 2
+    assert lib.bsa_decode_workspace_size(ctypes.byref(ds)) > 0

@@ -1,0 +1,85 @@
+"""GPU parity of the paged decode path against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_block_sparse_mean_gb300 as bsa
+import oracle
+from dynamic_block_sparse_mean_gb300 import synth
+from parity_utils import BF16_LSE_ABS, BF16_MAX_ABS, BF16_MEAN_ABS, TIE_BAND, BF16View, dev_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def _upload(x):
+    return (dev_tensor(x.q, "bf16"), dev_tensor(x.k_cache, "bf16"), dev_tensor(x.v_cache, "bf16"),
+            torch.as_tensor(x.block_table, device="cuda"),
+            torch.as_tensor(x.context_lens, device="cuda"))
+
+
+def check_decode(x, top_k, o, lse, sel, cnt, reqs, G):
+    q64 = synth.bf16_bits_to_f32(x.q).astype(np.float64)
+    oo, lo, so, co, sc = oracle.decode(q64, BF16View(x.k_cache), BF16View(x.v_cache),
+                                       x.block_table, x.context_lens, x.page_size, top_k,
+                                       reqs=reqs, return_scores=True)
+    Hk = x.k_cache.shape[1]
+    for rho in reqs:
+        for h in range(Hk):
+            n = int(x.context_lens[rho])
+            L = (n + 63) // 64
+            cg = int(cnt[rho, h])
+            assert cg == int(co[rho, h]) == min(top_k, L - 1) + 1
+            sg = [int(v) for v in sel[rho, h, :cg]]
+            assert sg == sorted(set(sg)) and sg[-1] == L - 1
+            assert all(int(v) == -1 for v in sel[rho, h, cg:])
+            dg, do = set(sg[:-1]), set(int(v) for v in so[rho, h, :cg - 1])
+            g = sc[(rho, h)]
+            if dg != do:
+                s_k = min(g[j] for j in do)
+                for j in dg ^ do:
+                    assert abs(g[j] - s_k) <= TIE_BAND
+    rows = np.array(list(reqs))
+    d = np.abs(o[rows].astype(np.float64) - oo[rows])
+    assert d.max() <= BF16_MAX_ABS and d.mean() <= BF16_MEAN_ABS, (d.max(), d.mean())
+    assert np.abs(lse[rows] - lo[rows]).max() <= BF16_LSE_ABS
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_small(G):
+    Hk = 2
+    rng = np.random.default_rng(G)
+    lens = rng.integers(1, 4000, size=7)
+    lens[0], lens[1] = 64, 65          # one page exactly; a second page with one key
+    x = synth.gen_decode(lens, G * Hk, Hk, 128, 64, seed=30 + G, max_pages=70)
+    q, kc, vc, bt, cl = _upload(x)
+    ps = bsa.page_summaries(kc, bt, cl)
+    top_k = 8
+    o, lse, sel, cnt = bsa.decode_paged(q, kc, vc, ps, bt, cl, top_k=top_k)
+    torch.cuda.synchronize()
+    check_decode(x, top_k, o.float().cpu().numpy(), lse.cpu().numpy(), sel.cpu().numpy(),
+                 cnt.cpu().numpy(), range(len(lens)), G)
+
+
+def test_page_summaries_match_page_means():
+    x = synth.gen_decode([130, 64, 1000], 4, 2, 128, 64, seed=40)
+    q, kc, vc, bt, cl = _upload(x)
+    ps = bsa.page_summaries(kc, bt, cl).cpu().numpy()
+    kv = BF16View(x.k_cache)
+    for rho, n in enumerate(x.context_lens):
+        L = (n + 63) // 64
+        for p in range(L):
+            phys = x.block_table[rho, p]
+            valid = min(64, n - 64 * p)
+            ref = kv[phys][:, :valid].mean(axis=1)            # [H_kv, d]
+            assert np.abs(ps[phys] - ref).max() < 1e-5
+
+
+def test_decode_every_page_selected_matches_dense():
+    """top_k >= pages: every page is read, so decode is dense attention."""
+    x = synth.gen_decode([500, 1200], 8, 2, 128, 64, seed=41)
+    q, kc, vc, bt, cl = _upload(x)
+    ps = bsa.page_summaries(kc, bt, cl)
+    o, lse, sel, cnt = bsa.decode_paged(q, kc, vc, ps, bt, cl, top_k=64)
+    torch.cuda.synchronize()
+    check_decode(x, 64, o.float().cpu().numpy(), lse.cpu().numpy(), sel.cpu().numpy(),
+                 cnt.cpu().numpy(), range(2), 4)

@@ -1,0 +1,268 @@
+"""GPU parity of the prefill path (summaries, router, worklist, attention) against
+the float64 oracle on identical seeded inputs, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_block_sparse_mean_gb300 as bsa
+import oracle
+from dynamic_block_sparse_mean_gb300 import synth
+from parity_utils import (BF16_LSE_ABS, BF16_MAX_ABS, BF16_MEAN_ABS, FP32_REL, TIE_BAND,
+                          attention_errors, check_route_rows, oracle_view, shape_of, upload)
+
+pytestmark = pytest.mark.gpu
+
+# (name, lengths, H, H_kv, d, b, mode, k_max, k_min, tau_delta, sink)
+CASES = [
+    ("tiny_n1024_d64_b64", [1024], 2, 2, 64, 64, oracle.TOPK, 4, 0, 0.0, True),
+    ("ragged_gqa4_d128_b64", [700, 129, 64, 1500], 8, 2, 128, 64, oracle.TOPK, 6, 0, 0.0, False),
+    ("gqa8_d128_b128_sink", [1000, 300], 16, 2, 128, 128, oracle.TOPK, 5, 0, 0.0, True),
+    ("gqa2_d128_b64_threshold", [777, 1300], 4, 2, 128, 64, oracle.THRESHOLD, 8, 2, 2.0, False),
+    ("gqa3_d64_b64", [640, 33], 6, 2, 64, 64, oracle.TOPK, 3, 0, 0.0, False),
+    ("gqa1_d64_b128", [900], 2, 2, 64, 128, oracle.TOPK, 4, 0, 0.0, True),
+]
+
+
+def _run_case(case, dtype="bf16", seed=7):
+    name, lengths, H, Hk, d, b, mode, k_max, k_min, tau, sink = case
+    x = synth.gen_prefill(lengths, H, Hk, d, b, seed, "iid", dtype)
+    q, k, v = upload(x)
+    sh = shape_of(x, H, Hk)
+    params = bsa.RouteParams(mode, k_max, k_min, tau, sink)
+    return x, q, k, v, sh, params
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_summaries_match_oracle(case):
+    x, q, k, v, sh, params = _run_case(case)
+    C = bsa.block_summaries(k, sh).cpu().numpy()
+    Co = oracle.block_summaries(oracle_view(x, "k"), x.cu_seqlens, x.block)
+    assert C.shape == Co.shape
+    assert np.abs(C - Co).max() < 1e-5
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_router_matches_oracle_tie_aware(case):
+    x, q, k, v, sh, params = _run_case(case)
+    H, Hk = case[2], case[3]
+    C = bsa.block_summaries(k, sh)
+    scores = torch.full((sh.num_seqs, Hk, sh.max_blocks, sh.max_blocks), float("nan"), device="cuda")
+    J, cnt = bsa.route(q, C, sh, params, scores=scores)
+    Jo, co, go, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, x.block,
+                                 H // Hk, params.mode, params.k_max, params.k_min, params.tau_delta,
+                                 params.force_sink)
+    rows = oracle.all_rows(x.cu_seqlens, x.block, Hk)
+    check_route_rows(J.cpu().numpy(), cnt.cpu().numpy(), Jo, co, go, rows, params.mode,
+                     params.force_sink, params.tau_delta)
+    # the score matrix itself: fp32-accurate against float64
+    sg = scores.cpu().numpy()
+    valid = np.isfinite(go)
+    assert np.abs(sg[valid] - go[valid]).max() < 2e-6 * max(1.0, np.abs(go[valid]).max())
+    # rows past a sequence's end are empty and -1 filled
+    info = oracle.seq_info(x.cu_seqlens, x.block)
+    cn = cnt.cpu().numpy()
+    for i, (_, _, nb) in enumerate(info):
+        assert (cn[i, :, nb:] == 0).all()
+
+
+def _worklist_from(Jo, co, sh, k_max, status):
+    J = torch.as_tensor(Jo.astype(np.int32), device="cuda").contiguous()
+    cnt = torch.as_tensor(co.astype(np.int32), device="cuda").contiguous()
+    if J.shape[-1] < k_max:
+        J = torch.nn.functional.pad(J, (0, k_max - J.shape[-1]), value=-1)
+    return bsa.build_worklist(J, cnt, sh, k_max, status)
+
+
+def _expected_csr(Jo, co, cu, b):
+    B, Hk, Nq = co.shape
+    info = oracle.seq_info(cu, b)
+    rp, ci = [0], []
+    for i in range(B):
+        for h in range(Hk):
+            for r in range(Nq):
+                if r < info[i][2]:
+                    ids = [int(v) for v in Jo[i, h, r, :co[i, h, r]]] or [r]
+                    ci += ids
+                rp.append(len(ci))
+    return np.array(rp), np.array(ci)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_worklist_csr_and_buckets(case):
+    x, q, k, v, sh, params = _run_case(case)
+    H, Hk = case[2], case[3]
+    Jo, co, _, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, x.block,
+                                H // Hk, params.mode, params.k_max, params.k_min, params.tau_delta,
+                                params.force_sink)
+    co = co.copy()
+    co[0, 0, min(2, co.shape[2] - 1)] = 0       # one empty row: falls back to {r}
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    bsa.check_status(status)
+    rp, ci = _expected_csr(Jo, co, x.cu_seqlens, x.block)
+    assert np.array_equal(wl.row_ptr.cpu().numpy(), rp)
+    assert np.array_equal(wl.col_idx.cpu().numpy()[:len(ci)], ci)
+    bo = wl.bucket_off.cpu().numpy()
+    nrows = bo[-1]
+    work = wl.work.cpu().numpy()[:nrows]
+    lens = np.diff(rp)
+    assert sorted(work.tolist()) == sorted(np.nonzero(lens)[0].tolist())
+    caps = [256 >> s for s in range(7)]
+    for s in range(7):
+        seg = work[bo[s]:bo[s + 1]]
+        assert all(max(4, 1 << int(np.ceil(np.log2(max(1, lens[w]))))) == caps[s] for w in seg)
+        assert list(seg) == sorted(seg)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_attention_bf16_on_oracle_index(case):
+    x, q, k, v, sh, params = _run_case(case)
+    H, Hk = case[2], case[3]
+    G = H // Hk
+    Jo, co, _, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, x.block,
+                                G, params.mode, params.k_max, params.k_min, params.tau_delta,
+                                params.force_sink)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    torch.cuda.synchronize()
+    bsa.check_status(status)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, x.block, G, Jo, co)
+    Og = O.float().cpu().numpy()
+    lg = lse.cpu().numpy()
+    mask = np.ones(lo.shape, dtype=bool)
+    mx, mean, lmx, _, _ = attention_errors(Og, lg, Oo, lo, mask)
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS, (mx, mean)
+    assert lmx <= BF16_LSE_ABS, lmx
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[2]], ids=[c[0] for c in CASES[:3]])
+def test_attention_fp32_path(case):
+    x, q, k, v, sh, params = _run_case(case, dtype="fp32")
+    H, Hk = case[2], case[3]
+    G = H // Hk
+    Qo, Ko, Vo = (getattr(x, n).astype(np.float64) for n in "qkv")
+    Jo, co, _, _ = oracle.route(Qo, Ko, x.cu_seqlens, x.block, G, params.mode, params.k_max,
+                                params.k_min, params.tau_delta, params.force_sink)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    torch.cuda.synchronize()
+    bsa.check_status(status)
+    Oo, lo = oracle.attention(Qo, Ko, Vo, x.cu_seqlens, x.block, G, Jo, co)
+    Og, lg = O.cpu().numpy(), lse.cpu().numpy()
+    assert np.abs(Og - Oo).max() / np.abs(Oo).max() <= FP32_REL
+    assert np.abs(lg - lo).max() / np.abs(lo).max() <= FP32_REL
+    # the FP32 router too: the same tie-aware rule
+    C = bsa.block_summaries(k, sh)
+    J, cnt = bsa.route(q, C, sh, params)
+    _, _, go, _ = oracle.route(Qo, Ko, x.cu_seqlens, x.block, G, params.mode, params.k_max,
+                               params.k_min, params.tau_delta, params.force_sink)
+    check_route_rows(J.cpu().numpy(), cnt.cpu().numpy(), Jo, co, go,
+                     oracle.all_rows(x.cu_seqlens, x.block, Hk), params.mode, params.force_sink,
+                     params.tau_delta)
+
+
+def test_all_causal_blocks_equal_dense_attention():
+    """Density 1.0: every causal block selected is dense causal attention."""
+    x = synth.gen_prefill([1024, 333], 8, 2, 128, 64, 21)
+    q, k, v = upload(x)
+    sh = shape_of(x, 8, 2)
+    Jo, co = oracle.causal_all_blocks(x.cu_seqlens, 64, 2)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = _worklist_from(Jo, co, sh, Jo.shape[-1], status)
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, 64, 4, Jo, co)
+    mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
+                                           np.ones(lo.shape, dtype=bool))
+    bsa.check_status(status)
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS
+
+
+def test_shuffled_tile_order_stays_within_tolerance():
+    """Tiles merged in any order give the same result up to rounding."""
+    x = synth.gen_prefill([1500], 8, 2, 128, 64, 22)
+    q, k, v = upload(x)
+    sh = shape_of(x, 8, 2)
+    Jo, co, _, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, 64, 4,
+                                oracle.TOPK, 8)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = _worklist_from(Jo, co, sh, 8, status)
+    rp = wl.row_ptr.cpu().numpy()
+    ci = wl.col_idx.cpu().numpy().copy()
+    rng = np.random.default_rng(0)
+    for rr in range(len(rp) - 1):
+        ci[rp[rr]:rp[rr + 1]] = rng.permutation(ci[rp[rr]:rp[rr + 1]])
+    wl.col_idx.copy_(torch.as_tensor(ci, device="cuda"))
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, 64, 4, Jo, co)
+    mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
+                                           np.ones(lo.shape, dtype=bool))
+    bsa.check_status(status)
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS
+
+
+@pytest.mark.parametrize("kind,code", [("duplicate", 17), ("descending", 17), ("future", 16),
+                                       ("negative", 16), ("count", 18)])
+def test_worklist_rejects_malformed_rows(kind, code):
+    x = synth.gen_prefill([640], 2, 1, 64, 64, 23)
+    sh = shape_of(x, 2, 1)
+    J = np.full((1, 1, 10, 4), -1, dtype=np.int32)
+    cnt = np.zeros((1, 1, 10), dtype=np.int32)
+    for r in range(10):
+        J[0, 0, r, 0] = r
+        cnt[0, 0, r] = 1
+    r = 5
+    bad = {"duplicate": [1, 1, 5], "descending": [3, 1, 5], "future": [1, 6],
+           "negative": [-2, 5], "count": [1, 2, 5]}[kind]
+    J[0, 0, r, :len(bad)] = bad
+    cnt[0, 0, r] = len(bad) if kind != "count" else 9
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsa.build_worklist(torch.as_tensor(J, device="cuda"), torch.as_tensor(cnt, device="cuda"), sh,
+                       4, status)
+    assert int(status.item()) == code
+
+
+def test_duplicate_through_multiset_would_change_result():
+    """The worklist refuses duplicates, and counting one twice (the oracle's
+    multiset mode) would move the output past the tolerance."""
+    x = synth.gen_prefill([512], 2, 1, 64, 64, 24)
+    Jd = np.full((1, 1, 8, 4), -1)
+    Jd[0, 0, 5, :3] = [2, 2, 5]
+    cd = np.zeros((1, 1, 8), dtype=np.int64)
+    cd[0, 0, 5] = 3
+    Os, _ = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                             x.cu_seqlens, 64, 2, Jd, cd, rows=[(0, 0, 5)])
+    Om, _ = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                             x.cu_seqlens, 64, 2, Jd, cd, rows=[(0, 0, 5)], multiset=True)
+    assert np.nanmax(np.abs(Os - Om)) > BF16_MAX_ABS
+    sh = shape_of(x, 2, 1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsa.build_worklist(torch.as_tensor(Jd.astype(np.int32), device="cuda"),
+                       torch.as_tensor(cd.astype(np.int32), device="cuda"), sh, 4, status)
+    assert int(status.item()) == 17
+
+
+def test_plan_end_to_end_small():
+    """PrefillPlan (the public API) on the tiny workload against the oracle."""
+    w = __import__("dynamic_block_sparse_mean_gb300.workloads", fromlist=["TINY"]).TINY
+    x = synth.make_prefill(w)
+    q, k, v = upload(x)
+    plan = bsa.PrefillPlan(x.cu_seqlens, w.num_heads, w.num_kv_heads, w.head_dim, w.block,
+                           bsa.RouteParams(w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink))
+    O, lse = plan.run(q, k, v)
+    torch.cuda.synchronize()
+    bsa.check_status(plan.status)
+    Jo, co, go, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, w.block,
+                                 w.group, w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink)
+    check_route_rows(plan.J.cpu().numpy(), plan.counts.cpu().numpy(), Jo, co, go,
+                     oracle.all_rows(x.cu_seqlens, w.block, w.num_kv_heads), w.mode, w.force_sink)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, w.block, w.group, plan.J.cpu().numpy(),
+                              plan.counts.cpu().numpy())
+    mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
+                                           np.ones(lo.shape, dtype=bool))
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS
