@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse attention hot path on GB300.
+
+One step = one pass of the prefill path over one batch: block summaries,
+router (scores + selection), worklist, sparse attention — on the 32k-token
+prompt workload (n=32768, H=32 / H_kv=8, d=128, b=64, 32 blocks per row).
+The JSON line's value is the selected-tile TFLOP/s of the whole step; the
+router ms, stage times, the tensor-core roofline of the attention kernel, an
+end-to-end number from host buffers, the paged-decode KV GB/s on the 64-request
+decode workload, and the float64 oracle timed on the host cores ride along.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+NCORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(NCORES))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn TFLOP/s on selected tiles + router ms; decode KV GB/s"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_ATTN = os.path.join(ROOT, "profiles", "attn_tc_prompt32k.md")
+ATTN_SOURCE = os.path.join(ROOT, "dynamic_block_sparse_mean_gb300", "csrc", "attn_tc.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="prompt")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- ranks
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        if device is not None and torch.distributed.get_backend() == "nccl":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def reduce_max_sum(world: int, ms: float, units: float, device=None):
+    """Slowest rank's time and the units all ranks processed."""
+    if world == 1:
+        return ms, units
+    dev = device if (device is not None and torch.distributed.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.sel = str(device_index)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons, n = [], None, set(), 0
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(path: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the counters were taken (else None)."""
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_sha or not m_tr:
+        return None
+    sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
+    return float(m_tr.group(1)) if sha == m_sha.group(1) else None
+
+
+# ---------------------------------------------------------------- workloads
+
+
+def prefill_workload(name: str):
+    from dynamic_block_sparse_mean_gb300 import workloads as W
+    table = {"tiny": W.TINY, "prompt": W.PROMPT_32K, "varlen": W.VARLEN_256K, "long": W.LONG_128K}
+    return table[name]
+
+
+def to_dev_bf16(a: np.ndarray, device):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def bench_prefill(w, steps, warmup, device, world, sampler):
+    import dynamic_block_sparse_mean_gb300 as bsa
+    from dynamic_block_sparse_mean_gb300 import accounting, synth
+
+    x = synth.make_prefill(w)
+    q, k, v = (to_dev_bf16(a, device) for a in (x.q, x.k, x.v))
+    plan = bsa.PrefillPlan(x.cu_seqlens, w.num_heads, w.num_kv_heads, w.head_dim, w.block,
+                           bsa.RouteParams(w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink),
+                           device=device)
+    for _ in range(max(3, warmup)):
+        plan.run(q, k, v)
+    torch.cuda.synchronize(device)
+    bsa.check_status(plan.status)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    t0.record()
+    for s in range(steps):
+        e = ev[s]
+        e[0].record()
+        plan.summaries(k)
+        e[1].record()
+        plan.select(q)
+        e[2].record()
+        plan.worklist()
+        e[3].record()
+        plan.attend(q, k, v)
+        e[4].record()
+    t1.record()
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    barrier(world, device)
+    bsa.check_status(plan.status)
+    total_ms = t0.elapsed_time(t1)
+    stage = lambda a, b_: statistics.mean(ev[s][a].elapsed_time(ev[s][b_]) for s in range(steps))  # noqa: E731
+    st = {"summaries": stage(0, 1), "route": stage(1, 2), "worklist": stage(2, 3),
+          "attention": stage(3, 4)}
+    counts = plan.counts.cpu().numpy()
+    J = plan.J.cpu().numpy()
+    G = w.num_heads // w.num_kv_heads
+    T = int(x.cu_seqlens[-1])
+    flops = accounting.attention_tile_flops(counts, G, w.block, w.head_dim)
+    eff = accounting.effective_pairs(J, counts, x.cu_seqlens, w.block, G) * 4.0 * w.head_dim
+    tiles = counts[counts > 0]
+    launches = sum(bsa.PrefillPlan.LAUNCHES.values()) * steps
+    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, stages=st, flops=flops,
+               eff_flops=eff, clocks=clocks, launches=launches, T=T,
+               tiles={"min": int(tiles.min()), "mean": float(tiles.mean()), "max": int(tiles.max()),
+                      "total": int(counts.sum())},
+               router_flops=accounting.router_flops(x.cu_seqlens, w.block, w.num_heads, w.head_dim),
+               attn_bytes=accounting.attention_bytes(w.num_heads, w.num_kv_heads, T, w.head_dim))
+    return res
+
+
+def bench_e2e(res, steps, device):
+    """Same metric through PrefillPlan.run with host (pinned) buffers: every step
+    copies Q, K, V host -> device and reads O back device -> host."""
+    x, plan = res["x"], res["plan"]
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for a in (x.q, x.k, x.v))
+    dq, dk, dv = (torch.empty(t.shape, dtype=torch.bfloat16, device=device) for t in (hq, hk, hv))
+    ho = torch.empty(plan.out.shape, dtype=torch.bfloat16).pin_memory()
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        out, _ = plan.run(dq, dk, dv)
+        ho.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / steps
+    bi = sum(t.numel() * 2 for t in (hq, hk, hv))
+    bo = ho.numel() * 2
+    return ms, bi, bo
+
+
+def bench_decode(steps, warmup, device):
+    import dynamic_block_sparse_mean_gb300 as bsa
+    from dynamic_block_sparse_mean_gb300 import accounting, synth
+    from dynamic_block_sparse_mean_gb300.workloads import DECODE_64 as w
+
+    dx = synth.make_decode(w)
+    q = to_dev_bf16(dx.q, device)
+    kc = to_dev_bf16(dx.k_cache, device)
+    vc = to_dev_bf16(dx.v_cache, device)
+    bt = torch.as_tensor(dx.block_table, device=device)
+    cl = torch.as_tensor(dx.context_lens, device=device)
+    ps = bsa.page_summaries(kc, bt, cl)
+    plan = bsa.DecodePlan(w.num_reqs, w.num_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                          dx.block_table.shape[1], dx.k_cache.shape[0], w.top_k, device=device)
+    for _ in range(max(3, warmup)):
+        plan.run(q, kc, vc, ps, bt, cl)
+    torch.cuda.synchronize(device)
+    bsa.check_status(plan.status)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        plan.run(q, kc, vc, ps, bt, cl)
+    t1.record()
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / steps
+    by = accounting.decode_bytes(dx.context_lens, plan.sel.cpu().numpy(),
+                                 plan.sel_counts.cpu().numpy(), w.num_heads, w.num_kv_heads,
+                                 w.head_dim, w.page_size)
+    del kc, vc
+    return ms, by, w
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+
+def oracle_rows(x, w, rows, cache):
+    """The oracle's route + attention for a list of (i, h, r) rows (block
+    summaries of the whole batch on first use); returns the selected-tile FLOPs
+    processed."""
+    import oracle
+    from dynamic_block_sparse_mean_gb300 import synth
+
+    class View:  # bf16 bits -> float64, converted slice by slice
+        def __init__(self, bits):
+            self.bits, self.shape = bits, bits.shape
+
+        def __getitem__(self, idx):
+            return synth.bf16_bits_to_f32(np.ascontiguousarray(self.bits[idx])).astype(np.float64)
+
+    Q, K, V = View(x.q), View(x.k), View(x.v)
+    G = w.num_heads // w.num_kv_heads
+    if "C" not in cache:
+        cache["C"] = oracle.block_summaries(K, x.cu_seqlens, w.block)
+    C = cache["C"]
+    flops = 0.0
+    for (i, h, r) in rows:
+        g = oracle.route_scores_row(Q, C, x.cu_seqlens, w.block, G, (i, h, r)) if r > 0 else []
+        sel = oracle.select_row(g, r, w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink)
+        J = np.full(C.shape[:3] + (len(sel),), -1)
+        J[i, h, r] = sel
+        cnt = np.zeros(C.shape[:3], dtype=np.int64)
+        cnt[i, h, r] = len(sel)
+        oracle.attention_row(Q, K, V, x.cu_seqlens, w.block, G, J, cnt, (i, h, r))
+        flops += len(sel) * G * 4.0 * w.block * w.block * w.head_dim
+    return flops
+
+
+def cpu_oracle_throughput(x, w, budget_s: float, seed: int = 0, max_rows: int = 4000):
+    """Time the oracle on random rows of the workload until budget_s has passed."""
+    rng = np.random.default_rng(seed)
+    info = [(int(x.cu_seqlens[i]), int(x.cu_seqlens[i + 1] - x.cu_seqlens[i])) for i in range(len(x.cu_seqlens) - 1)]
+    C_cache = {}
+    flops, n, t0 = 0.0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and n < max_rows:
+        i = int(rng.integers(len(info)))
+        nb = (info[i][1] + w.block - 1) // w.block
+        row = (i, int(rng.integers(w.num_kv_heads)), int(rng.integers(nb)))
+        flops += oracle_rows(x, w, [row], C_cache)
+        n += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, n, dt
+
+
+# ---------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    from dynamic_block_sparse_mean_gb300 import synth
+    w = prefill_workload(args.workload)
+    x = synth.make_prefill(w)
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for s in range(args.warmup):
+        cpu_oracle_throughput(x, w, per_step, seed=10_000 + s)
+    flops, dt, rows = 0.0, 0.0, 0
+    for s in range(args.steps):
+        v, n, t = cpu_oracle_throughput(x, w, per_step, seed=s)
+        flops += v * 1e12 * t
+        dt += t
+        rows += n
+    value = flops / dt / 1e12
+    sample = (f"{rows} random (sequence, KV head, query block) rows of {w.name}: oracle block "
+              f"summaries of the touched head, router scores and selection, masked full-row "
+              f"attention; about {per_step:.2f} s of rows per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": NCORES, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_native(args):
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier(world, device)
+    w = prefill_workload(args.workload)
+    sampler = ClockSampler(local)
+    res = bench_prefill(w, args.steps, args.warmup, device, world, sampler)
+    ms_step = res["total_ms"] / args.steps
+    max_ms, tot_flops = reduce_max_sum(world, ms_step, res["flops"], device)
+    value = tot_flops / (max_ms * 1e-3) / 1e12
+    peaks, src = measured_peaks()
+    st = res["stages"]
+    attn_tf = res["flops"] / (st["attention"] * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = recorded_traffic(PROFILE_ATTN, ATTN_SOURCE)
+    roofline = {"bound": "tensor", "kernel": "attn_tc_kernel<128,64>", "achieved": attn_tf,
+                "peak": peak_tf, "unit": "TFLOP/s", "frac": attn_tf / peak_tf,
+                "peak_source": f"{src} bf16 burst", "traffic": traffic,
+                "algorithmic_flops_per_launch": res["flops"],
+                "compulsory_bytes_per_launch": res["attn_bytes"]}
+    e2e = None
+    if not args.no_e2e:
+        e_ms, bi, bo = bench_e2e(res, max(3, min(args.steps, 20)), device)
+        e2e = {"value": res["flops"] * world / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_ms, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    dec = None
+    if not args.no_decode:
+        del res["q"], res["k"], res["v"]
+        d_ms, d_bytes, dw = bench_decode(max(20, min(args.steps, 200)), args.warmup, device)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        gbs = d_bytes["total"] / (d_ms * 1e-3) / 1e9
+        dec = {"workload": dw.name, "value": gbs, "unit": "GB/s", "ms_per_step": d_ms,
+               "kv_only_gbs": d_bytes["kv"] / (d_ms * 1e-3) / 1e9, "bytes": d_bytes,
+               "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                            "frac": gbs / hbm, "peak_source": f"{src} copy bandwidth"}}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, n, dt = cpu_oracle_throughput(res["x"], w, budget_s=12.0)
+        cpu = {"value": v, "unit": UNIT, "cores": NCORES, "kind": "oracle",
+               "sample": f"{n} random rows of {w.name} in {dt:.1f} s (oracle summaries of the "
+                         f"touched heads, router scores, selection, masked full-row attention); "
+                         f"FLOPs counted as selected physical tiles"}
+    if rank != 0:
+        return 0
+    x = res["x"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "total_tokens": res["T"],
+                   "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block": w.block, "k_max": w.k_max,
+                   "route": "topk" if w.mode == 0 else "threshold",
+                   "l2": "inputs larger than L2 (Q+K+V %.0f MB > 129 MB); no flush" %
+                         ((x.q.nbytes + x.k.nbytes + x.v.nbytes) / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "router_ms": st["summaries"] + st["route"],
+        "stages_ms": st,
+        "attention_tflops": attn_tf,
+        "effective_pair_tflops": res["eff_flops"] / (st["attention"] * 1e-3) / 1e12,
+        "router_tflops": res["router_flops"] / (st["route"] * 1e-3) / 1e12,
+        "tiles_per_row": res["tiles"],
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "decode": dec,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

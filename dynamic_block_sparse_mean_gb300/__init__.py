@@ -219,12 +219,25 @@ class PrefillPlan:
         self.lse = torch.empty(num_heads, sh.total_tokens, dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def route(self, q, k):
+    # kernels each stage launches (bsa_block_summaries 1, bsa_route 2,
+    # bsa_build_worklist 3, bsa_attention_fwd 1)
+    LAUNCHES = {"summaries": 1, "route": 2, "worklist": 3, "attention": 1}
+
+    def summaries(self, k):
         block_summaries(k, self.shape, out=self.C)
+
+    def select(self, q):
         route(q, self.C, self.shape, self.params, J=self.J, counts=self.counts,
               scores=self.scores, ws=self.route_ws, dev_status=self.status)
+
+    def worklist(self):
         build_worklist(self.J, self.counts, self.shape, self.params.k_max, self.status,
                        wl=self.wl, ws=self.wl_ws)
+
+    def route(self, q, k):
+        self.summaries(k)
+        self.select(q)
+        self.worklist()
 
     def attend(self, q, k, v, scale: float = 0.0):
         return attention_fwd(q, k, v, self.wl, self.shape, self.status, scale, out=self.out,

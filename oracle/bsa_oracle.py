@@ -148,12 +148,19 @@ def route_scores(Q, C, cu_seqlens, b: int, G: int, rows=None):
     if rows is None:
         rows = [(i, h, r) for i, (_, _, nb) in enumerate(info) for h in range(Hk) for r in range(nb)]
     for (i, h, r) in rows:
-        s0, n, nb = info[i]
-        if r == 0 or r >= nb:
+        if r == 0 or r >= info[i][2]:
             continue
-        qr = _f64(Q[h * G:(h + 1) * G, s0 + r * b: s0 + min(n, (r + 1) * b), :]).reshape(-1, d)
-        g[i, h, r, :r] = (qr @ C[i, h, :r, :].T).max(axis=0)
+        g[i, h, r, :r] = route_scores_row(Q, C, cu_seqlens, b, G, (i, h, r))
     return g
+
+
+def route_scores_row(Q, C, cu_seqlens, b: int, G: int, row):
+    """The scores g[i, h, r, 0 .. r-1] of one router row (see route_scores)."""
+    i, h, r = row
+    d = C.shape[3]
+    s0, n, _ = seq_info(cu_seqlens, b)[i]
+    qr = _f64(Q[h * G:(h + 1) * G, s0 + r * b: s0 + min(n, (r + 1) * b), :]).reshape(-1, d)
+    return (qr @ C[i, h, :r, :].T).max(axis=0)
 
 
 # ----------------------------------------------------------------------------
