@@ -58,6 +58,7 @@ PROTOTYPES = {
                         SZ, V]),
     "bsa_worklist_workspace_size": (SZ, [ctypes.POINTER(Shape), I32]),
     "bsa_build_worklist": (I32, [ctypes.POINTER(Shape), I32, V, V, V, V, V, V, V, V, SZ, V]),
+    "bsa_build_worklist_noalloc": (I32, [ctypes.POINTER(Shape), I32, V, V, V, V, V, V, V, V]),
     "bsa_attention_fwd": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, V, V, F32, V, V, V, V]),
     "bsa_page_summaries": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V]),
     "bsa_decode_workspace_size": (SZ, [ctypes.POINTER(DecodeShape)]),

@@ -134,6 +134,23 @@ bsa_status_t bsa_build_worklist(const bsa_shape_t *shape, int32_t k_max, const i
                                        bucket_off, dev_status, ws, stream));
 }
 
+bsa_status_t bsa_build_worklist_noalloc(const bsa_shape_t *shape, int32_t k_max,
+                                        const int32_t *J, const int32_t *counts,
+                                        int32_t *row_ptr, int32_t *col_idx, int32_t *work,
+                                        int32_t *bucket_off, int32_t *dev_status,
+                                        cudaStream_t stream) {
+  if (!shape_ok(shape) || J == nullptr || counts == nullptr || row_ptr == nullptr ||
+      col_idx == nullptr || work == nullptr || bucket_off == nullptr || dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (k_max < 1 || k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
+  const long long rows = (long long)shape->num_seqs * shape->num_kv_heads * shape->max_blocks;
+  if (rows > BSA_WORKLIST_NOALLOC_MAX_ROWS) return BSA_ERR_UNSUPPORTED;
+  int32_t *scratch = nullptr;
+  if (bsa::worklist_noalloc_scratch(&scratch) != cudaSuccess) return BSA_ERR_LAUNCH;
+  return launched(bsa::launch_worklist(*shape, k_max, J, counts, row_ptr, col_idx, work,
+                                       bucket_off, dev_status, scratch, stream));
+}
+
 bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const void *K,
                                const void *V, const int32_t *row_ptr, const int32_t *col_idx,
                                const int32_t *work, const int32_t *bucket_off,

@@ -32,6 +32,8 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
                             cudaStream_t st);
+// Device address of the fixed scratch array used by bsa_build_worklist_noalloc.
+cudaError_t worklist_noalloc_scratch(int32_t **out);
 
 // a5, tensor-core BF16 path (attn_tc.cu) and SIMT FP32 path (attn_simt.cu)
 cudaError_t launch_attention_tc(const bsa_shape_t &s, const void *Q, const void *K,

@@ -5,6 +5,8 @@
 //   2. scan kernel   row_ptr by prefix sum, and the work list: a stable counting
 //                    sort of rows by capacity bucket, largest first (one CTA)
 //   3. fill kernel   copies the block ids into col_idx (grid-wide)
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -159,7 +161,33 @@ __global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__r
   }
 }
 
+// Scratch of bsa_build_worklist_noalloc: one row code per row, shared by every
+// call on a device.  Host code must not pass this name to a kernel (on the host
+// it is only a stand-in); it passes the address cudaGetSymbolAddress returns.
+__device__ __align__(256) int32_t g_noalloc_rows[BSA_WORKLIST_NOALLOC_MAX_ROWS];
+
 }  // namespace
+
+// Device address of g_noalloc_rows on the current device, looked up once per
+// device (with that device current) and cached.
+cudaError_t worklist_noalloc_scratch(int32_t **out) {
+  constexpr int kMaxDevices = 64;
+  static int32_t *cache[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_rows);
+    if (e != cudaSuccess) return e;
+    cache[dev] = static_cast<int32_t *>(p);
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
 
 size_t worklist_workspace_bytes(const bsa_shape_t &s, int32_t) {
   return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * sizeof(int32_t);

@@ -167,6 +167,37 @@ bsa_status_t bsa_build_worklist(const bsa_shape_t *shape, int32_t k_max, const i
                                 void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Worklist builder that allocates nothing.  The pages have no counterpart:
+ * this is a packaging of bsa_build_worklist for callers that cannot hand the
+ * library any scratch memory — for example a serving runtime that plans every
+ * GPU buffer up front and only owns its inputs and outputs, or code running
+ * where a cudaMalloc would synchronise the device or is not permitted.
+ *
+ * Arguments, results, validation and device-side errors are exactly those of
+ * bsa_build_worklist, without ws / ws_bytes.  The scratch it needs (one int32
+ * per row) lives in a fixed device array inside the library,
+ * BSA_WORKLIST_NOALLOC_MAX_ROWS entries (1 MiB), which every GPU that loads
+ * the library keeps until the process exits.
+ *  - Shapes with B * H_kv * N_q > BSA_WORKLIST_NOALLOC_MAX_ROWS are rejected
+ *    with BSA_ERR_UNSUPPORTED before anything is enqueued.
+ *  - The first call on a device looks up that array's device address, with
+ *    the caller's current device; make this first call before any stream
+ *    capture.
+ *  - Every call uses the same array.  Calls ordered on one stream are safe;
+ *    calls whose kernels may overlap on the GPU (different streams, or host
+ *    threads issuing to one device without ordering) race on it and may all
+ *    produce wrong worklists.  Each call rewrites every entry it reads, so
+ *    nothing left by an earlier call needs clearing.
+ *  - It never calls cudaMalloc, cudaFree or any other allocating routine.
+ * ------------------------------------------------------------------------- */
+#define BSA_WORKLIST_NOALLOC_MAX_ROWS (1 << 18)
+bsa_status_t bsa_build_worklist_noalloc(const bsa_shape_t *shape, int32_t k_max,
+                                        const int32_t *J, const int32_t *counts,
+                                        int32_t *row_ptr, int32_t *col_idx, int32_t *work,
+                                        int32_t *bucket_off, int32_t *dev_status,
+                                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * a5. Sparse attention forward — [P2] §1.2 eqs.(1)-(5): for each row listed
  *   in `work` and every query head of its group, exact S = Q_r K_j^T * scale
  *   on the selected tiles only (eq.(2)), the causal mask s <= t inside the
