@@ -219,9 +219,10 @@ class PrefillPlan:
         self.lse = torch.empty(num_heads, sh.total_tokens, dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    # kernels each stage launches (bsa_block_summaries 1, bsa_route 2,
-    # bsa_build_worklist 3, bsa_attention_fwd 1)
-    LAUNCHES = {"summaries": 1, "route": 2, "worklist": 3, "attention": 1}
+    # kernels each stage launches on the BF16 path (bsa_block_summaries 1;
+    # bsa_route 3: summary split, tensor-core scores, selection;
+    # bsa_build_worklist 3; bsa_attention_fwd 1)
+    LAUNCHES = {"summaries": 1, "route": 3, "worklist": 3, "attention": 1}
 
     def summaries(self, k):
         block_summaries(k, self.shape, out=self.C)

@@ -110,7 +110,8 @@ bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *param
   if (params->force_sink && params->k_max < 2) return BSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(C)) return BSA_ERR_INVALID_ARG;
   const size_t need = bsa::route_workspace_bytes(*shape, *params);
-  if (scores == nullptr && (ws == nullptr || ws_bytes < need)) return BSA_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < need) return BSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return BSA_ERR_INVALID_ARG;
   return launched(bsa::launch_route(*shape, *params, Q, C, J, counts, scores, dev_status, ws,
                                     stream));
 }

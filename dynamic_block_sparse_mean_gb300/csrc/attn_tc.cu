@@ -22,10 +22,7 @@
 #include "common.cuh"
 #include "kernels.h"
 
-#include <cudaTypedefs.h>
-
 #include <algorithm>
-#include <mutex>
 
 namespace bsa {
 namespace {
@@ -103,13 +100,6 @@ BSA_DEV Unit decode_unit(const AttnParams &p, int u) {
   x.nkv = __ldg(p.row_ptr + x.row + 1) - x.kv0;
   x.nt = min(2, p.mtiles - 2 * x.pair);
   return x;
-}
-
-// Wait bounded only by time (used while draining after an abort).
-BSA_DEV void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return;
 }
 
 template <int D, int BK>
@@ -429,33 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                 uint32_t b0, uint32_t b1, uint32_t b2) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int BK>
 cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const void *V,
                       const int32_t *row_ptr, const int32_t *col_idx, const int32_t *work,
@@ -463,9 +426,9 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
                       int32_t *dev_status, cudaStream_t st) {
   using C = Cfg<D, BK>;
   CUtensorMap mq, mk, mv;
-  if (!make_map_3d(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
-      !make_map_3d(&mk, K, D, s.total_tokens, s.num_kv_heads, 64, BK, 1) ||
-      !make_map_3d(&mv, V, D, s.total_tokens, s.num_kv_heads, 64, BK, 1))
+  if (!make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
+      !make_tmap_3d_bf16(&mk, K, D, s.total_tokens, s.num_kv_heads, 64, BK, 1) ||
+      !make_tmap_3d_bf16(&mv, V, D, s.total_tokens, s.num_kv_heads, 64, BK, 1))
     return cudaErrorInvalidValue;
   AttnParams p;
   p.cu = s.cu_seqlens;

@@ -97,6 +97,13 @@ BSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_fl
   }
 }
 
+// Wait bounded only by time (used while draining copies / MMAs after an abort).
+BSA_DEV void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
+}
+
 // ---------------------------------------------------------------- TMA
 
 BSA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,

@@ -3,6 +3,7 @@
 // given stream and returns the launch error, if any.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -12,6 +13,17 @@
 namespace bsa {
 
 int num_sms();
+
+// 3-D bf16 TMA descriptor (dims d0 innermost .. d2, dense strides) with a
+// 128-byte swizzle and box b0 x b1 x b2 (tmap.cu).
+bool make_tmap_3d_bf16(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint32_t b0, uint32_t b1, uint32_t b2);
+
+// a2 on the tensor cores (route_tc.cu): exact fp32 scores from bf16 Q and the
+// three-way bf16 split of the fp32 summaries; writes S[row][j] for j < r.
+size_t route_tc_workspace_bytes(const bsa_shape_t &s);
+cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C, float *S,
+                                   void *ws, int32_t *dev_status, cudaStream_t st);
 
 // a1 and the decode page summaries (summaries.cu)
 cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,

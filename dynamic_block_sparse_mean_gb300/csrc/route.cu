@@ -238,26 +238,31 @@ __global__ void __launch_bounds__(32) route_select_kernel(
 
 }  // namespace
 
+// Workspace: [bf16 split of C, BF16 path only][score matrix, unless the caller
+// passes its own `scores` buffer].
 size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &) {
-  return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * s.max_blocks * sizeof(float);
+  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s) : 0;
+  return split + (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * s.max_blocks * sizeof(float);
 }
 
 cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
                          const float *C, int32_t *J, int32_t *counts, float *scores,
                          int32_t *dev_status, void *ws, cudaStream_t st) {
-  (void)dev_status;
-  float *S = scores != nullptr ? scores : static_cast<float *>(ws);
+  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s) : 0;
+  float *S = scores != nullptr ? scores
+                               : reinterpret_cast<float *>(static_cast<char *>(ws) + split);
   const int G = s.num_heads / s.num_kv_heads;
   const dim3 grid(s.max_blocks, s.num_kv_heads, s.num_seqs);
-  if (s.dtype == BSA_BF16)
-    route_scores_kernel<uint16_t><<<grid, kThreads, 0, st>>>(
-        static_cast<const uint16_t *>(Q), C, s.cu_seqlens, S, s.total_tokens, s.max_blocks,
-        s.num_kv_heads, G, s.head_dim, s.block);
-  else
+  cudaError_t e;
+  if (s.dtype == BSA_BF16) {
+    e = launch_route_scores_tc(s, Q, C, S, ws, dev_status, st);
+    if (e != cudaSuccess) return e;
+  } else {
     route_scores_kernel<float><<<grid, kThreads, 0, st>>>(
         static_cast<const float *>(Q), C, s.cu_seqlens, S, s.total_tokens, s.max_blocks,
         s.num_kv_heads, G, s.head_dim, s.block);
-  cudaError_t e = cudaGetLastError();
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = s.num_seqs * s.num_kv_heads * s.max_blocks;
   const size_t sm = (size_t)s.max_blocks * 5 + (size_t)(p.k_max + 2) * 4 + 16;

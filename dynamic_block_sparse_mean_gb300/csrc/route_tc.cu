@@ -1,0 +1,334 @@
+// a2 on the tensor cores: router scores g[i,h,r,j] = max over the group's query
+// rows of block r of q . c_j, j < r ("2.1 · 粗粒度选择" §2.1 eq.(6), pool = max).
+//
+// The selection is compared bit-exactly (up to a 1e-5 tie band) with a float64
+// oracle, so the scores must be fp32-accurate.  Q is exact in bf16; each fp32
+// summary is split without error into three bf16 terms c = c_hi + c_mid + c_lo
+// (the residuals of bf16 rounding are exact in fp32), and q . c is accumulated
+// on the tensor cores in fp32 as q . c_lo + q . c_mid + q . c_hi (small terms first).
+//
+// MMA orientation: M = 128 summaries (TMEM lanes), N = up to 256 query rows
+// (TMEM columns), K = d.  The max over query rows is then a per-thread max over
+// the TMEM columns of its own lane — no cross-thread reduction.
+//
+// Persistent kernel, one CTA per SM, 192 threads:
+//   warps 0-3  epilogue: tcgen05.ld of a 128 x N accumulator, masked row max,
+//              write / max-merge into S
+//   warp 4     TMA producer: query chunks (G*b rows, <= 256 per chunk) and
+//              16 KB panels of the split summaries, through rings of 2 and 4
+//   warp 5     MMA issuer (one thread), double-buffered accumulators in TMEM
+// Work order: rows with the longest history first (r descending).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace bsa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kQStages = 2;
+constexpr int kAStages = 4;
+constexpr int kAStage = 128 * 128;  // one 128-byte panel of one split part, 128 summaries
+
+template <int D>
+struct RCfg {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQStage = 256 * D * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffA = kOffQ + kQStages * kQStage;
+  static constexpr int kOffBar = kOffA + kAStages * kAStage;
+  static constexpr int B_QFULL = 0, B_QEMPTY = kQStages;
+  static constexpr int B_AFULL = 2 * kQStages, B_AEMPTY = B_AFULL + kAStages;
+  static constexpr int B_DFULL = B_AEMPTY + kAStages, B_DEMPTY = B_DFULL + 2;
+  static constexpr int B_FINAL = B_DEMPTY + 2;
+  static constexpr int kNumBars = B_FINAL + 1;
+  static constexpr int kOffCtl = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes =
+      kOffCtl + 16 + 1024 < 120 * 1024 ? 120 * 1024 : kOffCtl + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct RouteTcParams {
+  const int32_t *cu;
+  float *S;
+  int32_t *status;
+  int B, Nq, Hk, G, b;
+  int nch;        // query chunks per row: ceil(G*b / 256)
+};
+
+struct RUnit {
+  int i, h, r, s0, nvalid;
+  bool valid;
+};
+
+BSA_DEV RUnit runit(const RouteTcParams &p, int u) {
+  RUnit x;
+  const int BH = p.B * p.Hk;
+  x.r = p.Nq - 1 - u / BH;
+  const int ih = u % BH;
+  x.i = ih / p.Hk;
+  x.h = ih % p.Hk;
+  x.s0 = __ldg(p.cu + x.i);
+  const int n = __ldg(p.cu + x.i + 1) - x.s0;
+  const int nb = (n + p.b - 1) / p.b;
+  x.valid = x.r >= 1 && x.r < nb;
+  x.nvalid = min(p.b, n - x.r * p.b);
+  return x;
+}
+
+BSA_DEV int chunk_cols(const RouteTcParams &p, int ch) { return min(256, p.G * p.b - 256 * ch); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmC,
+                    const RouteTcParams p) {
+  using C = RCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (sbase - raw);
+  const uint32_t bars = sbase + C::kOffBar;
+  auto bar = [&](int k) { return bars + 8u * (uint32_t)k; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kOffCtl);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + C::kOffCtl + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(bar(C::B_QFULL + s), 1);
+      mbar_init(bar(C::B_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(bar(C::B_AFULL + s), 1);
+      mbar_init(bar(C::B_AEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_DFULL + s), 1);
+      mbar_init(bar(C::B_DEMPTY + s), 4);
+    }
+    mbar_init(bar(C::B_FINAL), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmC);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = p.B * p.Hk * p.Nq;
+  const uint32_t smQ = sbase + C::kOffQ, smA = sbase + C::kOffA;
+  const int heads_per_chunk = 256 / p.b;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      int qi = 0, ai = 0;
+      int lastQ[kQStages], lastA[kAStages];
+      for (int s = 0; s < kQStages; ++s) lastQ[s] = -1;
+      for (int s = 0; s < kAStages; ++s) lastA[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        const RUnit x = runit(p, u);
+        if (!x.valid) continue;
+        const int nmt = (x.r + 127) / 128;
+        const int crow = (x.i * p.Hk + x.h) * p.Nq;
+        for (int ch = 0; ok && ch < p.nch; ++ch, ++qi) {
+          const int qs = qi % kQStages;
+          if (!(ok = mbar_wait(bar(C::B_QEMPTY + qs), ((qi / kQStages) & 1) ^ 1, abort_flag, p.status)))
+            break;
+          mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQStage);
+          lastQ[qs] = (qi / kQStages) & 1;
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(smQ + qs * C::kQStage + pn * 32768, &tmQ, bar(C::B_QFULL + qs), pn * 64,
+                        x.s0 + x.r * p.b, x.h * p.G + ch * heads_per_chunk);
+          for (int mt = 0; ok && mt < nmt; ++mt)
+            for (int part = 2; ok && part >= 0; --part)
+              for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
+                const int as = ai % kAStages;
+                if (!(ok = mbar_wait(bar(C::B_AEMPTY + as), ((ai / kAStages) & 1) ^ 1, abort_flag,
+                                     p.status)))
+                  break;
+                mbar_arrive_expect_tx(bar(C::B_AFULL + as), kAStage);
+                lastA[as] = (ai / kAStages) & 1;
+                tma_load_3d(smA + as * kAStage, &tmC, bar(C::B_AFULL + as), pn * 64,
+                            crow + 128 * mt, part);
+              }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kQStages; ++s)
+          if (lastQ[s] >= 0) mbar_wait_drain(bar(C::B_QFULL + s), lastQ[s]);
+        for (int s = 0; s < kAStages; ++s)
+          if (lastA[s] >= 0) mbar_wait_drain(bar(C::B_AFULL + s), lastA[s]);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      int qi = 0, ai = 0, di = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        const RUnit x = runit(p, u);
+        if (!x.valid) continue;
+        const int nmt = (x.r + 127) / 128;
+        for (int ch = 0; ok && ch < p.nch; ++ch, ++qi) {
+          const int qs = qi % kQStages;
+          const uint32_t idesc = idesc_bf16(128, chunk_cols(p, ch), false);
+          if (!(ok = mbar_wait(bar(C::B_QFULL + qs), (qi / kQStages) & 1, abort_flag, p.status)))
+            break;
+          tc_fence_after();
+          for (int mt = 0; ok && mt < nmt; ++mt, ++di) {
+            const int db = di % 2;
+            if (!(ok = mbar_wait(bar(C::B_DEMPTY + db), ((di / 2) & 1) ^ 1, abort_flag, p.status)))
+              break;
+            tc_fence_after();
+            bool first = true;
+            for (int part = 2; ok && part >= 0; --part)
+              for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
+                const int as = ai % kAStages;
+                if (!(ok = mbar_wait(bar(C::B_AFULL + as), (ai / kAStages) & 1, abort_flag,
+                                     p.status)))
+                  break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t a = sdesc_sw128(smA + as * kAStage + kk * 32, 16, 1024);
+                  const uint64_t bdesc =
+                      sdesc_sw128(smQ + qs * C::kQStage + pn * 32768 + kk * 32, 16, 1024);
+                  mma_bf16_ss(tmem + db * 256, a, bdesc, idesc, first ? 0u : 1u);
+                  first = false;
+                }
+                mma_commit(bar(C::B_AEMPTY + as));
+              }
+            if (!ok) break;
+            mma_commit(bar(C::B_DFULL + db));
+          }
+          if (!ok) break;
+          mma_commit(bar(C::B_QEMPTY + qs));
+        }
+      }
+      mma_commit(bar(C::B_FINAL));
+      mbar_wait_drain(bar(C::B_FINAL), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    const int row = warp * 32 + lane;  // TMEM lane = summary within the M-tile
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    int di = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+      const RUnit x = runit(p, u);
+      if (!x.valid) continue;
+      const int nmt = (x.r + 127) / 128;
+      float *Srow = p.S + ((size_t)(x.i * p.Hk + x.h) * p.Nq + x.r) * p.Nq;
+      const bool full = x.nvalid == p.b;
+      for (int ch = 0; ok && ch < p.nch; ++ch) {
+        const int ncols = chunk_cols(p, ch);
+        for (int mt = 0; mt < nmt; ++mt, ++di) {
+          const int db = di % 2;
+          if (!(ok = mbar_wait(bar(C::B_DFULL + db), (di / 2) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          float m = -INFINITY;
+          for (int c0 = 0; c0 < ncols; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lane_base + db * 256 + c0, rr);
+            if (full) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) m = fmaxf(m, __uint_as_float(rr[c]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (((ch * 256 + c0 + c) % p.b) < x.nvalid) m = fmaxf(m, __uint_as_float(rr[c]));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_DEMPTY + db));
+          const int j = mt * 128 + row;
+          if (j < x.r) Srow[j] = ch == 0 ? m : fmaxf(Srow[j], m);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// C [rows, d] fp32 -> three bf16 planes [3, rows, d] with c = hi + mid + lo exactly
+// up to the last bf16 rounding (residuals of bf16 rounding are exact in fp32).
+__global__ void split3_kernel(const float *__restrict__ C, uint16_t *__restrict__ C3, size_t n) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const float c = C[e];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(c);
+    const float r1 = c - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    C3[e] = *reinterpret_cast<const uint16_t *>(&hi);
+    C3[n + e] = *reinterpret_cast<const uint16_t *>(&mid);
+    C3[2 * n + e] = *reinterpret_cast<const uint16_t *>(&lo);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float *S, void *ws,
+                     int32_t *dev_status, cudaStream_t st) {
+  using Cf = RCfg<D>;
+  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  uint16_t *C3 = static_cast<uint16_t *>(ws);
+  const size_t n = rows * D;
+  split3_kernel<<<(unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(C, C3, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int G = s.num_heads / s.num_kv_heads;
+  CUtensorMap mq, mc;
+  if (!make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, s.block, 256 / s.block) ||
+      !make_tmap_3d_bf16(&mc, C3, D, rows, 3, 64, 128, 1))
+    return cudaErrorInvalidValue;
+  RouteTcParams p;
+  p.cu = s.cu_seqlens;
+  p.S = S;
+  p.status = dev_status;
+  p.B = s.num_seqs;
+  p.Nq = s.max_blocks;
+  p.Hk = s.num_kv_heads;
+  p.G = G;
+  p.b = s.block;
+  p.nch = (G * s.block + 255) / 256;
+  e = cudaFuncSetAttribute(route_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cf::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<size_t>(num_sms(), std::max<size_t>(1, rows));
+  route_tc_kernel<D><<<grid, kThreads, Cf::kSmemBytes, st>>>(mq, mc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t route_tc_workspace_bytes(const bsa_shape_t &s) {
+  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  return ((rows * s.head_dim * 3 * sizeof(uint16_t)) + 255) & ~(size_t)255;
+}
+
+cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C, float *S,
+                                   void *ws, int32_t *dev_status, cudaStream_t st) {
+  if (s.head_dim == 64) return launch_d<64>(s, Q, C, S, ws, dev_status, st);
+  return launch_d<128>(s, Q, C, S, ws, dev_status, st);
+}
+
+}  // namespace bsa
