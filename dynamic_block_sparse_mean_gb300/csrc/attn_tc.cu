@@ -7,14 +7,26 @@
 // share the row's blocks, GQA) are cut into 128-row M-tiles, two per CTA, so
 // every K/V tile staged in shared memory feeds 256 query rows.
 //
+// Keys are walked in steps of 128: one 128-key block, or two 64-key blocks
+// placed side by side in one shared-memory stage (a trailing odd block is loaded
+// twice and its copy masked).  Every MMA therefore has N = 128, the shape at
+// which tcgen05 runs at its full rate (N = 64 runs at two thirds).
+//
 // Warp roles (320 threads):
 //   warps 0-3  softmax / epilogue for M-tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax / epilogue for M-tile 1
-//   warp 8     TMA producer: Q tiles, then K_j and V_j of each selected block j
-//   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j
-// TMEM (512 columns): O_0, O_1 (d columns each) and S_0, S_1 (b columns each).
-// P is written by the softmax threads into shared memory in the 128-byte
-// swizzled K-major layout the MMA reads.
+//   warp 8     TMA producer: Q tiles, then the K and V rows of each key step
+//   warp 9     MMA issuer (one thread)
+// TMEM (512 columns): O_0, O_1 (d columns each), S_0, S_1 (128 columns each).  The
+// softmax overwrites the first 64 columns of S_t with P (bf16 pairs) and the PV
+// product reads P straight from tensor memory.
+//
+// Issue order of the MMA thread for step s, per M-tile t:
+//     PV_t(s)   [after P_t(s)]      O_t += P_t(s) V(s)
+//     QK_t(s+1) [after K(s+1)]      S_t  = Q_t K(s+1)^T
+// tcgen05.mma operations of one thread execute in issue order, so QK_t(s+1)
+// overwrites S_t only after PV_t(s) has read P_t(s).  While the softmax of one
+// M-tile runs, the tensor cores work on the other M-tile.
 //
 // The running max used for the exponentials is refreshed only when the row max
 // grows by more than 8 (log2 units); O and l are then rescaled in TMEM.  u / l is
@@ -31,42 +43,41 @@ constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
+constexpr int kStep = 128;  // keys per step
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D, int BK>
 struct Cfg {
-  static constexpr int kPanels = D / 64;      // 128-byte panels along d
-  static constexpr int kPPanels = BK / 64;    // 128-byte panels of P along the keys
+  static constexpr int kPanels = D / 64;        // 128-byte panels along d
+  static constexpr int kBPS = kStep / BK;       // key blocks per step (2 or 1)
   static constexpr int kQTile = 128 * D * 2;
-  static constexpr int kKVTile = BK * D * 2;
-  static constexpr int kPTile = 128 * BK * 2;
-  static constexpr int NSK = (D == 128 && BK == 128) ? 2 : 3;
-  static constexpr int NSV = (D == 128 && BK == 128) ? 1 : 3;
+  static constexpr int kStage = kStep * D * 2;  // K (or V) rows of one step
+  static constexpr int kPanel = kStep * 128;    // one 128-byte panel of a stage
+  static constexpr int NS = D == 128 ? 2 : 4;   // K/V stages
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTile;
-  static constexpr int kOffV = kOffK + NSK * kKVTile;
-  static constexpr int kOffP = kOffV + NSV * kKVTile;
-  static constexpr int kOffBar = kOffP + 2 * kPTile;
+  static constexpr int kOffV = kOffK + NS * kStage;
+  static constexpr int kOffBar = kOffV + NS * kStage;
   // barrier slots
   static constexpr int B_QFULL = 0, B_QEMPTY = 1;
-  static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + NSK;
-  static constexpr int B_VFULL = B_KEMPTY + NSK, B_VEMPTY = B_VFULL + NSV;
-  static constexpr int B_SFULL = B_VEMPTY + NSV, B_PFULL = B_SFULL + 2;
+  static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + NS;
+  static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
+  static constexpr int B_SFULL = B_VEMPTY + NS, B_PFULL = B_SFULL + 2;
   static constexpr int B_ODONE = B_PFULL + 2, B_OFREE = B_ODONE + 2;
-  static constexpr int B_FINAL = B_OFREE + 2;
+  static constexpr int B_OFINAL = B_OFREE + 2;    // all PV of a unit done (once per unit)
+  static constexpr int B_FINAL = B_OFINAL + 2;
   static constexpr int kNumBars = B_FINAL + 1;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffCtl + 16;
   // 1 KB for base alignment; at least 120 KB so that exactly one CTA (which owns
   // all 512 TMEM columns) is resident per SM.
   static constexpr int kSmemBytes = kSmemUsed + 1024 < 120 * 1024 ? 120 * 1024 : kSmemUsed + 1024;
-  // TMEM columns of O_t and S_t
   BSA_DEV static uint32_t colO(int t) { return (uint32_t)(t * D); }
-  BSA_DEV static uint32_t colS(int t) { return 256u + (uint32_t)(t * BK); }
-  static constexpr uint32_t kIdescQK = idesc_bf16(128, BK, false);
+  BSA_DEV static uint32_t colS(int t) { return 256u + (uint32_t)(t * kStep); }
+  static constexpr uint32_t kIdescQK = idesc_bf16(128, kStep, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(256 + 2 * BK <= kTmemCols && 2 * D <= 256, "TMEM budget");
+  static_assert(2 * D <= 256, "TMEM budget");
 };
 
 struct AttnParams {
@@ -102,11 +113,117 @@ BSA_DEV Unit decode_unit(const AttnParams &p, int u) {
   return x;
 }
 
+// High word of every shared-memory descriptor used here: stride byte offset
+// 1024 (8 rows of 128 bytes), descriptor version 1, 128-byte swizzle.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+// Low word: start address >> 4 and leading byte offset >> 4.
+BSA_DEV uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
+}
+
+// tcgen05.mma kind::f16 with both operands in shared memory, descriptors given as
+// (low word, shared high word).
+BSA_DEV void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %5};\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
+      : "memory");
+}
+
+// Same with A (P, bf16 pairs) read from tensor memory.
+BSA_DEV void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
+      : "memory");
+}
+
+// 64 consecutive TMEM columns of this thread's lane: two loads, one wait.
+BSA_DEV void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
+BSA_DEV float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+BSA_DEV uint64_t pack2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+BSA_DEV float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
+BSA_DEV float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+BSA_DEV uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+BSA_DEV uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Max of 64 values (tree of three-input maxes).
+BSA_DEV float max64(const float (&v)[64]) {
+  float a[22];
+#pragma unroll
+  for (int k = 0; k < 21; ++k) a[k] = max3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  a[21] = v[63];
+  float b[8];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) b[k] = max3(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
+  b[7] = a[21];
+  return max3(max3(b[0], b[1], b[2]), max3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
+}
+
+// Load 64 S columns, apply the step's mask (columns >= lim are -inf; lim = 64
+// means none), into floats.
+BSA_DEV void load_masked(uint32_t taddr, int lim, float (&v)[64]) {
+  uint32_t rr[64];
+  tmem_ld64(taddr, rr);
+#pragma unroll
+  for (int c = 0; c < 64; ++c) v[c] = c < lim ? __uint_as_float(rr[c]) : -INFINITY;
+}
+
 template <int D, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = Cfg<D, BK>;
+  constexpr int BPS = C::kBPS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -120,11 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
     mbar_init(bar(C::B_QEMPTY), 1);
-    for (int s = 0; s < C::NSK; ++s) {
+    for (int s = 0; s < C::NS; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
       mbar_init(bar(C::B_KEMPTY + s), 1);
-    }
-    for (int s = 0; s < C::NSV; ++s) {
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
@@ -133,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_PFULL + t), 4);
       mbar_init(bar(C::B_ODONE + t), 1);
       mbar_init(bar(C::B_OFREE + t), 4);
+      mbar_init(bar(C::B_OFINAL + t), 1);
     }
     mbar_init(bar(C::B_FINAL), 1);
     *abort_flag = 0;
@@ -153,19 +269,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int total_units = __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.npairs;
-  const uint32_t smQ = sbase + C::kOffQ, smK = sbase + C::kOffK;
-  const uint32_t smV = sbase + C::kOffV, smP = sbase + C::kOffP;
+  const uint32_t smQ = sbase + C::kOffQ, smK = sbase + C::kOffK, smV = sbase + C::kOffV;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int kv_g = 0, ucount = 0;
-      int issuedK[C::NSK], issuedV[C::NSV], issuedQ = -1;
-      for (int s = 0; s < C::NSK; ++s) issuedK[s] = -1;
-      for (int s = 0; s < C::NSV; ++s) issuedV[s] = -1;
+      int stp = 0, ucount = 0;   // global step counter (stage ring), units
+      int issuedK[C::NS], issuedV[C::NS], issuedQ = -1;
+      for (int s = 0; s < C::NS; ++s) issuedK[s] = issuedV[s] = -1;
       bool ok = true;
+      Unit nx;
+      if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
-        const Unit x = decode_unit(p, u);
+        const Unit x = nx;
+        if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
         if (!(ok = mbar_wait(bar(C::B_QEMPTY), (ucount & 1) ^ 1, abort_flag, p.status))) break;
         mbar_arrive_expect_tx(bar(C::B_QFULL), x.nt * C::kQTile);
         issuedQ = ucount & 1;
@@ -175,115 +292,135 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smQ + t * C::kQTile + pn * 16384, &tmQ, bar(C::B_QFULL), pn * 64,
                         x.s0 + x.r * BK, hq0);
         }
-        for (int j = 0; j < x.nkv; ++j, ++kv_g) {
-          const int kb = __ldg(p.col_idx + x.kv0 + j);
-          const int y = x.s0 + kb * BK;
-          const int ks = kv_g % C::NSK, vs = kv_g % C::NSV;
-          if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), ((kv_g / C::NSK) & 1) ^ 1, abort_flag,
-                               p.status)))
-            break;
-          mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::kKVTile);
-          issuedK[ks] = (kv_g / C::NSK) & 1;
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(smK + ks * C::kKVTile + pn * (BK * 128), &tmK, bar(C::B_KFULL + ks),
-                        pn * 64, y, x.h);
-          if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), ((kv_g / C::NSV) & 1) ^ 1, abort_flag,
-                               p.status)))
-            break;
-          mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::kKVTile);
-          issuedV[vs] = (kv_g / C::NSV) & 1;
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(smV + vs * C::kKVTile + pn * (BK * 128), &tmV, bar(C::B_VFULL + vs),
-                        pn * 64, y, x.h);
+        const int nsteps = (x.nkv + BPS - 1) / BPS;
+        for (int s = 0; s < nsteps; ++s, ++stp) {
+          int y[BPS];
+#pragma unroll
+          for (int e = 0; e < BPS; ++e) {
+            const int jb = min(s * BPS + e, x.nkv - 1);  // a missing block repeats the last one
+            y[e] = x.s0 + __ldg(p.col_idx + x.kv0 + jb) * BK;
+          }
+          const int st = stp % C::NS;
+          const uint32_t ph = ((stp / C::NS) & 1) ^ 1;
+          if (!(ok = mbar_wait(bar(C::B_KEMPTY + st), ph, abort_flag, p.status))) break;
+          mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::kStage);
+          issuedK[st] = ph ^ 1;
+#pragma unroll
+          for (int e = 0; e < BPS; ++e)
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_load_3d(smK + st * C::kStage + pn * C::kPanel + e * BK * 128, &tmK,
+                          bar(C::B_KFULL + st), pn * 64, y[e], x.h);
+          if (!(ok = mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.status))) break;
+          mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::kStage);
+          issuedV[st] = ph ^ 1;
+#pragma unroll
+          for (int e = 0; e < BPS; ++e)
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_load_3d(smV + st * C::kStage + pn * C::kPanel + e * BK * 128, &tmV,
+                          bar(C::B_VFULL + st), pn * 64, y[e], x.h);
         }
       }
       if (!ok) {  // let every copy already in flight land before the CTA leaves
         if (issuedQ >= 0) mbar_wait_drain(bar(C::B_QFULL), issuedQ);
-        for (int s = 0; s < C::NSK; ++s)
+        for (int s = 0; s < C::NS; ++s) {
           if (issuedK[s] >= 0) mbar_wait_drain(bar(C::B_KFULL + s), issuedK[s]);
-        for (int s = 0; s < C::NSV; ++s)
           if (issuedV[s] >= 0) mbar_wait_drain(bar(C::B_VFULL + s), issuedV[s]);
+        }
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int kv_g = 0, ucount = 0;
-      int kvt[2] = {0, 0}, ut[2] = {0, 0};
+      int stp = 0, ucount = 0;
+      int k[2] = {0, 0};     // steps per M-tile (S / P / O-done phases)
+      int ut[2] = {0, 0};    // units per M-tile (O-free / O-final phases)
       bool ok = true;
-      auto issue_qk = [&](int t, int ks) {
-        const uint32_t qa = smQ + t * C::kQTile, kbse = smK + ks * C::kKVTile;
+      // Descriptors differ only in their low word; K-step offsets within a panel
+      // are compile-time constants, so each MMA costs one add.
+      const uint32_t qlo0 = desc_lo(smQ, 16), klo0 = desc_lo(smK, 16);
+      const uint32_t vlo0 = desc_lo(smV, C::kPanel);
+      const uint32_t dhi = kDescHi;
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t alo = qlo0 + (uint32_t)(t * C::kQTile) / 16u;
+        const uint32_t blo = klo0 + (uint32_t)(st * C::kStage) / 16u;
+        const uint32_t d = tmem + C::colS(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk % 4) * 32u;
-          const uint64_t a = sdesc_sw128(qa + (kk / 4) * 16384 + off, 16, 1024);
-          const uint64_t b = sdesc_sw128(kbse + (kk / 4) * (BK * 128) + off, 16, 1024);
-          mma_bf16_ss(tmem + C::colS(t), a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk % 4) * 2u;
+          mma_ss_lo(d, alo + (kk / 4) * (16384u / 16u) + off,
+                    blo + (kk / 4) * (uint32_t)(C::kPanel / 16) + off, dhi, C::kIdescQK,
+                    kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int vs, bool acc) {
-        const uint32_t pa = smP + t * C::kPTile, vb = smV + vs * C::kKVTile;
+      auto issue_pv = [&](int t, int st, bool acc) {
+        const uint32_t blo = vlo0 + (uint32_t)(st * C::kStage) / 16u;
+        const uint32_t a = tmem + C::colS(t), d = tmem + C::colO(t);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(pa + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(vb + kk * 2048, BK * 128, 1024);
-          mma_bf16_ss(tmem + C::colO(t), a, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kStep / 16; ++kk)
+          mma_ts_lo(d, a + kk * 8, blo + kk * (2048u / 16u), dhi, C::kIdescPV,
+                    (acc || kk > 0) ? 1u : 0u);
       };
+      Unit nx;
+      if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
-        const Unit x = decode_unit(p, u);
+        const Unit x = nx;
+        if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
+        const int nsteps = (x.nkv + BPS - 1) / BPS;
         if (!(ok = mbar_wait(bar(C::B_QFULL), ucount & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        {
-          const int ks = kv_g % C::NSK;
-          if (!(ok = mbar_wait(bar(C::B_KFULL + ks), (kv_g / C::NSK) & 1, abort_flag, p.status)))
+        {  // QK of step 0
+          const int st = stp % C::NS;
+          if (!(ok = mbar_wait(bar(C::B_KFULL + st), (stp / C::NS) & 1, abort_flag, p.status)))
             break;
           tc_fence_after();
           for (int t = 0; t < x.nt; ++t) {
-            issue_qk(t, ks);
+            issue_qk(t, st);
             mma_commit(bar(C::B_SFULL + t));
           }
-          mma_commit(bar(C::B_KEMPTY + ks));
-          if (x.nkv == 1) mma_commit(bar(C::B_QEMPTY));
+          mma_commit(bar(C::B_KEMPTY + st));
+          if (nsteps == 1) mma_commit(bar(C::B_QEMPTY));
         }
-        for (int j = 0; ok && j < x.nkv; ++j) {
-          const int g = kv_g + j;
-          const int vs = g % C::NSV;
-          if (!(ok = mbar_wait(bar(C::B_VFULL + vs), (g / C::NSV) & 1, abort_flag, p.status)))
+        for (int s = 0; ok && s < nsteps; ++s) {
+          const int g = stp + s, st = g % C::NS;
+          const int g1 = g + 1, st1 = g1 % C::NS;
+          const bool more = s + 1 < nsteps;
+          if (!(ok = mbar_wait(bar(C::B_VFULL + st), (g / C::NS) & 1, abort_flag, p.status)))
             break;
           tc_fence_after();
           for (int t = 0; t < x.nt; ++t) {
-            if (!(ok = mbar_wait(bar(C::B_PFULL + t), kvt[t] & 1, abort_flag, p.status))) break;
+            if (!(ok = mbar_wait(bar(C::B_PFULL + t), (k[t] + s) & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            if (j == 0) {
+            if (s == 0) {
               if (!(ok = mbar_wait(bar(C::B_OFREE + t), (ut[t] & 1) ^ 1, abort_flag, p.status)))
                 break;
               tc_fence_after();
             }
-            issue_pv(t, vs, j > 0);
+            issue_pv(t, st, s > 0);
             mma_commit(bar(C::B_ODONE + t));
-            ++kvt[t];
-            if (j + 1 < x.nkv) {
-              const int ks1 = (g + 1) % C::NSK;
+            if (!more) mma_commit(bar(C::B_OFINAL + t));
+            if (more) {
               if (t == 0) {
-                if (!(ok = mbar_wait(bar(C::B_KFULL + ks1), ((g + 1) / C::NSK) & 1, abort_flag,
+                if (!(ok = mbar_wait(bar(C::B_KFULL + st1), (g1 / C::NS) & 1, abort_flag,
                                      p.status)))
                   break;
                 tc_fence_after();
               }
-              issue_qk(t, ks1);
+              issue_qk(t, st1);
               mma_commit(bar(C::B_SFULL + t));
             }
           }
           if (!ok) break;
-          mma_commit(bar(C::B_VEMPTY + vs));
-          if (j + 1 < x.nkv) {
-            mma_commit(bar(C::B_KEMPTY + (g + 1) % C::NSK));
-            if (j + 2 == x.nkv) mma_commit(bar(C::B_QEMPTY));
+          mma_commit(bar(C::B_VEMPTY + st));
+          if (more) {
+            mma_commit(bar(C::B_KEMPTY + st1));
+            if (s + 2 == nsteps) mma_commit(bar(C::B_QEMPTY));
           }
         }
-        for (int t = 0; t < x.nt; ++t) ++ut[t];
-        kv_g += x.nkv;
+        for (int t = 0; t < x.nt; ++t) {
+          k[t] += nsteps;
+          ++ut[t];
+        }
+        stp += nsteps;
       }
       // Every MMA issued so far completes before TMEM is released.
       mma_commit(bar(C::B_FINAL));
@@ -295,55 +432,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp % 4;          // TMEM lane quarter
     const int rho = wq * 32 + lane;   // row of the M-tile
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::colS(t);
     const uint32_t tO = tmem + lane_base + C::colO(t);
-    uint8_t *Prow = sm + C::kOffP + t * C::kPTile + rho * 128;
-    int kvt = 0;
+    const uint32_t tS = tmem + lane_base + C::colS(t);
+    int kstep = 0;                    // steps of this tile (S / P / O-done phases)
+    int units = 0;                    // units of this tile (O-final phases)
     bool ok = true;
+    const uint64_t scale2 = pack2(p.scale_log2, p.scale_log2);
+    Unit nx;
+    if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit x = decode_unit(p, u);
+      const Unit x = nx;
+      if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
       if (t >= x.nt) continue;
+      const int nsteps = (x.nkv + BPS - 1) / BPS;
       const int grow = (2 * x.pair + t) * 128 + rho;   // row within the group's G*b rows
       const bool row_valid = grow < p.G * BK;
       const int hq = x.h * p.G + grow / BK;
-      const int tq = x.r * BK + grow % BK;             // sequence-relative query position
       const int tok_in_blk = grow % BK;
+      const int tq = x.r * BK + tok_in_blk;            // sequence-relative query position
+      // Position of the diagonal block r in the row (the token-level triangle), found
+      // once per unit by the whole warp; -1 if the row does not hold it.
+      int diag_j = -1;
+      for (int j0 = 0; j0 < x.nkv; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, j < x.nkv && __ldg(p.col_idx + x.kv0 + j) == x.r);
+        if (hit != 0u && diag_j < 0) diag_j = j0 + __ffs(hit) - 1;
+      }
       float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < x.nkv; ++j) {
-        const int kb = __ldg(p.col_idx + x.kv0 + j);
-        if (!(ok = mbar_wait(bar(C::B_SFULL + t), kvt & 1, abort_flag, p.status))) break;
+      for (int s = 0; s < nsteps; ++s, ++kstep) {
+        // Column limits of the two 64-column halves of this step: keys past the
+        // query (diagonal block) or past the row's last block are masked.
+        int lim[2] = {64, 64};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int jb = (BPS == 2) ? s * 2 + hh : s;       // block holding this half
+          const int key0 = (BPS == 2) ? 0 : hh * 64;        // first key of the half in its block
+          if (jb >= x.nkv) lim[hh] = 0;
+          else if (jb == diag_j) lim[hh] = max(0, min(64, tok_in_blk - key0 + 1));
+        }
+        if (!(ok = mbar_wait(bar(C::B_SFULL + t), kstep & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        float s[BK];
-#pragma unroll
-        for (int c0 = 0; c0 < BK; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tS + c0, rr);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(rr[c]);
+        float mx;
+        {
+          float v[64];
+          load_masked(tS, lim[0], v);
+          mx = max64(v);
+          load_masked(tS + 64, lim[1], v);
+          mx = fmaxf(mx, max64(v));
         }
-        if (kb == x.r) {  // diagonal block: token-level causal triangle
-#pragma unroll
-          for (int c = 0; c < BK; ++c)
-            if (c > tok_in_blk) s[c] = -INFINITY;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BK; ++c) mx = fmaxf(mx, s[c]);
         const float m_new = fmaxf(m_used, mx * p.scale_log2);
-        if (j > 0) {
-          // PV of the previous block must be done before O is rescaled or P rewritten.
-          if (!(ok = mbar_wait(bar(C::B_ODONE + t), (kvt - 1) & 1, abort_flag, p.status))) break;
-          tc_fence_after();
+        if (s > 0) {
           const bool resc = m_new > m_used + kRescaleThreshold;
           if (__any_sync(0xffffffffu, resc)) {
+            // O must hold PV(s-1) before it is rescaled.
+            if (!(ok = mbar_wait(bar(C::B_ODONE + t), (kstep - 1) & 1, abort_flag, p.status)))
+              break;
+            tc_fence_after();
             const float alpha = resc ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t rr[32];
-              tmem_ld32(tO + c0, rr);
+              uint32_t ro[32];
+              tmem_ld32(tO + c0, ro);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-              tmem_st32(tO + c0, rr);
+              for (int c = 0; c < 32; ++c) ro[c] = __float_as_uint(__uint_as_float(ro[c]) * alpha);
+              tmem_st32(tO + c0, ro);
             }
             l *= alpha;
             if (resc) m_used = m_new;
@@ -352,51 +505,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        float rs = 0.f;
+        const uint64_t negm = pack2(-mref, -mref);
+        uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-        for (int c = 0; c < BK; ++c) {
-          s[c] = fast_exp2(fmaf(s[c], p.scale_log2, -mref));
-          rs += s[c];
-        }
-        l += rs;
-        // P row -> shared memory, 128-byte swizzled K-major (16-byte chunk c8 of row rho at c8 ^ (rho & 7)).
+        for (int hh = 0; hh < 2; ++hh) {
+          // S columns 64 hh .. 64 hh + 63 -> P columns 32 hh .. 32 hh + 31 (the P
+          // half written here overlaps only S columns already read).
+          float v[64];
+          load_masked(tS + 64 * hh, lim[hh], v);
+          uint32_t pk[32];
 #pragma unroll
-        for (int c8 = 0; c8 < BK / 8; ++c8) {
-          const int pn = c8 / 8, ch = c8 % 8;
-          uint4 v;
-          v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-          v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-          v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-          v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-          *reinterpret_cast<uint4 *>(Prow + pn * 16384 + ((ch ^ (rho & 7)) * 16)) = v;
+          for (int c = 0; c < 32; ++c) {
+            const uint64_t z = fma2(pack2(v[2 * c], v[2 * c + 1]), scale2, negm);
+            const float e0 = fast_exp2(lo_of(z)), e1 = fast_exp2(hi_of(z));
+            pk[c] = pack_bf16x2(e0, e1);
+            if (c & 1)
+              acc1 = add2(acc1, pack2(e0, e1));
+            else
+              acc0 = add2(acc0, pack2(e0, e1));
+          }
+          tmem_st32(tS + 32 * hh, pk);
         }
-        fence_proxy_async_smem();
+        const uint64_t acc = add2(acc0, acc1);
+        l += lo_of(acc) + hi_of(acc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
-        ++kvt;
       }
       if (!ok) break;
       // epilogue: O = u / l, lse = (m + log2 l) ln 2
-      if (!(ok = mbar_wait(bar(C::B_ODONE + t), (kvt - 1) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(bar(C::B_OFINAL + t), units & 1, abort_flag, p.status))) break;
+      ++units;
       tc_fence_after();
       const bool store = row_valid && tq < x.n;
       const float inv_l = 1.f / l;
       uint16_t *orow = p.O + ((size_t)hq * p.T + x.s0 + tq) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tO + c0, rr);
+        uint32_t ro[32];
+        tmem_ld32(tO + c0, ro);
         if (store) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 0]) * inv_l, __uint_as_float(rr[q4 * 8 + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 2]) * inv_l, __uint_as_float(rr[q4 * 8 + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 4]) * inv_l, __uint_as_float(rr[q4 * 8 + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 6]) * inv_l, __uint_as_float(rr[q4 * 8 + 7]) * inv_l);
-            dst[q4] = v;
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 0]) * inv_l, __uint_as_float(ro[q4 * 8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 2]) * inv_l, __uint_as_float(ro[q4 * 8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 4]) * inv_l, __uint_as_float(ro[q4 * 8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 6]) * inv_l, __uint_as_float(ro[q4 * 8 + 7]) * inv_l);
+            dst[q4] = w;
           }
         }
       }
@@ -416,8 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
-
-// ---------------------------------------------------------------- host side
 
 template <int D, int BK>
 cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const void *V,
