@@ -44,6 +44,7 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 constexpr int kStep = 128;  // keys per step
+constexpr int kPrefetch = 2;  // steps of K / V prefetched into L2 ahead of their stage load
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D, int BK>
@@ -63,7 +64,7 @@ struct Cfg {
   static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + NS;
   static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
   static constexpr int B_SFULL = B_VEMPTY + NS, B_PFULL = B_SFULL + 2;
-  static constexpr int B_ODONE = B_PFULL + 2, B_OFREE = B_ODONE + 2;
+  static constexpr int B_OFREE = B_PFULL + 2;
   static constexpr int B_OFINAL = B_OFREE + 2;    // all PV of a unit done (once per unit)
   static constexpr int B_FINAL = B_OFINAL + 2;
   static constexpr int kNumBars = B_FINAL + 1;
@@ -146,6 +147,34 @@ BSA_DEV void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
       : "memory");
+}
+
+// Row max over 64 TMEM columns with the reducing load (sm_103a tcgen05.ld.red):
+// each lane gets the max of the columns it loads; two loads, one wait.
+BSA_DEV float tmem_max64(uint32_t taddr) {
+  float r[64], m0, m1;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %64, [%66];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %65, [%67];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
+        "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]),
+        "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]),
+        "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]),
+        "=f"(r[32]), "=f"(r[33]), "=f"(r[34]), "=f"(r[35]), "=f"(r[36]), "=f"(r[37]),
+        "=f"(r[38]), "=f"(r[39]), "=f"(r[40]), "=f"(r[41]), "=f"(r[42]), "=f"(r[43]),
+        "=f"(r[44]), "=f"(r[45]), "=f"(r[46]), "=f"(r[47]), "=f"(r[48]), "=f"(r[49]),
+        "=f"(r[50]), "=f"(r[51]), "=f"(r[52]), "=f"(r[53]), "=f"(r[54]), "=f"(r[55]),
+        "=f"(r[56]), "=f"(r[57]), "=f"(r[58]), "=f"(r[59]), "=f"(r[60]), "=f"(r[61]),
+        "=f"(r[62]), "=f"(r[63]), "=f"(m0), "=f"(m1)
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+  return fmaxf(m0, m1);
 }
 
 // 64 consecutive TMEM columns of this thread's lane: two loads, one wait.
@@ -246,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
       mbar_init(bar(C::B_PFULL + t), 4);
-      mbar_init(bar(C::B_ODONE + t), 1);
       mbar_init(bar(C::B_OFREE + t), 4);
       mbar_init(bar(C::B_OFINAL + t), 1);
     }
@@ -292,8 +320,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smQ + t * C::kQTile + pn * 16384, &tmQ, bar(C::B_QFULL), pn * 64,
                         x.s0 + x.r * BK, hq0);
         }
+        const bool has_next = u + (int)gridDim.x < total_units;
+        if (has_next)  // the next unit's queries come from HBM: start them towards L2 now
+          for (int t = 0; t < nx.nt; ++t)
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_prefetch_l2_3d(&tmQ, pn * 64, nx.s0 + nx.r * BK,
+                                 nx.h * p.G + ((2 * nx.pair + t) * 128) / BK);
         const int nsteps = (x.nkv + BPS - 1) / BPS;
+        const int nsteps_next = has_next ? (nx.nkv + BPS - 1) / BPS : 0;
+        // K / V of the step kPrefetch ahead (possibly in the next unit) go to L2 first,
+        // so the stage loads below hit L2 instead of waiting on HBM.
+        auto prefetch_step = [&](const Unit &w, int s) {
+#pragma unroll
+          for (int e = 0; e < BPS; ++e) {
+            const int jb = min(s * BPS + e, w.nkv - 1);
+            const int y = w.s0 + __ldg(p.col_idx + w.kv0 + jb) * BK;
+            for (int pn = 0; pn < C::kPanels; ++pn) {
+              tma_prefetch_l2_3d(&tmK, pn * 64, y, w.h);
+              tma_prefetch_l2_3d(&tmV, pn * 64, y, w.h);
+            }
+          }
+        };
+        if (u == (int)blockIdx.x)
+          for (int s = 0; s < kPrefetch && s < nsteps; ++s) prefetch_step(x, s);
         for (int s = 0; s < nsteps; ++s, ++stp) {
+          if (s + kPrefetch < nsteps)
+            prefetch_step(x, s + kPrefetch);
+          else if (s + kPrefetch - nsteps < nsteps_next)
+            prefetch_step(nx, s + kPrefetch - nsteps);
           int y[BPS];
 #pragma unroll
           for (int e = 0; e < BPS; ++e) {
@@ -396,7 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             issue_pv(t, st, s > 0);
-            mma_commit(bar(C::B_ODONE + t));
             if (!more) mma_commit(bar(C::B_OFINAL + t));
             if (more) {
               if (t == 0) {
@@ -474,7 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(bar(C::B_SFULL + t), kstep & 1, abort_flag, p.status))) break;
         tc_fence_after();
         float mx;
-        {
+        // tcgen05 loads are warp-collective: the path must be the same for every
+        // lane (the diagonal's limits differ from lane to lane).
+        if (__all_sync(0xffffffffu, lim[0] == 64 && lim[1] == 64)) {  // no mask: reducing loads
+          mx = fmaxf(tmem_max64(tS), tmem_max64(tS + 64));
+        } else {
           float v[64];
           load_masked(tS, lim[0], v);
           mx = max64(v);
@@ -485,10 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s > 0) {
           const bool resc = m_new > m_used + kRescaleThreshold;
           if (__any_sync(0xffffffffu, resc)) {
-            // O must hold PV(s-1) before it is rescaled.
-            if (!(ok = mbar_wait(bar(C::B_ODONE + t), (kstep - 1) & 1, abort_flag, p.status)))
-              break;
-            tc_fence_after();
+            // O already holds PV(s-1): the commit that signalled S(s) was issued
+            // after PV(s-1) and tracks every earlier MMA of the issuing thread.
             const float alpha = resc ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {

@@ -115,6 +115,15 @@ BSA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int
       : "memory");
 }
 
+// Bring one box of a tensor into L2 (no shared memory, no barrier).
+BSA_DEV void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 BSA_DEV void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
