@@ -6,9 +6,11 @@
 //           (request, KV head), max over the group's query heads
 //   select  exact top-k by (score desc, index asc) via a 4-pass radix select,
 //           plus the last page L-1, written in ascending order
-//   attn    split-KV: each CTA merges a few selected pages per warp with the
-//           online-softmax recurrences (eqs.(3)-(5)) in the log2 domain
-//   merge   combines the splits into o and lse
+//   attn    tensor cores: each unit of two selected pages gives a partial
+//           softmax (m, l, u) per query head (eqs.(3)-(5) within the unit)
+//   merge   combines the unit partials of a (request, KV head) into o and lse
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,10 +19,9 @@ namespace {
 
 constexpr int kD = 128;          // decode head_dim
 constexpr int kMaxG = 8;         // query heads per KV head supported (1, 2, 4 or 8)
-constexpr int kPagesPerSplit = 4;
+constexpr int kPage = 64;        // tokens per page
 constexpr int kScoreThreads = 256;
 constexpr int kSelThreads = 256;
-constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- score
 // grid (ceil(max_pages / 64), H_kv, R): 64 logical pages per CTA, 8 per warp.
@@ -195,189 +196,388 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
 }
 
 // ---------------------------------------------------------------- attention
-// grid (nsplit, H_kv, R), 4 warps; warp w of split s handles selected page
-// s * 4 + w.  Lane = 8 * tk + dl: token group tk (4 tokens per step), d-slice dl
-// of 16 elements; K and V rows are read as two 16-byte vectors per lane.
-template <int G>
-__global__ void __launch_bounds__(kPagesPerSplit * 32) dec_attn_kernel(
-    const uint16_t *__restrict__ q, const uint16_t *__restrict__ kc,
-    const uint16_t *__restrict__ vc, const int32_t *__restrict__ bt,
-    const int32_t *__restrict__ lens, const int32_t *__restrict__ sel,
-    const int32_t *__restrict__ sel_counts, float scale_log2, float *__restrict__ part_ml,
-    float *__restrict__ part_o, int H, int Hk, int max_pages, int top_k, int nsplit) {
-  __shared__ float qs[G][kD];
-  __shared__ float wm[kPagesPerSplit][G], wl[kPagesPerSplit][G];
-  __shared__ float wo[kPagesPerSplit][G][kD];
-  const int rho = blockIdx.z, h = blockIdx.y, split = blockIdx.x;
-  const int n = lens[rho];
-  const int cnt = sel_counts[(size_t)rho * Hk + h];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tk = lane / 8, dl = lane % 8;
-  for (int e = threadIdx.x; e < G * kD; e += blockDim.x)
-    qs[e / kD][e % kD] = bf16_to_f32(q[((size_t)rho * H + h * G + e / kD) * kD + e % kD]) * scale_log2;
-  __syncthreads();
+// Persistent, one CTA per SM, on the tensor cores.  A unit is two selected pages
+// of one (request, KV head) — 128 keys — and yields one partial (m, l, u) per
+// query head of the group:
+//   S^T = K Q^T   M = 128 keys,  N = 16 (the group's queries, padded), K = d
+//   O^T = V^T P^T M = d = 128,   N = 16,                                K = 128 keys
+// A unit holding one page only reads the second page at an out-of-range page
+// coordinate, which the tensor copy fills with zeros, and masks its keys.
+// Warp roles (192 threads):
+//   warps 0-3  softmax + epilogue: thread = one key row of S^T (TMEM lane), then
+//              one d row of O^T
+//   warp 4     producer: resolves the page indices of 32 units at a time, then
+//              stages K, V (two 64-column panels x two pages) and Q by TMA
+//   warp 5     MMA issuer (one thread); owns the TMEM allocation
+// TMEM (64 columns): S_0, S_1, O_0, O_1 (16 columns each), double-buffered by unit.
+constexpr int kDecThreads = 192;
+constexpr int kDecProducer = 4;
+constexpr int kDecMma = 5;
+constexpr int kNS = 3;                       // K/V/Q stages
+constexpr int kKVBytes = 2 * kPage * kD * 2;  // two pages of K (or V): 32 KB
+constexpr int kQPanel = 16 * 128;             // 16 rows x 128 bytes
+constexpr int kQRows = 8;                     // query rows copied (G <= 8)
+constexpr int kStageBytes = 2 * kKVBytes + 2 * kQPanel;  // K | V | Q
+constexpr int kPBytes = 2 * kQPanel;          // P^T: 16 rows x 128 keys (two panels)
+constexpr int kTxBytes = 2 * kKVBytes + 2 * kQRows * 128;
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffStages = 0;
+constexpr int kOffP = kOffStages + kNS * kStageBytes;
+constexpr int kOffHdr = kOffP + 2 * kPBytes;        // per stage: unit, valid A, valid B
+constexpr int kOffRed = kOffHdr + kNS * 16;          // [2][4][16] max, [2][4][16] sum
+constexpr int kOffBar = kOffRed + 2 * 2 * 4 * 16 * 4;
+// barriers: FULL[kNS], EMPTY[kNS], SFULL[2], PFULL[2], OFULL[2], MX[2], LS[2], FINAL
+constexpr int B_FULL = 0, B_EMPTY = kNS, B_SFULL = 2 * kNS, B_PFULL = B_SFULL + 2,
+              B_OFULL = B_PFULL + 2, B_MX = B_OFULL + 2, B_LS = B_MX + 2, B_FIN = B_LS + 2;
+constexpr int kNumBars = B_FIN + 1;
+constexpr int kOffCtl = kOffBar + kNumBars * 8;     // tmem base, abort flag
+constexpr int kDecSmem = kOffCtl + 16 + 1024;
+static_assert(kDecSmem <= 232448, "shared memory budget");
+constexpr uint32_t kColS = 0, kColO = 32;
+// kind::f16 descriptors: QK with both operands K-major; PV with A (= V^T) MN-major.
+constexpr uint32_t kIdescQK = idesc_bf16(128, 16, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 16, false) | (1u << 15);
 
-  float m[G], l[G], o[G][16];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) o[g][e] = 0.f;
+struct DecParams {
+  const int32_t *bt, *lens, *sel, *sel_counts;
+  float *part_ml, *part_o;
+  int32_t *status;
+  float scale_log2;
+  int H, Hk, G, max_pages, top_k, nchunk, units, oob_page;
+};
+
+BSA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+BSA_DEV void bar_warps_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_flag,
+                            int32_t *status, bool &ok) {
+  ok = ok && mbar_wait(bar, parity, abort_flag, status);
+  ok = __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+    dec_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const DecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (sbase - raw);
+  auto bar = [&](int k) { return sbase + kOffBar + 8u * (uint32_t)k; };
+  int32_t *hdr = reinterpret_cast<int32_t *>(sm + kOffHdr);
+  float *red_m = reinterpret_cast<float *>(sm + kOffRed);
+  float *red_l = red_m + 2 * 4 * 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffCtl);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + kOffCtl + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_PFULL + b), 4);
+      mbar_init(bar(B_OFULL + b), 1);
+      mbar_init(bar(B_MX + b), 4);
+      mbar_init(bar(B_LS + b), 4);
+    }
+    mbar_init(bar(B_FIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  const int pi = split * kPagesPerSplit + warp;
-  if (pi < cnt) {
-    const int lp = sel[((size_t)rho * Hk + h) * (top_k + 1) + pi];
-    const int phys = bt[(size_t)rho * max_pages + lp];
-    const int valid = min(64, n - lp * 64);
-    const uint16_t *kp = kc + ((size_t)phys * Hk + h) * 64 * kD;
-    const uint16_t *vp = vc + ((size_t)phys * Hk + h) * 64 * kD;
-    float s[16][G];
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int tok = it * 4 + tk;
-      const uint4 *kr = reinterpret_cast<const uint4 *>(kp + (size_t)tok * kD + dl * 16);
-      const uint4 a = __ldg(kr), b = __ldg(kr + 1);
-      float kv[16];
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        kv[2 * e] = __uint_as_float(w[e] << 16);
-        kv[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (g < G) {
-          float acc = 0.f;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc = fmaf(qs[g][dl * 16 + e], kv[e], acc);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          s[it][g] = tok < valid ? acc : -INFINITY;
-        }
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (g < G) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int it = 0; it < 16; ++it) mx = fmaxf(mx, s[it][g]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        m[g] = mx;  // one page per warp: the first tile sets the running max
-        float sum = 0.f;
-#pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          s[it][g] = fast_exp2(s[it][g] - mx);
-          sum += s[it][g];
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-        l[g] = sum;
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int tok = it * 4 + tk;
-      const uint4 *vr = reinterpret_cast<const uint4 *>(vp + (size_t)tok * kD + dl * 16);
-      const uint4 a = __ldg(vr), b = __ldg(vr + 1);
-      float vv[16];
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        vv[2 * e] = __uint_as_float(w[e] << 16);
-        vv[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        if (g < G)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[g][e] = fmaf(s[it][g], vv[e], o[g][e]);
-    }
-    // sum the four token groups
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (g < G)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 8);
-          o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
-        }
+  if (warp == kDecMma) {
+    tmem_alloc(smem_u32(tmem_slot), 64);
+    tmem_relinquish();
   }
-  // Combine the warps of this split (eqs.(3)-(5)) through shared memory.
-  if (lane == 0)
-    for (int g = 0; g < G; ++g) {
-      wm[warp][g] = m[g];
-      wl[warp][g] = l[g];
-    }
-  if (tk == 0)
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 16; ++e) wo[warp][g][dl * 16 + e] = o[g][e];
+  if (warp == kDecProducer && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
   __syncthreads();
-  const size_t base = (((size_t)rho * Hk + h) * nsplit + split) * G;
-  for (int idx = threadIdx.x; idx < G * kD; idx += blockDim.x) {
-    const int g = idx / kD, c = idx % kD;
-    float M = -INFINITY;
-    for (int w = 0; w < kPagesPerSplit; ++w) M = fmaxf(M, wm[w][g]);
-    float Lsum = 0.f, acc = 0.f;
-    if (M != -INFINITY)
-      for (int w = 0; w < kPagesPerSplit; ++w) {
-        if (wm[w][g] == -INFINITY) continue;
-        const float f = fast_exp2(wm[w][g] - M);
-        Lsum += f * wl[w][g];
-        acc += f * wo[w][g][c];
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int per_pair = p.top_k + 1;
+
+  if (warp == kDecProducer) {
+    // ------------------------------------------------------------ producer
+    int j = 0;
+    int last[kNS];
+    for (int s = 0; s < kNS; ++s) last[s] = -1;
+    bool ok = true;
+    for (int b0 = blockIdx.x; ok && b0 < p.units; b0 += 32 * gridDim.x) {
+      const int u = b0 + lane * gridDim.x;
+      int zA = 0, zB = 0, qrow = 0, vA = 0, vB = 0;
+      bool live = false;
+      if (u < p.units) {
+        const int pair = u / p.nchunk, c = u - pair * p.nchunk;
+        const int cnt = __ldg(p.sel_counts + pair);
+        if (2 * c < cnt) {
+          live = true;
+          const int rho = pair / p.Hk, h = pair - rho * p.Hk;
+          const int n = __ldg(p.lens + rho);
+          const int32_t *sp = p.sel + (size_t)pair * per_pair + 2 * c;
+          const int lpA = __ldg(sp);
+          zA = __ldg(p.bt + (size_t)rho * p.max_pages + lpA) * p.Hk + h;
+          vA = min(kPage, n - lpA * kPage);
+          if (2 * c + 1 < cnt) {
+            const int lpB = __ldg(sp + 1);
+            zB = __ldg(p.bt + (size_t)rho * p.max_pages + lpB) * p.Hk + h;
+            vB = min(kPage, n - lpB * kPage);
+          } else {
+            zB = p.oob_page;  // zero-filled by the copy, keys masked
+          }
+          qrow = rho * p.H + h * p.G;
+        }
       }
-    part_o[(base + g) * kD + c] = acc;
-    if (c == 0) {
-      part_ml[(base + g) * 2] = M;
-      part_ml[(base + g) * 2 + 1] = Lsum;
+      uint32_t todo = __ballot_sync(0xffffffffu, live);
+      while (todo != 0u) {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int uu = __shfl_sync(0xffffffffu, u, src);
+        const int a = __shfl_sync(0xffffffffu, zA, src);
+        const int b = __shfl_sync(0xffffffffu, zB, src);
+        const int qr = __shfl_sync(0xffffffffu, qrow, src);
+        const int va = __shfl_sync(0xffffffffu, vA, src);
+        const int vb = __shfl_sync(0xffffffffu, vB, src);
+        if (lane == 0) {
+          const int st = j % kNS;
+          const uint32_t ph = ((j / kNS) & 1) ^ 1;
+          ok = mbar_wait(bar(B_EMPTY + st), ph, abort_flag, p.status);
+          if (ok) {
+            hdr[st * 4 + 0] = uu;
+            hdr[st * 4 + 1] = va;
+            hdr[st * 4 + 2] = vb;
+            const uint32_t full = bar(B_FULL + st);
+            mbar_arrive_expect_tx(full, kTxBytes);
+            last[st] = ph ^ 1;
+            const uint32_t stg = sbase + kOffStages + st * kStageBytes;
+            for (int pn = 0; pn < 2; ++pn) {
+              tma_load_3d(stg + pn * 16384, &tmK, full, pn * 64, 0, a);
+              tma_load_3d(stg + pn * 16384 + 8192, &tmK, full, pn * 64, 0, b);
+            }
+            for (int pn = 0; pn < 2; ++pn)
+              tma_load_3d(stg + 2 * kKVBytes + pn * kQPanel, &tmQ, full, pn * 64, qr, 0);
+            for (int pn = 0; pn < 2; ++pn) {
+              tma_load_3d(stg + kKVBytes + pn * 16384, &tmV, full, pn * 64, 0, a);
+              tma_load_3d(stg + kKVBytes + pn * 16384 + 8192, &tmV, full, pn * 64, 0, b);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++j;
+      }
     }
+    if (lane == 0) {
+      if (ok) {  // end of work: a stage whose header holds unit -1
+        const int st = j % kNS;
+        if (mbar_wait(bar(B_EMPTY + st), ((j / kNS) & 1) ^ 1, abort_flag, p.status)) {
+          hdr[st * 4 + 0] = -1;
+          mbar_arrive(bar(B_FULL + st));
+        }
+      } else {  // copies in flight land before the CTA leaves
+        for (int s = 0; s < kNS; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar(B_FULL + s), last[s]);
+      }
+    }
+  } else if (warp == kDecMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t stg0 = sbase + kOffStages, pb0 = sbase + kOffP;
+      auto qk = [&](int i) {
+        const int st = i % kNS, b = i & 1;
+        const uint32_t k0 = stg0 + st * kStageBytes, q0 = k0 + 2 * kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16_ss(tmem + kColS + 16 * b,
+                      sdesc_sw128(k0 + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                      sdesc_sw128(q0 + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024), kIdescQK,
+                      kk > 0 ? 1u : 0u);
+        mma_commit(bar(B_SFULL + b));
+      };
+      auto pv = [&](int i) {
+        const int st = i % kNS, b = i & 1;
+        const uint32_t v0 = stg0 + st * kStageBytes + kKVBytes, p0 = pb0 + b * kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 2 * kPage / 16; ++kk)
+          mma_bf16_ss(tmem + kColO + 16 * b, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
+                      sdesc_sw128(p0 + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024), kIdescPV,
+                      kk > 0 ? 1u : 0u);
+        mma_commit(bar(B_OFULL + b));
+        mma_commit(bar(B_EMPTY + st));
+      };
+      bool ok = mbar_wait(bar(B_FULL + 0), 0, abort_flag, p.status);
+      bool more = ok && hdr[0] >= 0;
+      if (more) {
+        tc_fence_after();
+        qk(0);
+      }
+      for (int i = 0; more; ++i) {
+        // QK of the next unit goes ahead of PV of this one
+        const int i1 = i + 1, st1 = i1 % kNS;
+        if (!(ok = mbar_wait(bar(B_FULL + st1), (i1 / kNS) & 1, abort_flag, p.status))) break;
+        const bool next = hdr[st1 * 4] >= 0;
+        if (next) {
+          tc_fence_after();
+          qk(i1);
+        }
+        if (!(ok = mbar_wait(bar(B_PFULL + (i & 1)), (i / 2) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        pv(i);
+        more = next;
+      }
+      // Every MMA issued so far completes before TMEM is released.
+      mma_commit(bar(B_FIN));
+      mbar_wait_drain(bar(B_FIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp * 32 + lane;  // key row of S^T, then d row of O^T
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // byte offset of P^T[g][t] inside one P buffer (128-byte swizzle, 8-row atoms)
+    const uint32_t t_panel = (uint32_t)(t >> 6) * kQPanel, t_chunk = (uint32_t)((t & 63) >> 3),
+                   t_in = (uint32_t)(t & 7) * 2;
+    bool ok = true;
+    for (int i = 0;; ++i) {
+      const int st = i % kNS, b = i & 1;
+      bar_warps_wait(bar(B_FULL + st), (i / kNS) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      const int u = hdr[st * 4 + 0];
+      if (u < 0) break;
+      const int va = hdr[st * 4 + 1], vb = hdr[st * 4 + 2];
+      const bool valid = t < kPage ? t < va : t - kPage < vb;
+      bar_warps_wait(bar(B_SFULL + b), (i / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + kColS + 16 * b, r);
+      float x[kMaxG];
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g) {
+        x[g] = valid ? __uint_as_float(r[g]) * p.scale_log2 : -INFINITY;
+        float m = x[g];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) red_m[(b * 4 + warp) * 16 + g] = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_MX + b));
+      bar_warps_wait(bar(B_MX + b), (i / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      float M[kMaxG], l[kMaxG];
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g) {
+        M[g] = fmaxf(fmaxf(red_m[(b * 4 + 0) * 16 + g], red_m[(b * 4 + 1) * 16 + g]),
+                     fmaxf(red_m[(b * 4 + 2) * 16 + g], red_m[(b * 4 + 3) * 16 + g]));
+        // a unit's first page always holds a valid key, so M is finite
+        const float pg = g < p.G ? fast_exp2(x[g] - M[g]) : 0.f;
+        l[g] = pg;
+        const __nv_bfloat16 pb = __float2bfloat16_rn(pg);
+        const uint32_t off = t_panel + (uint32_t)g * 128u + ((t_chunk ^ (uint32_t)(g & 7)) << 4) + t_in;
+        *reinterpret_cast<__nv_bfloat16 *>(sm + kOffP + b * kPBytes + off) = pb;
+      }
+      // Rows 8-15 of P^T are never written: they only feed columns of O^T that are
+      // never read (likewise rows 8-15 of the staged queries).
+      fence_proxy_async_smem();  // P^T is read by the tensor cores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + b));
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g) {
+        float sum = l[g];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) red_l[(b * 4 + warp) * 16 + g] = sum;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_LS + b));
+      // epilogue: O^T row t of this unit
+      bar_warps_wait(bar(B_OFULL + b), (i / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      tc_fence_after();
+      tmem_ld16(tmem + lane_base + kColO + 16 * b, r);
+      float *po = p.part_o + (size_t)u * p.G * kD;
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g)
+        if (g < p.G) po[g * kD + t] = __uint_as_float(r[g]);
+      bar_warps_wait(bar(B_LS + b), (i / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      if (t < p.G) {
+        float lsum = 0.f, mt = 0.f;
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g)
+          if (g == t) {
+            lsum = red_l[(b * 4 + 0) * 16 + g] + red_l[(b * 4 + 1) * 16 + g] +
+                   red_l[(b * 4 + 2) * 16 + g] + red_l[(b * 4 + 3) * 16 + g];
+            mt = M[g];
+          }
+        p.part_ml[((size_t)u * p.G + t) * 2] = mt;
+        p.part_ml[((size_t)u * p.G + t) * 2 + 1] = lsum;
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kDecMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, 64);
   }
 }
 
-// grid (H_kv, R), 128 threads: combine the splits of every query head of the group.
-__global__ void __launch_bounds__(128) dec_merge_kernel(
-    const float *__restrict__ part_ml, const float *__restrict__ part_o, uint16_t *__restrict__ o,
-    float *__restrict__ lse, int H, int Hk, int nsplit) {
+// grid (H_kv, R), G * 128 threads (one output element each): combine the unit
+// partials of a (request, KV head) with eqs.(3)-(5) in the log2 domain.
+__global__ void __launch_bounds__(kMaxG * kD) dec_merge_kernel(
+    const float *__restrict__ part_ml, const float *__restrict__ part_o,
+    const int32_t *__restrict__ sel_counts, uint16_t *__restrict__ o, float *__restrict__ lse,
+    int H, int Hk, int nchunk) {
   const int rho = blockIdx.y, h = blockIdx.x;
   const int G = H / Hk;
-  for (int idx = threadIdx.x; idx < G * kD; idx += blockDim.x) {
-    const int g = idx / kD, c = idx % kD;
-    const size_t base = ((size_t)rho * Hk + h) * nsplit;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[((base + s) * G + g) * 2]);
-    float Lsum = 0.f, acc = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float ms = part_ml[((base + s) * G + g) * 2];
-      if (ms == -INFINITY) continue;
-      const float f = fast_exp2(ms - M);
-      Lsum += f * part_ml[((base + s) * G + g) * 2 + 1];
-      acc += f * part_o[((base + s) * G + g) * kD + c];
-    }
-    const int hq = h * G + g;
-    const __nv_bfloat16 ob = __float2bfloat16_rn(acc / Lsum);
-    o[((size_t)rho * H + hq) * kD + c] = *reinterpret_cast<const uint16_t *>(&ob);
-    if (lse != nullptr && c == 0) lse[(size_t)rho * H + hq] = (M + log2f(Lsum)) * 0.6931471805599453f;
+  const int pair = rho * Hk + h;
+  const int g = threadIdx.x / kD, c = threadIdx.x % kD;
+  const int nu = (sel_counts[pair] + 1) / 2;
+  const size_t u0 = (size_t)pair * nchunk;
+  float M = -INFINITY;
+  for (int k = 0; k < nu; ++k) M = fmaxf(M, part_ml[((u0 + k) * G + g) * 2]);
+  float Lsum = 0.f, acc = 0.f;
+  for (int k = 0; k < nu; ++k) {
+    const float f = fast_exp2(part_ml[((u0 + k) * G + g) * 2] - M);
+    Lsum += f * part_ml[((u0 + k) * G + g) * 2 + 1];
+    acc += f * part_o[((u0 + k) * G + g) * kD + c];
   }
+  const int hq = h * G + g;
+  const __nv_bfloat16 ob = __float2bfloat16_rn(acc / Lsum);
+  o[((size_t)rho * H + hq) * kD + c] = *reinterpret_cast<const uint16_t *>(&ob);
+  if (lse != nullptr && c == 0) lse[(size_t)rho * H + hq] = (M + log2f(Lsum)) * 0.6931471805599453f;
 }
 
-int num_splits(const bsa_decode_shape_t &s) {
-  return (s.top_k + 1 + kPagesPerSplit - 1) / kPagesPerSplit;
-}
+int num_chunks(const bsa_decode_shape_t &s) { return (s.top_k + 2) / 2; }
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// Workspace: scores [R, H_kv, max_pages] | unit partials (m, l) | unit partials u.
 size_t decode_workspace_bytes(const bsa_decode_shape_t &s) {
   const size_t G = (size_t)(s.num_heads / s.num_kv_heads);
+  const size_t units = (size_t)s.num_reqs * s.num_kv_heads * num_chunks(s);
   const size_t pairs = (size_t)s.num_reqs * s.num_kv_heads;
-  const size_t scores = pairs * s.max_pages_per_req * sizeof(float);
-  const size_t ml = pairs * num_splits(s) * G * 2 * sizeof(float);
-  const size_t ob = pairs * num_splits(s) * G * kD * sizeof(float);
-  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return up(scores) + up(ml) + up(ob);
+  return up256(pairs * s.max_pages_per_req * sizeof(float)) + up256(units * G * 2 * sizeof(float)) +
+         up256(units * G * kD * sizeof(float));
 }
 
 cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void *k_cache,
@@ -385,17 +585,23 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
                           const int32_t *block_table, const int32_t *context_lens, float scale,
                           void *o, float *lse, int32_t *sel, int32_t *sel_counts,
                           int32_t *dev_status, void *ws, cudaStream_t st) {
-  (void)dev_status;
-  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const int G = s.num_heads / s.num_kv_heads;
-  const int nsplit = num_splits(s);
+  const int nchunk = num_chunks(s);
   const size_t pairs = (size_t)s.num_reqs * s.num_kv_heads;
+  const size_t units = pairs * nchunk;
   char *w = static_cast<char *>(ws);
   float *scores = reinterpret_cast<float *>(w);
-  w += up(pairs * s.max_pages_per_req * sizeof(float));
+  w += up256(pairs * s.max_pages_per_req * sizeof(float));
   float *part_ml = reinterpret_cast<float *>(w);
-  w += up(pairs * nsplit * G * 2 * sizeof(float));
+  w += up256(units * G * 2 * sizeof(float));
   float *part_o = reinterpret_cast<float *>(w);
+
+  CUtensorMap mq, mk, mv;
+  const uint64_t zpages = (uint64_t)s.num_phys_pages * s.num_kv_heads;
+  if (!make_tmap_3d_bf16(&mq, q, kD, (uint64_t)s.num_reqs * s.num_heads, 1, 64, kQRows, 1) ||
+      !make_tmap_3d_bf16(&mk, k_cache, kD, kPage, zpages, 64, kPage, 1) ||
+      !make_tmap_3d_bf16(&mv, v_cache, kD, kPage, zpages, 64, kPage, 1))
+    return cudaErrorInvalidValue;
 
   const uint16_t *qb = static_cast<const uint16_t *>(q);
   dec_score_kernel<<<dim3((s.max_pages_per_req + 63) / 64, s.num_kv_heads, s.num_reqs),
@@ -413,25 +619,33 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
       scores, context_lens, sel, sel_counts, s.num_kv_heads, s.max_pages_per_req, s.top_k);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const float scale_log2 = scale * 1.4426950408889634f;
-  const dim3 agrid(nsplit, s.num_kv_heads, s.num_reqs);
-#define BSA_DEC_ATTN(GG)                                                                      \
-  dec_attn_kernel<GG><<<agrid, kPagesPerSplit * 32, 0, st>>>(                                 \
-      qb, static_cast<const uint16_t *>(k_cache), static_cast<const uint16_t *>(v_cache),     \
-      block_table, context_lens, sel, sel_counts, scale_log2, part_ml, part_o, s.num_heads,   \
-      s.num_kv_heads, s.max_pages_per_req, s.top_k, nsplit)
-  switch (G) {
-    case 1: BSA_DEC_ATTN(1); break;
-    case 2: BSA_DEC_ATTN(2); break;
-    case 4: BSA_DEC_ATTN(4); break;
-    case 8: BSA_DEC_ATTN(8); break;
-    default: return cudaErrorInvalidValue;
-  }
-#undef BSA_DEC_ATTN
+
+  DecParams p;
+  p.bt = block_table;
+  p.lens = context_lens;
+  p.sel = sel;
+  p.sel_counts = sel_counts;
+  p.part_ml = part_ml;
+  p.part_o = part_o;
+  p.status = dev_status;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.H = s.num_heads;
+  p.Hk = s.num_kv_heads;
+  p.G = G;
+  p.max_pages = s.max_pages_per_req;
+  p.top_k = s.top_k;
+  p.nchunk = nchunk;
+  p.units = (int)units;
+  p.oob_page = (int)zpages;
+  e = cudaFuncSetAttribute(dec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<size_t>((size_t)num_sms(), units);
+  dec_tc_kernel<<<grid, kDecThreads, kDecSmem, st>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dec_merge_kernel<<<dim3(s.num_kv_heads, s.num_reqs), 128, 0, st>>>(
-      part_ml, part_o, static_cast<uint16_t *>(o), lse, s.num_heads, s.num_kv_heads, nsplit);
+  dec_merge_kernel<<<dim3(s.num_kv_heads, s.num_reqs), G * kD, 0, st>>>(
+      part_ml, part_o, sel_counts, static_cast<uint16_t *>(o), lse, s.num_heads, s.num_kv_heads,
+      nchunk);
   return cudaGetLastError();
 }
 
