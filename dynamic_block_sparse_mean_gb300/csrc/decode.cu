@@ -24,33 +24,81 @@ constexpr int kScoreThreads = 256;
 constexpr int kSelThreads = 256;
 
 // ---------------------------------------------------------------- score
-// grid (ceil(max_pages / 64), H_kv, R): 64 logical pages per CTA, 8 per warp.
+// grid (ceil(max_pages / 64), R): 64 logical pages of one request per CTA, for
+// every KV head.  The CTA stages the pages' block-table entries and the request's
+// queries once (fp32 rows of kQStride floats in dynamic shared memory); each warp
+// then takes (KV head, 8 pages) items.  Every load instruction reads one whole
+// 512-byte summary row (lane = float4 column), so a warp's request touches four
+// cache lines; the 8 G partial dot products per lane are then summed across the
+// warp by a reduce-scatter (31 shuffles for G = 4 instead of 5 per dot product).
+constexpr int kQStride = kD + 4;
+
+// Reduce-scatter of N per-lane partial sums over the 32 lanes of a warp (halving
+// butterfly): at offset o a lane keeps the half of its values selected by bit o
+// of its lane index and adds its partner's copy of that half.  With N = 8 G
+// values indexed j = 8-page row * G + head, lane l ends with the full sums of
+// j = l >> (5 - log2 N) (N <= 32: the remaining offsets add plainly) or of
+// j = 2 l, 2 l + 1 (N = 64): in every case row = l >> 2.
+template <int N, int O>
+BSA_DEV void rs_step(float (&v)[64], int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (N > 1) {
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[i + N / 2];
+        const float keep = up ? v[i + N / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      rs_step<N / 2, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      rs_step<1, O / 2>(v, lane);
+    }
+  }
+}
+
+template <int G>
 __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
     const uint16_t *__restrict__ q, const float *__restrict__ ps, const int32_t *__restrict__ bt,
-    const int32_t *__restrict__ lens, float *__restrict__ scores, int H, int Hk, int max_pages) {
-  __shared__ float qs[kMaxG][kD];
-  const int rho = blockIdx.z, h = blockIdx.y;
-  const int G = H / Hk;
-  const int L = (lens[rho] + 63) / 64;  // page_size 64
+    const int32_t *__restrict__ lens, float *__restrict__ scores, int Hk, int max_pages) {
+  extern __shared__ __align__(16) float qs[];  // [H][kQStride]
+  __shared__ int phys_s[64];
+  const int rho = blockIdx.y;
+  const int H = G * Hk;
+  const int L = (lens[rho] + kPage - 1) / kPage;
   const int p_begin = blockIdx.x * 64;
   if (p_begin >= L - 1) return;
-  for (int e = threadIdx.x; e < G * kD; e += blockDim.x)
-    qs[e / kD][e % kD] = bf16_to_f32(q[((size_t)rho * H + h * G + e / kD) * kD + e % kD]);
+  const int npg = min(L - 1, p_begin + 64) - p_begin;
+  if (threadIdx.x < npg) phys_s[threadIdx.x] = __ldg(bt + (size_t)rho * max_pages + p_begin + threadIdx.x);
+  for (int e = threadIdx.x; e < H * kD; e += blockDim.x)
+    qs[(e / kD) * kQStride + e % kD] = bf16_to_f32(q[(size_t)rho * H * kD + e]);
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int p_end = min(L - 1, p_begin + 64);
-  for (int p = p_begin + warp; p < p_end; p += kScoreThreads / 32) {
-    const int phys = bt[(size_t)rho * max_pages + p];
-    const float4 c = __ldg(reinterpret_cast<const float4 *>(ps + ((size_t)phys * Hk + h) * kD) + lane);
-    float best = -INFINITY;
-    for (int g = 0; g < G; ++g) {
-      float s = qs[g][4 * lane] * c.x + qs[g][4 * lane + 1] * c.y + qs[g][4 * lane + 2] * c.z +
-                qs[g][4 * lane + 3] * c.w;
+  const int ngrp = (npg + 7) / 8;
+  for (int item = warp; item < Hk * ngrp; item += kScoreThreads / 32) {
+    const int h = item / ngrp, p0 = (item - h * ngrp) * 8;
+    float4 c[8];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      best = fmaxf(best, s);
+    for (int k = 0; k < 8; ++k) {  // a missing page of the last group repeats the first
+      const int pg = p0 + k < npg ? p0 + k : p0;
+      c[k] = __ldg(reinterpret_cast<const float4 *>(ps + ((size_t)phys_s[pg] * Hk + h) * kD) + lane);
     }
-    if (lane == 0) scores[((size_t)rho * Hk + h) * max_pages + p] = best;
+    float v[64];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float4 qq = *reinterpret_cast<const float4 *>(qs + (h * G + g) * kQStride + 4 * lane);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k * G + g] = qq.x * c[k].x + qq.y * c[k].y + qq.z * c[k].z + qq.w * c[k].w;
+    }
+    rs_step<8 * G, 16>(v, lane);
+    float best = G == 8 ? fmaxf(v[0], v[1]) : v[0];  // max over the group's heads
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
+    const int row = lane >> 2;
+    if ((lane & 3) == 0 && p0 + row < npg)
+      scores[((size_t)rho * Hk + h) * max_pages + p_begin + p0 + row] = best;
   }
 }
 
@@ -604,10 +652,26 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
     return cudaErrorInvalidValue;
 
   const uint16_t *qb = static_cast<const uint16_t *>(q);
-  dec_score_kernel<<<dim3((s.max_pages_per_req + 63) / 64, s.num_kv_heads, s.num_reqs),
-                     kScoreThreads, 0, st>>>(qb, page_summ, block_table, context_lens, scores,
-                                             s.num_heads, s.num_kv_heads, s.max_pages_per_req);
-  cudaError_t e = cudaGetLastError();
+  const int qs_bytes = s.num_heads * kQStride * (int)sizeof(float);
+  const dim3 sgrid((s.max_pages_per_req + 63) / 64, s.num_reqs);
+  cudaError_t e;
+#define BSA_DEC_SCORE(GG)                                                                     \
+  do {                                                                                        \
+    e = cudaFuncSetAttribute(dec_score_kernel<GG>,                                            \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, qs_bytes);          \
+    if (e != cudaSuccess) return e;                                                           \
+    dec_score_kernel<GG><<<sgrid, kScoreThreads, qs_bytes, st>>>(                             \
+        qb, page_summ, block_table, context_lens, scores, s.num_kv_heads, s.max_pages_per_req); \
+  } while (0)
+  switch (G) {
+    case 1: BSA_DEC_SCORE(1); break;
+    case 2: BSA_DEC_SCORE(2); break;
+    case 4: BSA_DEC_SCORE(4); break;
+    case 8: BSA_DEC_SCORE(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef BSA_DEC_SCORE
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t sm = (size_t)s.max_pages_per_req * sizeof(uint32_t);
   if (sm > 40 * 1024) {

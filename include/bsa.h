@@ -92,8 +92,8 @@ typedef struct {
 /* Paged decode shape ([P2] §2.2 decode; §3.1 paged KV cache and block table). */
 typedef struct {
   int32_t num_reqs;          /* R requests, one query token each                 */
-  int32_t num_heads;         /* H                                                */
-  int32_t num_kv_heads;      /* H_kv, H % H_kv == 0                              */
+  int32_t num_heads;         /* H <= 256                                         */
+  int32_t num_kv_heads;      /* H_kv, H / H_kv in {1, 2, 4, 8}                   */
   int32_t head_dim;          /* 128                                              */
   int32_t page_size;         /* tokens per page = routing block: 64              */
   int32_t max_pages_per_req; /* columns of block_table                           */
