@@ -36,7 +36,9 @@ sys.path.insert(0, ROOT)
 METRIC = "block-sparse attn TFLOP/s on selected tiles + router ms; decode KV GB/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_ATTN = os.path.join(ROOT, "profiles", "attn_tc_prompt32k.md")
+PROFILE_ATTN = {name: os.path.join(ROOT, "profiles", f"attn_tc_{tag}.md")
+                for name, tag in (("prompt", "prompt32k"), ("varlen", "varlen256k"),
+                                  ("long", "long128k"), ("tiny", "tiny"))}
 ATTN_SOURCE = os.path.join(ROOT, "dynamic_block_sparse_mean_gb300", "csrc", "attn_tc.cu")
 
 
@@ -46,10 +48,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="prompt")
+    ap.add_argument("--workload", default="prompt", choices=["tiny", "prompt", "varlen", "long"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the paged decode (a diagnostic line, e.g. for profiling)")
+    ap.add_argument("--decode-reqs", type=int, default=None,
+                    help="run the decode workload on its first N requests (default: all)")
     return ap.parse_args(argv)
 
 
@@ -263,19 +269,20 @@ def bench_e2e(res, steps, device):
     return ms, bi, bo
 
 
-def bench_decode(steps, warmup, device):
+def bench_decode(steps, warmup, device, num_reqs=None):
     import dynamic_block_sparse_mean_gb300 as bsa
     from dynamic_block_sparse_mean_gb300 import accounting, synth
     from dynamic_block_sparse_mean_gb300.workloads import DECODE_64 as w
 
-    dx = synth.make_decode(w)
+    R = w.num_reqs if num_reqs is None else min(num_reqs, w.num_reqs)
+    dx = synth.make_decode(w, num_reqs=R)
     q = to_dev_bf16(dx.q, device)
     kc = to_dev_bf16(dx.k_cache, device)
     vc = to_dev_bf16(dx.v_cache, device)
     bt = torch.as_tensor(dx.block_table, device=device)
     cl = torch.as_tensor(dx.context_lens, device=device)
     ps = bsa.page_summaries(kc, bt, cl)
-    plan = bsa.DecodePlan(w.num_reqs, w.num_heads, w.num_kv_heads, w.head_dim, w.page_size,
+    plan = bsa.DecodePlan(R, w.num_heads, w.num_kv_heads, w.head_dim, w.page_size,
                           dx.block_table.shape[1], dx.k_cache.shape[0], w.top_k, device=device)
     for _ in range(max(3, warmup)):
         plan.run(q, kc, vc, ps, bt, cl)
@@ -292,7 +299,7 @@ def bench_decode(steps, warmup, device):
                                  plan.sel_counts.cpu().numpy(), w.num_heads, w.num_kv_heads,
                                  w.head_dim, w.page_size)
     del kc, vc
-    return ms, by, w
+    return ms, by, w, R
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -380,6 +387,18 @@ def run_reference(args):
     return 0
 
 
+def decode_entry(args, device, peaks, src):
+    d_ms, d_bytes, dw, R = bench_decode(max(20, min(args.steps, 200)), args.warmup, device,
+                                        args.decode_reqs)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = d_bytes["total"] / (d_ms * 1e-3) / 1e9
+    name = dw.name if R == dw.num_reqs else f"{dw.name}_first{R}"
+    return {"workload": name, "value": gbs, "unit": "GB/s", "ms_per_step": d_ms,
+            "kv_only_gbs": d_bytes["kv"] / (d_ms * 1e-3) / 1e9, "bytes": d_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_source": f"{src} copy bandwidth"}}
+
+
 def run_native(args):
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -391,6 +410,15 @@ def run_native(args):
     if rank == 0 or world == 1:
         __graft_entry__.build()
     barrier(world, device)
+    if args.decode_only:  # diagnostic: the decode leg alone, one line
+        peaks, src = measured_peaks()
+        dec = decode_entry(args, device, peaks, src)
+        if rank == 0:
+            print(json.dumps({"metric": "decode KV GB/s", "value": dec["value"], "unit": "GB/s",
+                              "n_gpus": world, "steps": max(20, min(args.steps, 200)),
+                              "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
+                              "higher_is_better": True, "decode": dec}), flush=True)
+        return 0
     w = prefill_workload(args.workload)
     sampler = ClockSampler(local)
     res = bench_prefill(w, args.steps, args.warmup, device, world, sampler)
@@ -401,8 +429,9 @@ def run_native(args):
     st = res["stages"]
     attn_tf = res["flops"] / (st["attention"] * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = recorded_traffic(PROFILE_ATTN, ATTN_SOURCE)
-    roofline = {"bound": "tensor", "kernel": "attn_tc_kernel<128,64>", "achieved": attn_tf,
+    traffic = recorded_traffic(PROFILE_ATTN[args.workload], ATTN_SOURCE)
+    roofline = {"bound": "tensor", "kernel": f"attn_tc_kernel<{w.head_dim},{w.block}>",
+                "achieved": attn_tf,
                 "peak": peak_tf, "unit": "TFLOP/s", "frac": attn_tf / peak_tf,
                 "peak_source": f"{src} bf16 burst", "traffic": traffic,
                 "algorithmic_flops_per_launch": res["flops"],
@@ -415,13 +444,7 @@ def run_native(args):
     dec = None
     if not args.no_decode:
         del res["q"], res["k"], res["v"]
-        d_ms, d_bytes, dw = bench_decode(max(20, min(args.steps, 200)), args.warmup, device)
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        gbs = d_bytes["total"] / (d_ms * 1e-3) / 1e9
-        dec = {"workload": dw.name, "value": gbs, "unit": "GB/s", "ms_per_step": d_ms,
-               "kv_only_gbs": d_bytes["kv"] / (d_ms * 1e-3) / 1e9, "bytes": d_bytes,
-               "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                            "frac": gbs / hbm, "peak_source": f"{src} copy bandwidth"}}
+        dec = decode_entry(args, device, peaks, src)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, dt = cpu_oracle_throughput(res["x"], w, budget_s=12.0)

@@ -191,27 +191,32 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
         }
       }
       __syncthreads();
+      const int bin_count = hist[s_bin];
       remaining -= s_above;
       prefix |= (uint32_t)s_bin << shift;
       mask |= 0xFFu << shift;
       __syncthreads();
+      // The bin holding the k-th key holds exactly the keys still needed: all of
+      // them are selected, whatever their lower bits, so the select is complete.
+      if (bin_count == remaining) break;
     }
   }
-  // Compact in index order: keys above the k-th key, then the first `remaining`
-  // keys equal to it (ties go to the lower page index).
+  // Compact in index order: keys above the k-th key's bin (compared on the
+  // resolved top bits, `mask`), then the first `remaining` keys of that bin (ties
+  // go to the lower page index).
   const int per = (N + blockDim.x - 1) / blockDim.x;
   const int lo = min(N, (int)threadIdx.x * per), hi = min(N, lo + per);
   int n_eq = 0;
-  for (int e = lo; e < hi; ++e) n_eq += (k < N && keys[e] == prefix) ? 1 : 0;
+  for (int e = lo; e < hi; ++e) n_eq += (k < N && (keys[e] & mask) == prefix) ? 1 : 0;
   const int2 eq = block_scan(n_eq, scan_buf);
   int taken = 0, eq_seen = eq.x;
   for (int e = lo; e < hi; ++e) {
     bool s;
     if (k >= N) {
       s = true;
-    } else if (keys[e] > prefix) {
+    } else if ((keys[e] & mask) > prefix) {
       s = true;
-    } else if (keys[e] == prefix) {
+    } else if ((keys[e] & mask) == prefix) {
       s = eq_seen < remaining;
       ++eq_seen;
     } else {
@@ -226,9 +231,9 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
     bool s;
     if (k >= N) {
       s = true;
-    } else if (keys[e] > prefix) {
+    } else if ((keys[e] & mask) > prefix) {
       s = true;
-    } else if (keys[e] == prefix) {
+    } else if ((keys[e] & mask) == prefix) {
       s = eq_seen < remaining;
       ++eq_seen;
     } else {
@@ -588,29 +593,61 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // grid (H_kv, R), G * 128 threads (one output element each): combine the unit
-// partials of a (request, KV head) with eqs.(3)-(5) in the log2 domain.
+// partials of a (request, KV head) with eqs.(3)-(5) in the log2 domain.  Warp g
+// first turns the partials' (m, l) of query head g into weights 2^(m_k - M) and
+// the total l; then every thread sums its column of u with loads kept in flight.
+constexpr int kMaxChunks = (64 + 2) / 2;  // units per (request, KV head) at top_k = 64
+
 __global__ void __launch_bounds__(kMaxG * kD) dec_merge_kernel(
     const float *__restrict__ part_ml, const float *__restrict__ part_o,
     const int32_t *__restrict__ sel_counts, uint16_t *__restrict__ o, float *__restrict__ lse,
     int H, int Hk, int nchunk) {
+  __shared__ float wgt[kMaxG][kMaxChunks];
+  __shared__ float tot_l[kMaxG], tot_m[kMaxG];
   const int rho = blockIdx.y, h = blockIdx.x;
   const int G = H / Hk;
   const int pair = rho * Hk + h;
-  const int g = threadIdx.x / kD, c = threadIdx.x % kD;
   const int nu = (sel_counts[pair] + 1) / 2;
   const size_t u0 = (size_t)pair * nchunk;
-  float M = -INFINITY;
-  for (int k = 0; k < nu; ++k) M = fmaxf(M, part_ml[((u0 + k) * G + g) * 2]);
-  float Lsum = 0.f, acc = 0.f;
-  for (int k = 0; k < nu; ++k) {
-    const float f = fast_exp2(part_ml[((u0 + k) * G + g) * 2] - M);
-    Lsum += f * part_ml[((u0 + k) * G + g) * 2 + 1];
-    acc += f * part_o[((u0 + k) * G + g) * kD + c];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp < G) {
+    const int g = warp;
+    float mk[2], lk[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int k = lane + 32 * r;
+      mk[r] = k < nu ? part_ml[((u0 + k) * G + g) * 2] : -INFINITY;
+      lk[r] = k < nu ? part_ml[((u0 + k) * G + g) * 2 + 1] : 0.f;
+    }
+    float M = fmaxf(mk[0], mk[1]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int k = lane + 32 * r;
+      const float f = k < nu ? fast_exp2(mk[r] - M) : 0.f;
+      if (k < kMaxChunks) wgt[g][k] = f;
+      L += f * lk[r];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      tot_l[g] = L;
+      tot_m[g] = M;
+    }
   }
+  __syncthreads();
+  const int g = threadIdx.x / kD, c = threadIdx.x % kD;
+  const float *col = part_o + (u0 * G + g) * kD + c;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < nu; ++k) acc = fmaf(wgt[g][k], col[(size_t)k * G * kD], acc);
   const int hq = h * G + g;
-  const __nv_bfloat16 ob = __float2bfloat16_rn(acc / Lsum);
+  const __nv_bfloat16 ob = __float2bfloat16_rn(acc / tot_l[g]);
   o[((size_t)rho * H + hq) * kD + c] = *reinterpret_cast<const uint16_t *>(&ob);
-  if (lse != nullptr && c == 0) lse[(size_t)rho * H + hq] = (M + log2f(Lsum)) * 0.6931471805599453f;
+  if (lse != nullptr && c == 0)
+    lse[(size_t)rho * H + hq] = (tot_m[g] + log2f(tot_l[g])) * 0.6931471805599453f;
 }
 
 int num_chunks(const bsa_decode_shape_t &s) { return (s.top_k + 2) / 2; }
