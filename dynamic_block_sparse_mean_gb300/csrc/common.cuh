@@ -41,6 +41,15 @@ BSA_DEV float fast_log2(float x) {
   return y;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while its predecessor is still running; it must call
+// grid_dep_wait() before it reads anything the predecessor writes (the wait
+// returns once that grid has completed and its writes are visible; without the
+// launch attribute it returns at once).  grid_dep_launch() lets the dependent
+// grid be scheduled before this one ends.
+BSA_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+BSA_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 BSA_DEV uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
     if ((lane & 3) == 0 && p0 + row < npg)
       scores[((size_t)rho * Hk + h) * max_pages + p_begin + p0 + row] = best;
   }
+  grid_dep_launch();
 }
 
 // ---------------------------------------------------------------- select
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
   const float *sc = scores + ((size_t)rho * Hk + h) * max_pages;
   int32_t *out = sel + ((size_t)rho * Hk + h) * (top_k + 1);
   const int k = min(top_k, N);
+  grid_dep_wait();  // scores come from the previous launch
   for (int e = threadIdx.x; e < N; e += blockDim.x) keys[e] = order_key(sc[e]);
   __syncthreads();
 
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
     for (int e = k + 1; e <= top_k; ++e) out[e] = -1;
     sel_counts[(size_t)rho * Hk + h] = k + 1;
   }
+  grid_dep_launch();
 }
 
 // ---------------------------------------------------------------- attention
@@ -362,6 +365,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int per_pair = p.top_k + 1;
+  grid_dep_wait();    // the selection comes from the previous launch
+  grid_dep_launch();  // the merge may be scheduled now; it waits for this grid
 
   if (warp == kDecProducer) {
     // ------------------------------------------------------------ producer
@@ -607,6 +612,7 @@ __global__ void __launch_bounds__(kMaxG * kD) dec_merge_kernel(
   const int rho = blockIdx.y, h = blockIdx.x;
   const int G = H / Hk;
   const int pair = rho * Hk + h;
+  grid_dep_wait();  // the partials come from the previous launch
   const int nu = (sel_counts[pair] + 1) / 2;
   const size_t u0 = (size_t)pair * nchunk;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -716,9 +722,9 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
                              (int)sm);
     if (e != cudaSuccess) return e;
   }
-  dec_select_kernel<<<dim3(s.num_kv_heads, s.num_reqs), kSelThreads, sm, st>>>(
-      scores, context_lens, sel, sel_counts, s.num_kv_heads, s.max_pages_per_req, s.top_k);
-  e = cudaGetLastError();
+  e = launch_dependent(dec_select_kernel, dim3(s.num_kv_heads, s.num_reqs), dim3(kSelThreads), sm,
+                       st, scores, context_lens, sel, sel_counts, s.num_kv_heads,
+                       s.max_pages_per_req, s.top_k);
   if (e != cudaSuccess) return e;
 
   DecParams p;
@@ -741,13 +747,11 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
   e = cudaFuncSetAttribute(dec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<size_t>((size_t)num_sms(), units);
-  dec_tc_kernel<<<grid, kDecThreads, kDecSmem, st>>>(mq, mk, mv, p);
-  e = cudaGetLastError();
+  e = launch_dependent(dec_tc_kernel, dim3(grid), dim3(kDecThreads), kDecSmem, st, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
-  dec_merge_kernel<<<dim3(s.num_kv_heads, s.num_reqs), G * kD, 0, st>>>(
-      part_ml, part_o, sel_counts, static_cast<uint16_t *>(o), lse, s.num_heads, s.num_kv_heads,
-      nchunk);
-  return cudaGetLastError();
+  return launch_dependent(dec_merge_kernel, dim3(s.num_kv_heads, s.num_reqs), dim3(G * kD), 0, st,
+                          part_ml, part_o, sel_counts, static_cast<uint16_t *>(o), lse,
+                          s.num_heads, s.num_kv_heads, nchunk);
 }
 
 }  // namespace bsa

@@ -14,6 +14,25 @@ namespace bsa {
 
 int num_sms();
 
+// Launch `kernel` with programmatic stream serialization: it may begin while the
+// previous kernel on the stream is still running, and must call grid_dep_wait()
+// before reading that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // 3-D bf16 TMA descriptor (dims d0 innermost .. d2, dense strides) with a
 // 128-byte swizzle and box b0 x b1 x b2 (tmap.cu).
 bool make_tmap_3d_bf16(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
