@@ -177,6 +177,53 @@ BSA_DEV float tmem_max64(uint32_t taddr) {
   return fmaxf(m0, m1);
 }
 
+// Row max over 128 TMEM columns: four reducing loads, one wait (values dropped).
+BSA_DEV float tmem_max128(uint32_t taddr) {
+  float d[128], m0, m1, m2, m3;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %128, [%132];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %129, [%133];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, %130, [%134];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %131, [%135];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3]), "=f"(d[4]), "=f"(d[5]), "=f"(d[6]), "=f"(d[7]), "=f"(d[8]), "=f"(d[9]), "=f"(d[10]), "=f"(d[11]), "=f"(d[12]), "=f"(d[13]), "=f"(d[14]), "=f"(d[15]), "=f"(d[16]), "=f"(d[17]), "=f"(d[18]), "=f"(d[19]), "=f"(d[20]), "=f"(d[21]), "=f"(d[22]), "=f"(d[23]), "=f"(d[24]), "=f"(d[25]), "=f"(d[26]), "=f"(d[27]), "=f"(d[28]), "=f"(d[29]), "=f"(d[30]), "=f"(d[31]), "=f"(d[32]), "=f"(d[33]), "=f"(d[34]), "=f"(d[35]), "=f"(d[36]), "=f"(d[37]), "=f"(d[38]), "=f"(d[39]), "=f"(d[40]), "=f"(d[41]), "=f"(d[42]), "=f"(d[43]), "=f"(d[44]), "=f"(d[45]), "=f"(d[46]), "=f"(d[47]), "=f"(d[48]), "=f"(d[49]), "=f"(d[50]), "=f"(d[51]), "=f"(d[52]), "=f"(d[53]), "=f"(d[54]), "=f"(d[55]), "=f"(d[56]), "=f"(d[57]), "=f"(d[58]), "=f"(d[59]), "=f"(d[60]), "=f"(d[61]), "=f"(d[62]), "=f"(d[63]), "=f"(d[64]), "=f"(d[65]), "=f"(d[66]), "=f"(d[67]), "=f"(d[68]), "=f"(d[69]), "=f"(d[70]), "=f"(d[71]), "=f"(d[72]), "=f"(d[73]), "=f"(d[74]), "=f"(d[75]), "=f"(d[76]), "=f"(d[77]), "=f"(d[78]), "=f"(d[79]), "=f"(d[80]), "=f"(d[81]), "=f"(d[82]), "=f"(d[83]), "=f"(d[84]), "=f"(d[85]), "=f"(d[86]), "=f"(d[87]), "=f"(d[88]), "=f"(d[89]), "=f"(d[90]), "=f"(d[91]), "=f"(d[92]), "=f"(d[93]), "=f"(d[94]), "=f"(d[95]), "=f"(d[96]), "=f"(d[97]), "=f"(d[98]), "=f"(d[99]), "=f"(d[100]), "=f"(d[101]), "=f"(d[102]), "=f"(d[103]), "=f"(d[104]), "=f"(d[105]), "=f"(d[106]), "=f"(d[107]), "=f"(d[108]), "=f"(d[109]), "=f"(d[110]), "=f"(d[111]), "=f"(d[112]), "=f"(d[113]), "=f"(d[114]), "=f"(d[115]), "=f"(d[116]), "=f"(d[117]), "=f"(d[118]), "=f"(d[119]), "=f"(d[120]), "=f"(d[121]), "=f"(d[122]), "=f"(d[123]), "=f"(d[124]), "=f"(d[125]), "=f"(d[126]), "=f"(d[127]),
+        "=f"(m0), "=f"(m1), "=f"(m2), "=f"(m3)
+      : "r"(taddr), "r"(taddr + 32u), "r"(taddr + 64u), "r"(taddr + 96u)
+      : "memory");
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// 32 TMEM columns of this thread's lane, not waited: the registers become valid
+// at the next tmem_wait_ld on them.
+BSA_DEV void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Wait for this thread's TMEM loads; naming the loaded registers as operands
+// keeps every use of them after the wait.
+BSA_DEV void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// 16 TMEM columns of this thread's lane, not waited (tmem_wait_st before the
+// values are consumed).
+BSA_DEV void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+BSA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 64 consecutive TMEM columns of this thread's lane: two loads, one wait.
 BSA_DEV void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
   asm volatile(
@@ -245,6 +292,46 @@ BSA_DEV void load_masked(uint32_t taddr, int lim, float (&v)[64]) {
   tmem_ld64(taddr, rr);
 #pragma unroll
   for (int c = 0; c < 64; ++c) v[c] = c < lim ? __uint_as_float(rr[c]) : -INFINITY;
+}
+
+
+// P for one step: S columns 32 q .. 32 q + 31 -> P columns 16 q .. 16 q + 15 (bf16
+// pairs), for q = 0..3.  The load of quarter q + 1 is in flight while quarter q is
+// exponentiated, and the P stores are waited once at the end; a P quarter only
+// overwrites S columns already read.  MASKED applies the step's column limits
+// (lim[h] for the half h of 64 columns).  Returns the row sum of the new P.
+template <bool MASKED>
+BSA_DEV float exp_step(uint32_t tS, uint64_t scale2, uint64_t negm, const int (&lim)[2]) {
+  uint32_t buf[2][32];
+  uint64_t acc0 = 0, acc1 = 0;
+  tmem_ld32_async(tS, buf[0]);
+  tmem_wait_ld(buf[0]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q < 3) tmem_ld32_async(tS + 32 * (q + 1), buf[(q + 1) & 1]);
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float a = __uint_as_float(buf[q & 1][2 * c]), b = __uint_as_float(buf[q & 1][2 * c + 1]);
+      if (MASKED) {
+        const int col = (q & 1) * 32 + 2 * c;  // column within the 64-column half q / 2
+        a = col < lim[q >> 1] ? a : -INFINITY;
+        b = col + 1 < lim[q >> 1] ? b : -INFINITY;
+      }
+      const uint64_t z = fma2(pack2(a, b), scale2, negm);
+      const float e0 = fast_exp2(lo_of(z)), e1 = fast_exp2(hi_of(z));
+      pk[c] = pack_bf16x2(e0, e1);
+      if (c & 1)
+        acc1 = add2(acc1, pack2(e0, e1));
+      else
+        acc0 = add2(acc0, pack2(e0, e1));
+    }
+    tmem_st16_nowait(tS + 16 * q, pk);
+    if (q < 3) tmem_wait_ld(buf[(q + 1) & 1]);
+  }
+  tmem_wait_st();
+  const uint64_t acc = add2(acc0, acc1);
+  return lo_of(acc) + hi_of(acc);
 }
 
 template <int D, int BK>
@@ -530,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tcgen05 loads are warp-collective: the path must be the same for every
         // lane (the diagonal's limits differ from lane to lane).
         if (__all_sync(0xffffffffu, lim[0] == 64 && lim[1] == 64)) {  // no mask: reducing loads
-          mx = fmaxf(tmem_max64(tS), tmem_max64(tS + 64));
+          mx = tmem_max128(tS);
         } else {
           float v[64];
           load_masked(tS, lim[0], v);
@@ -561,28 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t negm = pack2(-mref, -mref);
-        uint64_t acc0 = 0, acc1 = 0;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          // S columns 64 hh .. 64 hh + 63 -> P columns 32 hh .. 32 hh + 31 (the P
-          // half written here overlaps only S columns already read).
-          float v[64];
-          load_masked(tS + 64 * hh, lim[hh], v);
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint64_t z = fma2(pack2(v[2 * c], v[2 * c + 1]), scale2, negm);
-            const float e0 = fast_exp2(lo_of(z)), e1 = fast_exp2(hi_of(z));
-            pk[c] = pack_bf16x2(e0, e1);
-            if (c & 1)
-              acc1 = add2(acc1, pack2(e0, e1));
-            else
-              acc0 = add2(acc0, pack2(e0, e1));
-          }
-          tmem_st32(tS + 32 * hh, pk);
-        }
-        const uint64_t acc = add2(acc0, acc1);
-        l += lo_of(acc) + hi_of(acc);
+        if (__all_sync(0xffffffffu, lim[0] == 64 && lim[1] == 64))
+          l += exp_step<false>(tS, scale2, negm, lim);
+        else
+          l += exp_step<true>(tS, scale2, negm, lim);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
