@@ -167,17 +167,26 @@ def route_scores_row(Q, C, cu_seqlens, b: int, G: int, row):
 # a3: selection
 # ----------------------------------------------------------------------------
 
-def forced_blocks(r: int, force_sink: bool):
-    """The diagonal r is always kept (triangle branch, [P2] §2.1 causal rule);
-    block 0 is added when the sink is forced (R-4)."""
-    f = {r}
+def forced_blocks(r: int, force_sink: bool, window: int = 1, global_blocks=()):
+    """Blocks every row r keeps, outside the dynamic budget.
+
+    The diagonal r is always kept (triangle branch, [P2] §2.1 causal rule); block 0
+    when the sink is forced (R-4).  Union routing ([P2] §3.2, N_u = L_u ∪ G ∪ I_u,
+    with the representations of [P2] §3.1): the local window L_r = the `window`
+    most recent blocks r - window + 1 .. r (an implicit rule; window <= 1 is the
+    diagonal alone) and the global list G (blocks at or before r; later blocks are
+    invisible under the causal rule).  The union is a set: a block named by two
+    branches is kept once (R-15)."""
+    f = set(range(max(0, r - max(1, window) + 1), r + 1))
     if force_sink:
         f.add(0)
+    f |= {int(g) for g in global_blocks if 0 <= int(g) <= r}
     return f
 
 
 def select_row(g_row, r: int, mode: int, k_max: int, k_min: int = 0,
-               tau_delta: float = 0.0, force_sink: bool = False):
+               tau_delta: float = 0.0, force_sink: bool = False, window: int = 1,
+               global_blocks=()):
     """Selected key blocks of query block r, deduplicated and sorted by address.
 
     Top-k: [P2] §2.1 "top-k, threshold and capacity" — every row gets the same
@@ -185,9 +194,11 @@ def select_row(g_row, r: int, mode: int, k_max: int, k_min: int = 0,
     Threshold: eq.(7) k_r = min(k_max, max(k_min, |{j : g_rj >= tau_r}|)) with
     tau_r relative to the row maximum (R-5).
     Dedup and ascending order: [P2] §1.2 (eq.(1) address list, sorted for
-    locality) and §3.2 (union then dedup).
+    locality) and §3.2 (union then dedup).  The dynamic candidates exclude every
+    forced block, window included ([P2] §3.1: dynamic top-k leaves out the blocks
+    the local window covers).
     """
-    F = forced_blocks(r, force_sink)
+    F = forced_blocks(r, force_sink, window, global_blocks)
     cand = np.array([j for j in range(r) if j not in F], dtype=np.int64)
     if mode == TOPK:
         k_dyn = max(0, k_max - len(F))
@@ -209,7 +220,8 @@ def select_row(g_row, r: int, mode: int, k_max: int, k_min: int = 0,
 
 
 def route(Q, K, cu_seqlens, b: int, G: int, mode: int, k_max: int, k_min: int = 0,
-          tau_delta: float = 0.0, force_sink: bool = False, rows=None):
+          tau_delta: float = 0.0, force_sink: bool = False, rows=None, window: int = 1,
+          global_blocks=()):
     """Summaries, scores and selection: returns J [B, H_kv, N_q, k_max] (-1 padded),
     counts [B, H_kv, N_q], scores g and summaries C.  Rows not requested keep
     count 0 and -1 entries."""
@@ -224,7 +236,8 @@ def route(Q, K, cu_seqlens, b: int, G: int, mode: int, k_max: int, k_min: int = 
     for (i, h, r) in rows:
         if r >= info[i][2]:
             continue
-        sel = select_row(g[i, h, r], r, mode, k_max, k_min, tau_delta, force_sink)
+        sel = select_row(g[i, h, r], r, mode, k_max, k_min, tau_delta, force_sink, window,
+                         global_blocks)
         J[i, h, r, :len(sel)] = sel
         counts[i, h, r] = len(sel)
     return J, counts, g, C

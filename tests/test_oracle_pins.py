@@ -202,6 +202,51 @@ def test_threshold_rule_hand_worked_row():
     assert oracle.select_row(np.array([1.0, 2.0, 2.0, 2.0]), 4, oracle.TOPK, 3) == [1, 2, 4]
 
 
+def test_union_routing_hand_worked_row():
+    # N_u = L_u ∪ G ∪ I_u for row r = 6 with scores of history blocks 0..5:
+    # window 3 -> L = {4, 5, 6}; global list [1] -> F = {1, 4, 5, 6}.
+    g = np.array([1.0, 3.0, 2.5, 0.9, 2.0, 2.9])
+    # k_max 6 leaves two dynamic picks among {0, 2, 3}: 2 (2.5) and 0 (1.0).  Blocks 1
+    # (3.0) and 5 (2.9) score highest but are already kept, so they spend no budget.
+    assert oracle.select_row(g, 6, oracle.TOPK, 6, window=3, global_blocks=[1]) == [0, 1, 2, 4, 5, 6]
+    assert oracle.select_row(g, 6, oracle.TOPK, 5, window=3, global_blocks=[1]) == [1, 2, 4, 5, 6]
+    # a global block inside the window is kept once and frees no extra slot
+    assert oracle.select_row(g, 6, oracle.TOPK, 5, window=3, global_blocks=[5]) == \
+        oracle.select_row(g, 6, oracle.TOPK, 5, window=3) == [1, 2, 4, 5, 6]
+    # blocks after r are invisible (causal) whatever the global list says
+    assert oracle.select_row(g[:3], 3, oracle.TOPK, 3, window=1, global_blocks=[2, 7]) == [1, 2, 3]
+    # threshold mode, eq.(7) over the non-forced candidates {0, 2, 3}: delta 1.0 ->
+    # tau 1.5 -> A = {2}; k_r = min(8, max(2, |F| + 1), |F| + 3) = 5 -> F plus block 2.
+    assert oracle.select_row(g, 6, oracle.THRESHOLD, 8, 2, 1.0, window=3, global_blocks=[1]) == \
+        [1, 2, 4, 5, 6]
+
+
+def test_union_selection_properties_and_enumeration():
+    rng = np.random.default_rng(21)
+    for trial in range(60):
+        r = int(rng.integers(0, 10))
+        g = np.round(rng.normal(size=r), 1)
+        w = int(rng.integers(0, 5))
+        glob = sorted(set(int(x) for x in rng.integers(0, 12, size=int(rng.integers(0, 4)))))
+        sink = bool(rng.integers(0, 2))
+        for k_max in (1, 3, 6, 12):
+            sel = oracle.select_row(g, r, oracle.TOPK, k_max, force_sink=sink, window=w,
+                                    global_blocks=glob)
+            assert sel == sorted(set(sel)) and all(0 <= j <= r for j in sel)
+            window = set(range(max(0, r - max(1, w) + 1), r + 1))
+            kept = window | {j for j in glob if j <= r} | ({0} if sink else set())
+            assert kept <= set(sel)                              # every forced block is kept
+            dyn = [j for j in sel if j not in kept]
+            assert len(sel) == max(len(kept), min(k_max, r + 1))  # the budget counts forced blocks
+            # the dynamic part is the exhaustive best subset of the remaining history
+            cand = {j: g[j] for j in range(r) if j not in kept}
+            k_dyn = max(0, k_max - len(kept))
+            want = oracle.brute_topk_by_enumeration(cand, k_dyn) if cand and k_dyn else []
+            assert sorted(dyn) == sorted(want)
+        # a window reaching block 0 selects the whole causal row
+        assert oracle.select_row(g, r, oracle.TOPK, r + 1, window=r + 1) == list(range(r + 1))
+
+
 # ---------------------------------------------------------------- summaries
 
 
