@@ -15,7 +15,7 @@ from __future__ import annotations
 
 import ctypes
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import numpy as np
 import torch
@@ -53,15 +53,33 @@ def _dtype_code(dt: torch.dtype) -> int:
 
 @dataclass
 class RouteParams:
+    """Router parameters (bsa_route_params_t).  Union routing: `window` keeps the
+    most recent blocks of every row (diagonal included), `global_blocks` a short
+    list of block ids kept by every row that can see them; the dynamic top-k or
+    threshold choice covers the rest of the history."""
     mode: int = ROUTE_TOPK
     k_max: int = 32
     k_min: int = 0
     tau_delta: float = 0.0
     force_sink: bool = False
+    window: int = 1
+    global_blocks: tuple = ()
+    _gdev: object = field(default=None, repr=False, compare=False)
 
-    def c(self) -> _lib.RouteParams:
+    def _globals_on(self, device):
+        if not self.global_blocks:
+            return None
+        if self._gdev is None or self._gdev.device != torch.device(device):
+            self._gdev = torch.as_tensor([int(g) for g in self.global_blocks], dtype=torch.int32,
+                                         device=device)
+        return self._gdev
+
+    def c(self, device=None) -> _lib.RouteParams:
+        g = self._globals_on(device) if device is not None else None
         return _lib.RouteParams(self.mode, self.k_max, self.k_min, self.tau_delta,
-                                1 if self.force_sink else 0)
+                                1 if self.force_sink else 0, self.window,
+                                0 if g is None else g.numel(),
+                                None if g is None else g.data_ptr())
 
 
 @dataclass
@@ -146,7 +164,7 @@ def route(q, C, shape: PrefillShape, params: RouteParams, J=None, counts=None, s
                          device=dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    s, p = shape.c(), params.c()
+    s, p = shape.c(), params.c(dev)
     check("bsa_route", _lib.lib().bsa_route(ctypes.byref(s), ctypes.byref(p), _p(q), _p(C), _p(J),
                                             _p(counts), _p(scores), _p(dev_status), _p(ws),
                                             ws.numel(), _stream()))

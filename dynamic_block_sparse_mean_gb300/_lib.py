@@ -20,6 +20,7 @@ STATUS_NAMES = {
 BSA_BF16, BSA_FP32 = 0, 1
 NUM_BUCKETS = 7
 MAX_K = 256
+MAX_GLOBAL = 32
 
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 c_f32p = ctypes.POINTER(ctypes.c_float)
@@ -35,7 +36,9 @@ class Shape(ctypes.Structure):
 
 class RouteParams(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("k_max", ctypes.c_int32), ("k_min", ctypes.c_int32),
-                ("tau_delta", ctypes.c_float), ("force_sink", ctypes.c_int32)]
+                ("tau_delta", ctypes.c_float), ("force_sink", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("num_global", ctypes.c_int32),
+                ("global_blocks", ctypes.c_void_p)]
 
 
 class DecodeShape(ctypes.Structure):

@@ -108,7 +108,13 @@ bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *param
   if (params->mode == BSA_ROUTE_THRESHOLD &&
       (params->k_min < 0 || !(params->tau_delta >= 0.f) || !isfinite(params->tau_delta)))
     return BSA_ERR_INVALID_ARG;
-  if (params->force_sink && params->k_max < 2) return BSA_ERR_INVALID_ARG;
+  if (params->num_global < 0 || params->num_global > BSA_MAX_GLOBAL ||
+      (params->num_global > 0 && params->global_blocks == nullptr))
+    return BSA_ERR_INVALID_ARG;
+  if (params->window > params->k_max ||
+      (params->window > 1 ? params->window : 1) + params->num_global +
+              (params->force_sink ? 1 : 0) > params->k_max)
+    return BSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(C)) return BSA_ERR_INVALID_ARG;
   const size_t need = bsa::route_workspace_bytes(*shape, *params);
   if (ws == nullptr || ws_bytes < need) return BSA_ERR_WORKSPACE;

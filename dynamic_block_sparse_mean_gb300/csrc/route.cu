@@ -145,7 +145,8 @@ BSA_DEV Cand warp_best(Cand c) {
 __global__ void __launch_bounds__(32) route_select_kernel(
     const float *__restrict__ S, const int32_t *__restrict__ cu, int32_t *__restrict__ J,
     int32_t *__restrict__ counts, int Nq, int Hk, int b, int mode, int k_max, int k_min,
-    float tau_delta, int force_sink) {
+    float tau_delta, int force_sink, int window, int num_global,
+    const int32_t *__restrict__ global_blocks) {
   extern __shared__ uint8_t sm[];
   float *sc = reinterpret_cast<float *>(sm);
   int32_t *ids = reinterpret_cast<int32_t *>(sm + (size_t)Nq * 4);
@@ -163,18 +164,30 @@ __global__ void __launch_bounds__(32) route_select_kernel(
     return;
   }
   const float *Srow = S + (size_t)row * Nq;
-  const bool sink = force_sink && r > 0;
-  const int nforced = sink ? 2 : 1;
-  int ncand = 0;
+  // Forced blocks F_r (union routing: local window, global list, sink, diagonal)
+  // are marked `taken` so the dynamic choice never spends budget on them; a block
+  // named by several branches is kept once.
+  const int wlo = max(0, r - max(1, window) + 1);
   for (int j = lane; j < r; j += 32) {
-    const bool is_cand = !(sink && j == 0);
     sc[j] = Srow[j];
-    taken[j] = is_cand ? 0 : 1;
-    ncand += is_cand ? 1 : 0;
+    taken[j] = (j >= wlo || (force_sink && j == 0)) ? 1 : 0;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ncand += __shfl_xor_sync(0xffffffffu, ncand, off);
   __syncwarp();
+  if (lane < num_global) {
+    const int gb = global_blocks[lane];
+    if (gb >= 0 && gb < r) taken[gb] = 1;
+  }
+  __syncwarp();
+  int nhist = 0;  // forced history blocks (j < r), listed first in ids
+  for (int j0 = 0; j0 < r; j0 += 32) {
+    const int j = j0 + lane;
+    const bool f = j < r && taken[j];
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (f) ids[nhist + __popc(m & ((1u << lane) - 1u))] = j;
+    nhist += __popc(m);
+  }
+  const int nforced = nhist + 1;  // + the diagonal
+  const int ncand = r - nhist;
 
   int k_dyn;
   if (mode == BSA_ROUTE_TOPK) {
@@ -216,10 +229,7 @@ __global__ void __launch_bounds__(32) route_select_kernel(
     }
     __syncwarp();
   }
-  if (lane == 0) {
-    ids[0] = r;
-    if (sink) ids[1] = 0;
-  }
+  if (lane == 0) ids[nhist] = r;
   __syncwarp();
   const int cnt = nforced + k_dyn;
   // Rank sort (ids are distinct) into ascending order.
@@ -273,7 +283,8 @@ cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, cons
   }
   route_select_kernel<<<rows, 32, sm, st>>>(S, s.cu_seqlens, J, counts, s.max_blocks,
                                             s.num_kv_heads, s.block, p.mode, p.k_max, p.k_min,
-                                            p.tau_delta, p.force_sink);
+                                            p.tau_delta, p.force_sink, p.window, p.num_global,
+                                            p.global_blocks);
   return cudaGetLastError();
 }
 

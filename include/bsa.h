@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 1
+#define BSA_VERSION 2
 
 typedef enum {
   BSA_OK = 0,
@@ -65,6 +65,8 @@ enum { BSA_ROUTE_TOPK = 0, BSA_ROUTE_THRESHOLD = 1 };
 #define BSA_NUM_BUCKETS 7
 /* Largest supported row capacity k_max. */
 #define BSA_MAX_K 256
+/* Longest global block list of union routing (bsa_route_params_t.global_blocks). */
+#define BSA_MAX_GLOBAL 32
 
 /* Shape of a packed prefill batch ([P2] section 1, problem statement). */
 typedef struct {
@@ -80,13 +82,25 @@ typedef struct {
   const int32_t *cu_seqlens; /* device [B + 1], non-decreasing, cu[0] = 0      */
 } bsa_shape_t;
 
-/* Router parameters ([P2] §2.1 "top-k, threshold and capacity", eq.(7)). */
+/* Router parameters ([P2] §2.1 "top-k, threshold and capacity", eq.(7); union
+ * routing N_u = L_u ∪ G ∪ I_u of [P2] §3.2 with the representations of §3.1: an
+ * implicit local window, one short global list, and the dynamic top-k or
+ * threshold choice over the history blocks neither of them keeps).
+ * Row r keeps F_r = {r-window+1 .. r} ∪ {g in global_blocks : g <= r} (∪ {0} with
+ * force_sink), each block once, plus the dynamic picks; k_max counts F_r, so the
+ * call is rejected (BSA_ERR_INVALID_ARG) unless
+ * max(1, window) + num_global + (force_sink != 0) <= k_max. */
 typedef struct {
   int32_t mode;       /* BSA_ROUTE_TOPK or BSA_ROUTE_THRESHOLD                      */
   int32_t k_max;      /* row capacity of J, forced blocks included; 1 .. BSA_MAX_K  */
   int32_t k_min;      /* threshold mode: lower clamp of eq.(7)                      */
   float tau_delta;    /* threshold mode: tau_r = (max candidate score) - tau_delta   */
   int32_t force_sink; /* non-zero: block 0 is always kept (a global sink block)      */
+  int32_t window;     /* local window in blocks, diagonal included; <= 1: diagonal  */
+  int32_t num_global; /* entries of global_blocks, 0 .. BSA_MAX_GLOBAL               */
+  const int32_t *global_blocks; /* device [num_global] sequence-relative block ids
+                                   (>= 0; ids past a row are ignored by that row);
+                                   NULL when num_global == 0; read during the call */
 } bsa_route_params_t;
 
 /* Paged decode shape ([P2] §2.2 decode; §3.1 paged KV cache and block table). */

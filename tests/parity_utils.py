@@ -55,7 +55,7 @@ def sample_rows(cu, b, Hk, n_random, seed, all_rows=False):
 
 
 def check_route_rows(J_gpu, cnt_gpu, J_ora, cnt_ora, g_ora, rows, mode, force_sink,
-                     tau_delta=0.0, band=TIE_BAND):
+                     tau_delta=0.0, band=TIE_BAND, window=1, global_blocks=()):
     """Tie-aware comparison of selected sets.
 
     Forced blocks must be present; each GPU row must be ascending, unique and -1
@@ -73,7 +73,7 @@ def check_route_rows(J_gpu, cnt_gpu, J_ora, cnt_ora, g_ora, rows, mode, force_si
         sg = row[:cg]
         assert sg == sorted(set(sg)), (i, h, r, sg)
         so = [int(x) for x in J_ora[i, h, r, :co]]
-        F = {r} | ({0} if force_sink else set())
+        F = oracle.forced_blocks(r, force_sink, window, global_blocks)
         assert F <= set(sg), (i, h, r, sg)
         g = np.asarray(g_ora[i, h, r, :r], dtype=np.float64)
         cand = [j for j in range(r) if j not in F]

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.bsa_version() == 1
+    assert lib.bsa_version() == 2
     for code in _lib.STATUS_NAMES:
         assert lib.bsa_status_string(code)
 
@@ -70,6 +70,16 @@ def test_host_side_argument_errors(lib):
     assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 3
     p = _lib.RouteParams(5, 4, 0, 0.0, 0)
     assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 1
+    # union routing: the forced set must fit the row capacity, the list its bound
+    gl = ctypes.c_void_p(16)
+    for bad_p in (_lib.RouteParams(0, 4, 0, 0.0, 0, 5, 0, None),       # window > k_max
+                  _lib.RouteParams(0, 4, 0, 0.0, 1, 2, 2, gl),         # 2 + 2 + sink > 4
+                  _lib.RouteParams(0, 64, 0, 0.0, 0, 1, 33, gl),       # list too long
+                  _lib.RouteParams(0, 64, 0, 0.0, 0, 1, 1, None)):     # list missing
+        assert lib.bsa_route(ctypes.byref(s), ctypes.byref(bad_p), *args, null, null, null, 0,
+                             null) == 1
+    ok_p = _lib.RouteParams(0, 4, 0, 0.0, 1, 2, 1, gl)                # 2 + 1 + sink = 4
+    assert lib.bsa_route(ctypes.byref(s), ctypes.byref(ok_p), *args, null, null, null, 0, null) == 3
     split = (1 * 2 * 16 * 64 * 3 * 2 + 255) // 256 * 256      # bf16 three-way split of C
     assert lib.bsa_route_workspace_size(ctypes.byref(s), ctypes.byref(p)) == split + 1 * 2 * 16 * 16 * 4
     wl = [ctypes.c_void_p(16)] * 7

@@ -266,3 +266,59 @@ def test_plan_end_to_end_small():
     mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
                                            np.ones(lo.shape, dtype=bool))
     assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS
+
+
+# Union routing N_u = L_u ∪ G ∪ I_u: (name, lengths, H, H_kv, d, b, mode, k_max, k_min,
+# tau_delta, sink, window, global list).  The last case repeats a global block and
+# names blocks inside the window and past the sequence end.
+UNION_CASES = [
+    ("union_w3_g2_sink_topk", [1500, 700], 8, 2, 128, 64, oracle.TOPK, 10, 0, 0.0, True, 3, (2, 5)),
+    ("union_w4_g1_threshold", [1300, 900], 4, 2, 128, 64, oracle.THRESHOLD, 12, 2, 2.0, False, 4,
+     (1,)),
+    ("union_w2_dup_b128", [2000], 16, 2, 128, 128, oracle.TOPK, 6, 0, 0.0, False, 2, (0, 3, 3, 40)),
+]
+
+
+def _union_case(case, seed=11):
+    name, lengths, H, Hk, d, b, mode, k_max, k_min, tau, sink, window, glob = case
+    x = synth.gen_prefill(lengths, H, Hk, d, b, seed, "iid", "bf16")
+    q, k, v = upload(x)
+    sh = shape_of(x, H, Hk)
+    params = bsa.RouteParams(mode, k_max, k_min, tau, sink, window=window, global_blocks=glob)
+    return x, q, k, v, sh, params
+
+
+@pytest.mark.parametrize("case", UNION_CASES, ids=[c[0] for c in UNION_CASES])
+def test_union_router_matches_oracle(case):
+    x, q, k, v, sh, params = _union_case(case)
+    H, Hk = case[2], case[3]
+    C = bsa.block_summaries(k, sh)
+    J, cnt = bsa.route(q, C, sh, params)
+    Jo, co, go, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, x.block,
+                                 H // Hk, params.mode, params.k_max, params.k_min, params.tau_delta,
+                                 params.force_sink, window=params.window,
+                                 global_blocks=params.global_blocks)
+    rows = oracle.all_rows(x.cu_seqlens, x.block, Hk)
+    check_route_rows(J.cpu().numpy(), cnt.cpu().numpy(), Jo, co, go, rows, params.mode,
+                     params.force_sink, params.tau_delta, window=params.window,
+                     global_blocks=params.global_blocks)
+
+
+@pytest.mark.parametrize("case", UNION_CASES, ids=[c[0] for c in UNION_CASES])
+def test_union_routing_end_to_end(case):
+    x, q, k, v, sh, params = _union_case(case)
+    H, Hk = case[2], case[3]
+    G = H // Hk
+    plan = bsa.PrefillPlan(x.cu_seqlens, H, Hk, case[4], case[5], params, device="cuda")
+    O, lse = plan.run(q, k, v)
+    torch.cuda.synchronize()
+    bsa.check_status(plan.status)
+    # the oracle's attention over the index the GPU chose (checked above against the
+    # oracle's own selection) gives the exact expected output for that index
+    Jg = plan.J.cpu().numpy().astype(np.int64)
+    cg = plan.counts.cpu().numpy().astype(np.int64)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, x.block, G, Jg, cg)
+    mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
+                                           np.ones(lo.shape, dtype=bool))
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS, (mx, mean, lmx)
