@@ -404,6 +404,35 @@ def missed_mass(q, Kseq, t: int, allowed_blocks, b: int, scale: float):
     return float(a[~inside].sum())
 
 
+def coverage(Q, K, cu_seqlens, b: int, G: int, J, counts, rows=None, scale=None):
+    """Coverage C_i of eq.(10) ([P2] §3.1, second validation layer): for every query
+    token i of the requested rows and every query head of the group, the dense
+    causal softmax probability mass that falls on the keys the row selected,
+    C_i = sum over j in N(i) of alpha_ij^dense.  [H, T], NaN outside the rows.
+    An empty row keeps only its diagonal (R-7)."""
+    H, T, d = Q.shape
+    Hk = K.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if rows is None:
+        rows = all_rows(cu_seqlens, b, Hk)
+    C = np.full((H, T), np.nan)
+    info = seq_info(cu_seqlens, b)
+    for (i, h, r) in rows:
+        s0, n, nb = info[i]
+        if r >= nb:
+            continue
+        cnt = int(counts[i, h, r])
+        sel = [int(x) for x in J[i, h, r, :cnt]] or [r]
+        Kseq = K[h, s0:s0 + n]
+        for hq in range(h * G, (h + 1) * G):
+            for t in range(r * b, min(n, (r + 1) * b)):
+                a = dense_probabilities(Q[hq, s0 + t], Kseq, t, scale)
+                inside = np.isin(np.arange(t + 1) // b, np.asarray(sel))
+                C[hq, s0 + t] = float(a[inside].sum())
+    return C
+
+
 def dense_causal_pairs(n: int) -> int:
     """eq.(8) of [P2] §2.2: n (n + 1) / 2 token pairs for one head."""
     return n * (n + 1) // 2

@@ -247,6 +247,32 @@ def test_union_selection_properties_and_enumeration():
         assert oracle.select_row(g, r, oracle.TOPK, r + 1, window=r + 1) == list(range(r + 1))
 
 
+def test_coverage_matches_library_logsumexp_and_limits():
+    # eq.(10) C_i = exp(lse over the selected keys - lse over all causal keys), both
+    # log-sum-exps from torch; all causal blocks give C = 1; a superset of blocks
+    # never covers less.
+    x, Q, K, V = _inputs([300, 200], 4, 2, 32, 64, seed=31)
+    G, b = 2, 64
+    Jo, co, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 2)
+    C = oracle.coverage(Q, K, x.cu_seqlens, b, G, Jo, co)
+    info = oracle.seq_info(x.cu_seqlens, b)
+    for (i, h, r) in oracle.all_rows(x.cu_seqlens, b, 2):
+        s0, n, nb = info[i]
+        sel = [int(v) for v in Jo[i, h, r, :co[i, h, r]]]
+        for hq in range(h * G, (h + 1) * G):
+            for t in range(r * b, min(n, (r + 1) * b), 17):
+                s = torch.from_numpy(K[h, s0:s0 + t + 1] @ Q[hq, s0 + t]) / math.sqrt(32)
+                keep = torch.from_numpy(np.isin(np.arange(t + 1) // b, sel))
+                want = math.exp(float(torch.logsumexp(s[keep], 0) - torch.logsumexp(s, 0)))
+                assert abs(C[hq, s0 + t] - want) < 1e-12
+    Ja, ca = oracle.causal_all_blocks(x.cu_seqlens, b, 2)
+    assert np.nanmax(np.abs(oracle.coverage(Q, K, x.cu_seqlens, b, G, Ja, ca) - 1.0)) < 1e-12
+    Jb, cb, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 3)
+    Cb = oracle.coverage(Q, K, x.cu_seqlens, b, G, Jb, cb)
+    ok = ~np.isnan(C)
+    assert (Cb[ok] >= C[ok] - 1e-12).all()
+
+
 # ---------------------------------------------------------------- summaries
 
 
