@@ -28,7 +28,8 @@ ROUTE_THRESHOLD = 1
 
 __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "PrefillPlan",
            "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
-           "attention_fwd", "page_summaries", "decode_paged", "check_status", "library_path"]
+           "attention_fwd", "causal_worklist", "coverage", "page_summaries", "decode_paged",
+           "check_status", "library_path"]
 
 
 def library_path() -> str:
@@ -204,6 +205,36 @@ def attention_fwd(q, k, v, wl: Worklist, shape: PrefillShape, dev_status, scale:
     return out, lse
 
 
+def causal_worklist(shape: PrefillShape, device, wl: Worklist | None = None, ws=None) -> Worklist:
+    """Worklist of every causal block (bsa_build_causal_worklist): fed to
+    attention_fwd it gives dense causal attention with the same kernel."""
+    s = shape.c()
+    rows = shape.num_rows
+    if wl is None:
+        cap = int(_lib.lib().bsa_causal_worklist_capacity(ctypes.byref(s)))
+        wl = Worklist(torch.empty(rows + 1, dtype=torch.int32, device=device),
+                      torch.empty(max(1, cap), dtype=torch.int32, device=device),
+                      torch.empty(max(1, rows), dtype=torch.int32, device=device),
+                      torch.empty(NUM_BUCKETS + 1, dtype=torch.int32, device=device))
+    if ws is None:
+        n = int(_lib.lib().bsa_worklist_workspace_size(ctypes.byref(s), 1))
+        ws = torch.empty(max(256, n), dtype=torch.uint8, device=device)
+    check("bsa_build_causal_worklist", _lib.lib().bsa_build_causal_worklist(
+        ctypes.byref(s), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work), _p(wl.bucket_off), _p(ws),
+        ws.numel(), _stream()))
+    return wl
+
+
+def coverage(lse_sparse, lse_dense, shape: PrefillShape, out=None):
+    """Coverage C_i of eq.(10), [H, T] fp32 (bsa_coverage)."""
+    if out is None:
+        out = torch.empty_like(lse_sparse)
+    s = shape.c()
+    check("bsa_coverage", _lib.lib().bsa_coverage(ctypes.byref(s), _p(lse_sparse), _p(lse_dense),
+                                                  _p(out), _stream()))
+    return out
+
+
 class PrefillPlan:
     """All buffers of one prefill shape, allocated once; run() enqueues the four calls
     (summaries, route, worklist, attention) on the current stream."""
@@ -265,6 +296,15 @@ class PrefillPlan:
     def run(self, q, k, v, scale: float = 0.0):
         self.route(q, k)
         return self.attend(q, k, v, scale)
+
+    def coverage(self, q, k, v, scale: float = 0.0):
+        """Coverage C_i of eq.(10) of the current route: the lse of the routed
+        attention against the lse of the same kernel over every causal block.
+        Returns (C [H, T], O_dense, lse_dense); run() must have been called."""
+        if getattr(self, "_dense_wl", None) is None:
+            self._dense_wl = causal_worklist(self.shape, q.device)
+        Od, ld = attention_fwd(q, k, v, self._dense_wl, self.shape, self.status, scale)
+        return coverage(self.lse, ld, self.shape), Od, ld
 
 
 # ---------------------------------------------------------------- decode

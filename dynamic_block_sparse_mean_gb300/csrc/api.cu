@@ -1,6 +1,7 @@
 // C ABI of libbsa.so: argument checks, workspace sizing and dispatch to the
 // launchers.  Every entry point validates its arguments before anything is
 // enqueued; nothing here allocates, copies or synchronises.
+#include <climits>
 #include <math.h>
 
 #include <mutex>
@@ -157,6 +158,31 @@ bsa_status_t bsa_build_worklist_noalloc(const bsa_shape_t *shape, int32_t k_max,
   if (bsa::worklist_noalloc_scratch(&scratch) != cudaSuccess) return BSA_ERR_LAUNCH;
   return launched(bsa::launch_worklist(*shape, k_max, J, counts, row_ptr, col_idx, work,
                                        bucket_off, dev_status, scratch, stream));
+}
+
+size_t bsa_causal_worklist_capacity(const bsa_shape_t *shape) {
+  if (!shape_ok(shape)) return 0;
+  return bsa::causal_worklist_capacity(*shape);
+}
+
+bsa_status_t bsa_build_causal_worklist(const bsa_shape_t *shape, int32_t *row_ptr,
+                                       int32_t *col_idx, int32_t *work, int32_t *bucket_off,
+                                       void *ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!shape_ok(shape) || row_ptr == nullptr || col_idx == nullptr || work == nullptr ||
+      bucket_off == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (bsa::causal_worklist_capacity(*shape) > (size_t)INT32_MAX) return BSA_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < bsa::worklist_workspace_bytes(*shape, 1))
+    return BSA_ERR_WORKSPACE;
+  return launched(
+      bsa::launch_causal_worklist(*shape, row_ptr, col_idx, work, bucket_off, ws, stream));
+}
+
+bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
+                          const float *lse_dense, float *C, cudaStream_t stream) {
+  if (!shape_ok(shape) || lse_sparse == nullptr || lse_dense == nullptr || C == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_coverage(*shape, lse_sparse, lse_dense, C, stream));
 }
 
 bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const void *K,

@@ -63,6 +63,12 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
                             cudaStream_t st);
+// Density-1 worklist (every causal block) and coverage of eq.(10) (worklist.cu).
+size_t causal_worklist_capacity(const bsa_shape_t &s);
+cudaError_t launch_causal_worklist(const bsa_shape_t &s, int32_t *row_ptr, int32_t *col_idx,
+                                   int32_t *work, int32_t *bucket_off, void *ws, cudaStream_t st);
+cudaError_t launch_coverage(const bsa_shape_t &s, const float *lse_sparse, const float *lse_dense,
+                            float *C, cudaStream_t st);
 // Device address of the fixed scratch array used by bsa_build_worklist_noalloc.
 cudaError_t worklist_noalloc_scratch(int32_t **out);
 

@@ -5,6 +5,7 @@
 //   2. scan kernel   row_ptr by prefix sum, and the work list: a stable counting
 //                    sort of rows by capacity bucket, largest first (one CTA)
 //   3. fill kernel   copies the block ids into col_idx (grid-wide)
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -161,6 +162,30 @@ __global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__r
   }
 }
 
+// Density 1 (every causal block): row r of a sequence with nb blocks holds 0..r.
+__global__ void wl_causal_rows_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ code,
+                                      int nrows, int Nq, int Hk, int b) {
+  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
+       row += gridDim.x * blockDim.x) {
+    const int r = row % Nq, i = row / (Nq * Hk);
+    const int nb = (cu[i + 1] - cu[i] + b - 1) / b;
+    code[row] = r < nb ? r + 1 : 0;
+  }
+}
+
+__global__ void wl_causal_fill_kernel(const int32_t *__restrict__ code,
+                                      const int32_t *__restrict__ row_ptr,
+                                      int32_t *__restrict__ col_idx, int nrows) {
+  // one warp per row: the row's block ids 0 .. c - 1
+  const int lane = threadIdx.x % 32;
+  for (int row = (blockIdx.x * blockDim.x + threadIdx.x) / 32; row < nrows;
+       row += gridDim.x * blockDim.x / 32) {
+    const int c = code[row];
+    int32_t *out = col_idx + row_ptr[row];
+    for (int e = lane; e < c; e += 32) out[e] = e;
+  }
+}
+
 // Scratch of bsa_build_worklist_noalloc: one row code per row, shared by every
 // call on a device.  Host code must not pass this name to a kernel (on the host
 // it is only a stand-in); it passes the address cudaGetSymbolAddress returns.
@@ -209,6 +234,45 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
   if (e != cudaSuccess) return e;
   wl_fill_kernel<<<max(blocks, 1), 256, 0, st>>>(J, code, row_ptr, col_idx, nrows, s.max_blocks,
                                                  k_max);
+  return cudaGetLastError();
+}
+
+size_t causal_worklist_capacity(const bsa_shape_t &s) {
+  return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * (s.max_blocks + 1) / 2;
+}
+
+cudaError_t launch_causal_worklist(const bsa_shape_t &s, int32_t *row_ptr, int32_t *col_idx,
+                                   int32_t *work, int32_t *bucket_off, void *ws, cudaStream_t st) {
+  const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
+  int32_t *code = static_cast<int32_t *>(ws);
+  const int blocks = max(1, min(4 * num_sms(), (nrows + 255) / 256));
+  wl_causal_rows_kernel<<<blocks, 256, 0, st>>>(s.cu_seqlens, code, nrows, s.max_blocks,
+                                                s.num_kv_heads, s.block);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wl_scan_kernel<<<1, kScanThreads, 0, st>>>(code, row_ptr, work, bucket_off, nrows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int fblocks = max(1, min(8 * num_sms(), (nrows + 7) / 8));
+  wl_causal_fill_kernel<<<fblocks, 256, 0, st>>>(code, row_ptr, col_idx, nrows);
+  return cudaGetLastError();
+}
+
+// Coverage of eq.(10): C = exp(lse_sparse - lse_dense) elementwise over [H, T].
+namespace {
+__global__ void coverage_kernel(const float *__restrict__ ls, const float *__restrict__ ld,
+                                float *__restrict__ C, size_t n) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x)
+    C[e] = expf(ls[e] - ld[e]);
+}
+}  // namespace
+
+cudaError_t launch_coverage(const bsa_shape_t &s, const float *lse_sparse, const float *lse_dense,
+                            float *C, cudaStream_t st) {
+  const size_t n = (size_t)s.num_heads * s.total_tokens;
+  const int blocks = (int)std::min<size_t>((size_t)8 * num_sms(), (n + 255) / 256);
+  coverage_kernel<<<std::max(blocks, 1), 256, 0, st>>>(lse_sparse, lse_dense, C, n);
   return cudaGetLastError();
 }
 

@@ -270,6 +270,33 @@ bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
                               int32_t *dev_status, void *ws, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Density-1 worklist — every causal block: row r of a sequence holds blocks
+ *   0 .. r ([P2] §3.1 validation, the dense side of the second layer; §2.2 the
+ *   dense causal baseline).  Same outputs as bsa_build_worklist, fed to
+ *   bsa_attention_fwd it computes dense causal attention with the same kernel:
+ *   the reference for the coverage below and for density-1 timing.  No J and no
+ *   row-length limit (rows longer than BSA_MAX_K go to the longest bucket).
+ *   col_idx  : at least bsa_causal_worklist_capacity() int32 entries (an upper
+ *              bound: B * H_kv * N_q (N_q + 1) / 2); larger than INT32_MAX entries:
+ *              BSA_ERR_UNSUPPORTED.
+ *   ws       : at least bsa_worklist_workspace_size(shape, 1) bytes.
+ * ------------------------------------------------------------------------- */
+size_t bsa_causal_worklist_capacity(const bsa_shape_t *shape);
+bsa_status_t bsa_build_causal_worklist(const bsa_shape_t *shape, int32_t *row_ptr,
+                                       int32_t *col_idx, int32_t *work, int32_t *bucket_off,
+                                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Coverage C_i of [P2] §3.1 eq.(10): the dense softmax mass that the selected
+ *   blocks hold, per query head and token, computed as
+ *   C = exp(lse_sparse - lse_dense) from the lse of bsa_attention_fwd on the
+ *   routed worklist and on the density-1 worklist (same scale).
+ *   lse_sparse, lse_dense : [H, T] fp32;   C : [H, T] fp32, in (0, 1] up to rounding.
+ * ------------------------------------------------------------------------- */
+bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
+                          const float *lse_dense, float *C, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status_t status);
 

@@ -322,3 +322,66 @@ def test_union_routing_end_to_end(case):
     mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo,
                                            np.ones(lo.shape, dtype=bool))
     assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS, (mx, mean, lmx)
+
+
+# Density-1 worklist and the coverage C_i of eq.(10).
+DENSE_CASES = [
+    ("dense_ragged_gqa4", [700, 129, 1500], 8, 2, 128, 64, None),
+    # N_q = 258 > BSA_MAX_K: rows longer than any routed row; sampled rows only
+    ("dense_258_blocks", [257 * 64 + 10], 2, 1, 64, 64, [(0, 0, 0), (0, 0, 128), (0, 0, 256), (0, 0, 257)]),
+]
+
+
+@pytest.mark.parametrize("case", DENSE_CASES, ids=[c[0] for c in DENSE_CASES])
+def test_causal_worklist_gives_dense_attention(case):
+    name, lengths, H, Hk, d, b, rows = case
+    x = synth.gen_prefill(lengths, H, Hk, d, b, 13, "iid", "bf16")
+    q, k, v = upload(x)
+    sh = shape_of(x, H, Hk)
+    wl = bsa.causal_worklist(sh, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    torch.cuda.synchronize()
+    bsa.check_status(status)
+    # CSR: row r of a sequence holds 0 .. r, rows past a sequence's end are empty
+    info = oracle.seq_info(x.cu_seqlens, b)
+    rp = wl.row_ptr.cpu().numpy()
+    lens = np.diff(rp)
+    Nq = sh.max_blocks
+    for i, (_, _, nb) in enumerate(info):
+        for h in range(Hk):
+            base = (i * Hk + h) * Nq
+            assert list(lens[base:base + Nq]) == [r + 1 for r in range(nb)] + [0] * (Nq - nb)
+    ci = wl.col_idx.cpu().numpy()
+    for row in (0, Nq - 1, len(lens) - 1):
+        if lens[row]:
+            assert list(ci[rp[row]:rp[row + 1]]) == list(range(lens[row]))
+    bo = wl.bucket_off.cpu().numpy()
+    assert bo[-1] == int((lens > 0).sum())
+    # dense causal attention through the same kernel
+    Ja, ca = oracle.causal_all_blocks(x.cu_seqlens, b, Hk)
+    Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
+                              x.cu_seqlens, b, H // Hk, Ja, ca, rows=rows)
+    mask = ~np.isnan(lo)
+    mx, mean, lmx, _, _ = attention_errors(O.float().cpu().numpy(), lse.cpu().numpy(), Oo, lo, mask)
+    assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS, (mx, mean, lmx)
+
+
+def test_coverage_matches_oracle():
+    lengths, H, Hk, d, b = [900, 400], 8, 2, 128, 64
+    x = synth.gen_prefill(lengths, H, Hk, d, b, 17, "iid", "bf16")
+    q, k, v = upload(x)
+    params = bsa.RouteParams(oracle.TOPK, 4, 0, 0.0, True)
+    plan = bsa.PrefillPlan(x.cu_seqlens, H, Hk, d, b, params, device="cuda")
+    plan.run(q, k, v)
+    C, _, _ = plan.coverage(q, k, v)
+    torch.cuda.synchronize()
+    bsa.check_status(plan.status)
+    Jg = plan.J.cpu().numpy().astype(np.int64)
+    cg = plan.counts.cpu().numpy().astype(np.int64)
+    Co = oracle.coverage(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, b, H // Hk, Jg, cg)
+    Cg = C.cpu().numpy()
+    assert not np.isnan(Co).any()
+    # C = exp(lse_sparse - lse_dense): each lse within BF16_LSE_ABS of float64
+    assert np.abs(Cg - Co).max() <= 2 * BF16_LSE_ABS + 1e-4, np.abs(Cg - Co).max()
+    assert Cg.min() > 0 and Cg.max() <= 1 + 2 * BF16_LSE_ABS
