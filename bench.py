@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-quality", action="store_true",
+                    help="skip the coverage / planted-recall / density-1 leg")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the paged decode (a diagnostic line, e.g. for profiling)")
     ap.add_argument("--decode-reqs", type=int, default=None,
@@ -236,6 +238,58 @@ def bench_prefill(w, steps, warmup, device, world, sampler):
                router_flops=accounting.router_flops(x.cu_seqlens, w.block, w.num_heads, w.head_dim),
                attn_bytes=accounting.attention_bytes(w.num_heads, w.num_kv_heads, T, w.head_dim))
     return res
+
+
+def router_quality(res, w, device):
+    """Outside the timed loop: the coverage C_i of eq.(10) of the routed rows
+    (the lse of the routed attention against the lse of the same kernel over every
+    causal block), the recall of planted (key block, query block) pairs, and the
+    density-1 attention time with the same kernel."""
+    import dynamic_block_sparse_mean_gb300 as bsa
+    from dynamic_block_sparse_mean_gb300 import accounting
+    plan, q, k, v, x = res["plan"], res["q"], res["k"], res["v"], res["x"]
+    dense = bsa.causal_worklist(plan.shape, device)
+    for _ in range(2):
+        Od, ld = bsa.attention_fwd(q, k, v, dense, plan.shape, plan.status)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    t0.record()
+    for _ in range(reps):
+        Od, ld = bsa.attention_fwd(q, k, v, dense, plan.shape, plan.status)
+    t1.record()
+    torch.cuda.synchronize(device)
+    dense_ms = t0.elapsed_time(t1) / reps
+    plan.attend(q, k, v)
+    C = bsa.coverage(plan.lse, ld, plan.shape)
+    torch.cuda.synchronize(device)
+    bsa.check_status(plan.status)
+    c = C.flatten().float()
+    qs = torch.quantile(c[:min(c.numel(), 1 << 24)], torch.tensor([0.001, 0.01, 0.05, 0.5],
+                                                                  device=device)).tolist()
+    G = w.num_heads // w.num_kv_heads
+    info = []
+    for i in range(len(x.cu_seqlens) - 1):
+        nb = (int(x.cu_seqlens[i + 1] - x.cu_seqlens[i]) + w.block - 1) // w.block
+        info.append(nb)
+    dense_counts = np.zeros_like(plan.counts.cpu().numpy())
+    for i, nb in enumerate(info):
+        dense_counts[i, :, :nb] = np.arange(1, nb + 1)
+    dense_flops = accounting.attention_tile_flops(dense_counts, G, w.block, w.head_dim)
+    out = {"coverage": {"mean": float(c.mean()), "min": float(c.min()), "p0.1": qs[0],
+                        "p1": qs[1], "p5": qs[2], "p50": qs[3],
+                        "frac_below_0.9": float((c < 0.9).float().mean())},
+           "dense_attention_ms": dense_ms,
+           "dense_attention_tflops": dense_flops / (dense_ms * 1e-3) / 1e12,
+           "density": res["flops"] / dense_flops,
+           "speedup_vs_dense": dense_ms / res["stages"]["attention"]}
+    if x.planted:
+        J = plan.J.cpu().numpy()
+        cnt = plan.counts.cpu().numpy()
+        hit = sum(1 for (h, j, u) in x.planted if j in set(J[0, h, u, :cnt[0, h, u]].tolist()))
+        out["planted_recall"] = hit / len(x.planted)
+        out["planted_pairs"] = len(x.planted)
+    del Od, ld, C, dense
+    return out
 
 
 def bench_e2e(res, steps, device):
@@ -436,6 +490,7 @@ def run_native(args):
                 "peak_source": f"{src} bf16 burst", "traffic": traffic,
                 "algorithmic_flops_per_launch": res["flops"],
                 "compulsory_bytes_per_launch": res["attn_bytes"]}
+    quality = router_quality(res, w, device) if not args.no_quality else None
     e2e = None
     if not args.no_e2e:
         e_ms, bi, bo = bench_e2e(res, max(3, min(args.steps, 20)), device)
@@ -476,6 +531,7 @@ def run_native(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "decode": dec,
+        "router_quality": quality,
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
