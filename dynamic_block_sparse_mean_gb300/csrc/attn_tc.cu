@@ -58,7 +58,9 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTile;
   static constexpr int kOffV = kOffK + NS * kStage;
-  static constexpr int kOffBar = kOffV + NS * kStage;
+  static constexpr int kStageO = 128 * 128;      // output staging: 128 rows x 64 columns
+  static constexpr int kOffStageO = kOffV + NS * kStage;  // one half-tile per M-tile
+  static constexpr int kOffBar = kOffStageO + 2 * kStageO;
   // barrier slots
   static constexpr int B_QFULL = 0, B_QEMPTY = 1;
   static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + NS;
@@ -66,7 +68,9 @@ struct Cfg {
   static constexpr int B_SFULL = B_VEMPTY + NS, B_PFULL = B_SFULL + 2;
   static constexpr int B_OFREE = B_PFULL + 2;
   static constexpr int B_OFINAL = B_OFREE + 2;    // all PV of a unit done (once per unit)
-  static constexpr int B_FINAL = B_OFINAL + 2;
+  static constexpr int B_OSTAGED = B_OFINAL + 2;  // a staged output half is complete (4 warps)
+  static constexpr int B_OSFREE = B_OSTAGED + 2;  // the staging buffer was read by its store
+  static constexpr int B_FINAL = B_OSFREE + 2;
   static constexpr int kNumBars = B_FINAL + 1;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffCtl + 16;
@@ -148,6 +152,20 @@ BSA_DEV void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
       : "memory");
 }
+
+// Shared -> global tensor store of one box (bulk async group of this thread).
+BSA_DEV void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+BSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+BSA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has completed.
+BSA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Row max over 64 TMEM columns with the reducing load (sm_103a tcgen05.ld.red):
 // each lane gets the max of the columns it loads; two loads, one wait.
@@ -337,7 +355,8 @@ BSA_DEV float exp_step(uint32_t tS, uint64_t scale2, uint64_t negm, const int (&
 template <int D, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const AttnParams p) {
   using C = Cfg<D, BK>;
   constexpr int BPS = C::kBPS;
   extern __shared__ uint8_t smem_raw[];
@@ -364,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_PFULL + t), 4);
       mbar_init(bar(C::B_OFREE + t), 4);
       mbar_init(bar(C::B_OFINAL + t), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_OSTAGED + t), 4);
+      mbar_init(bar(C::B_OSFREE + t), 1);
     }
     mbar_init(bar(C::B_FINAL), 1);
     *abort_flag = 0;
@@ -576,29 +599,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + C::colS(t);
     int kstep = 0;                    // steps of this tile (S / P / O-done phases)
     int units = 0;                    // units of this tile (O-final phases)
+    int ostage = 0;                   // output staging uses of this tile
     bool ok = true;
     const uint64_t scale2 = pack2(p.scale_log2, p.scale_log2);
+    // Position of the diagonal block r in a unit's row (the token-level triangle),
+    // found by the whole warp; -1 if the row does not hold it.
+    auto diag_of = [&](const Unit &w) {
+      int dj = -1;
+      for (int j0 = 0; j0 < w.nkv; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, j < w.nkv && __ldg(p.col_idx + w.kv0 + j) == w.r);
+        if (hit != 0u && dj < 0) dj = j0 + __ffs(hit) - 1;
+      }
+      return dj;
+    };
     Unit nx;
-    if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
+    int nx_diag = -1;
+    if (blockIdx.x < total_units) {
+      nx = decode_unit(p, blockIdx.x);
+      nx_diag = diag_of(nx);
+    }
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit x = nx;
-      if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
-      if (t >= x.nt) continue;
+      const int diag_j = nx_diag;
+      const bool has_next = u + (int)gridDim.x < total_units;
+      if (has_next) nx = decode_unit(p, u + gridDim.x);  // prefetch
+      if (t >= x.nt) {
+        if (has_next) nx_diag = diag_of(nx);
+        continue;
+      }
       const int nsteps = (x.nkv + BPS - 1) / BPS;
       const int grow = (2 * x.pair + t) * 128 + rho;   // row within the group's G*b rows
       const bool row_valid = grow < p.G * BK;
       const int hq = x.h * p.G + grow / BK;
       const int tok_in_blk = grow % BK;
       const int tq = x.r * BK + tok_in_blk;            // sequence-relative query position
-      // Position of the diagonal block r in the row (the token-level triangle), found
-      // once per unit by the whole warp; -1 if the row does not hold it.
-      int diag_j = -1;
-      for (int j0 = 0; j0 < x.nkv; j0 += 32) {
-        const int j = j0 + lane;
-        const unsigned hit =
-            __ballot_sync(0xffffffffu, j < x.nkv && __ldg(p.col_idx + x.kv0 + j) == x.r);
-        if (hit != 0u && diag_j < 0) diag_j = j0 + __ffs(hit) - 1;
-      }
       float m_used = -INFINITY, l = 0.f;
       for (int s = 0; s < nsteps; ++s, ++kstep) {
         // Column limits of the two 64-column halves of this step: keys past the
@@ -655,6 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
+        // The next unit's diagonal position: its load overlaps the wait for S(1).
+        if (s == 0 && has_next) nx_diag = diag_of(nx);
       }
       if (!ok) break;
       // epilogue: O = u / l, lse = (m + log2 l) ln 2
@@ -663,32 +701,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool store = row_valid && tq < x.n;
       const float inv_l = 1.f / l;
-      uint16_t *orow = p.O + ((size_t)hq * p.T + x.s0 + tq) * D;
+      // Read the whole O row as bf16 pairs first, release O to the next unit's PV,
+      // and only then write the row out.
+      uint32_t ob[D / 2];
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ro[32];
         tmem_ld32(tO + c0, ro);
-        if (store) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 0]) * inv_l, __uint_as_float(ro[q4 * 8 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 2]) * inv_l, __uint_as_float(ro[q4 * 8 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 4]) * inv_l, __uint_as_float(ro[q4 * 8 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(ro[q4 * 8 + 6]) * inv_l, __uint_as_float(ro[q4 * 8 + 7]) * inv_l);
-            dst[q4] = w;
-          }
-        }
+        for (int e = 0; e < 16; ++e)
+          ob[c0 / 2 + e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv_l,
+                                       __uint_as_float(ro[2 * e + 1]) * inv_l);
       }
-      if (store && p.lse != nullptr)
-        p.lse[(size_t)hq * p.T + x.s0 + tq] = (m_used + fast_log2(l)) * 0.6931471805599453f;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_OFREE + t));
+      if (store && p.lse != nullptr)
+        p.lse[(size_t)hq * p.T + x.s0 + tq] = (m_used + fast_log2(l)) * 0.6931471805599453f;
+      // A tile whose 128 rows are all valid query rows of a full block goes out
+      // through shared memory and tensor stores (one 64-column half at a time, in
+      // the 128-byte-swizzled layout of the store box); other tiles (sequence
+      // tails, partial groups) store their valid rows directly.
+      const bool via_tma = (2 * x.pair + t + 1) * 128 <= p.G * BK && (x.r + 1) * BK <= x.n;
+      if (via_tma) {
+        const uint32_t stg = sbase + C::kOffStageO + t * C::kStageO;
+        const bool elected = wq == 0 && lane == 0;
+#pragma unroll
+        for (int hh = 0; hh < C::kPanels; ++hh, ++ostage) {
+          // the previous store out of this buffer has finished reading it
+          if (!(ok = mbar_wait(bar(C::B_OSFREE + t), (ostage & 1) ^ 1, abort_flag, p.status)))
+            break;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(stg + rho * 128 + ((c ^ (rho & 7)) << 4), ob[hh * 32 + 4 * c],
+                         ob[hh * 32 + 4 * c + 1], ob[hh * 32 + 4 * c + 2], ob[hh * 32 + 4 * c + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_OSTAGED + t));
+          if (elected) {
+            if (!(ok = mbar_wait(bar(C::B_OSTAGED + t), ostage & 1, abort_flag, p.status))) break;
+            tma_store_3d(&tmO, stg, hh * 64, x.s0 + x.r * BK,
+                         x.h * p.G + ((2 * x.pair + t) * 128) / BK);
+            bulk_commit();
+            bulk_wait_read();
+            mbar_arrive(bar(C::B_OSFREE + t));
+          }
+        }
+        if (!ok) break;
+      } else if (store) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.O + ((size_t)hq * p.T + x.s0 + tq) * D);
+#pragma unroll
+        for (int q4 = 0; q4 < D / 8; ++q4)
+          dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+      }
     }
   }
 
+  if (warp < 8 && (warp % 4) == 0 && lane == 0) bulk_wait_all();  // output stores done
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -705,7 +774,9 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
                       int32_t *dev_status, cudaStream_t st) {
   using C = Cfg<D, BK>;
   CUtensorMap mq, mk, mv;
-  if (!make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
+  CUtensorMap mo;
+  if (!make_tmap_3d_bf16(&mo, O, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
+      !make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
       !make_tmap_3d_bf16(&mk, K, D, s.total_tokens, s.num_kv_heads, 64, BK, 1) ||
       !make_tmap_3d_bf16(&mv, V, D, s.total_tokens, s.num_kv_heads, 64, BK, 1))
     return cudaErrorInvalidValue;
@@ -731,7 +802,7 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   if (e != cudaSuccess) return e;
   const long long max_units = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks * p.npairs;
   const int grid = (int)std::min<long long>(num_sms(), std::max<long long>(1, max_units));
-  attn_tc_kernel<D, BK><<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  attn_tc_kernel<D, BK><<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
