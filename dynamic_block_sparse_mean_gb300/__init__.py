@@ -28,7 +28,8 @@ ROUTE_THRESHOLD = 1
 
 __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "PrefillPlan",
            "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
-           "attention_fwd", "causal_worklist", "coverage", "page_summaries", "decode_paged",
+           "attention_fwd", "causal_worklist", "coverage", "page_summaries", "page_summaries_append",
+           "decode_paged",
            "check_status", "library_path"]
 
 
@@ -325,6 +326,18 @@ def page_summaries(k_cache, block_table, context_lens, out=None):
     check("bsa_page_summaries", _lib.lib().bsa_page_summaries(
         ctypes.byref(s), _p(k_cache), _p(block_table), _p(context_lens), _p(out), _stream()))
     return out
+
+
+def page_summaries_append(k_cache, block_table, context_lens, page_sum, page_summ):
+    """eq.(11) streaming update for the key each request just appended
+    (bsa_page_summaries_append): page_sum is the running-sum state, page_summ the
+    means; context_lens are the counts after the append (0 skips a request)."""
+    P, Hk, page, d = k_cache.shape
+    s = _lib.DecodeShape(block_table.shape[0], Hk, Hk, d, page, block_table.shape[1], P, 1)
+    check("bsa_page_summaries_append", _lib.lib().bsa_page_summaries_append(
+        ctypes.byref(s), _p(k_cache), _p(block_table), _p(context_lens), _p(page_sum),
+        _p(page_summ), _stream()))
+    return page_summ
 
 
 class DecodePlan:

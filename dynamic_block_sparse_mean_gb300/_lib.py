@@ -67,6 +67,7 @@ PROTOTYPES = {
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),
     "bsa_page_summaries": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V]),
+    "bsa_page_summaries_append": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V, V]),
     "bsa_decode_workspace_size": (SZ, [ctypes.POINTER(DecodeShape)]),
     "bsa_decode_paged": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V, V, F32, V, V, V, V, V,
                                V, SZ, V]),

@@ -218,6 +218,17 @@ bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_c
                                              page_summ, stream));
 }
 
+bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const void *k_cache,
+                                       const int32_t *block_table, const int32_t *context_lens,
+                                       float *page_sum, float *page_summ, cudaStream_t stream) {
+  if (!decode_ok(shape) || k_cache == nullptr || block_table == nullptr ||
+      context_lens == nullptr || page_sum == nullptr || page_summ == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!decode_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  return launched(bsa::launch_page_summaries_append(*shape, k_cache, block_table, context_lens,
+                                                    page_sum, page_summ, stream));
+}
+
 size_t bsa_decode_workspace_size(const bsa_decode_shape_t *shape) {
   if (!decode_ok(shape)) return 0;
   return bsa::decode_workspace_bytes(*shape);

@@ -47,6 +47,10 @@ cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const fl
 // a1 and the decode page summaries (summaries.cu)
 cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
                                    cudaStream_t st);
+cudaError_t launch_page_summaries_append(const bsa_decode_shape_t &s, const void *k_cache,
+                                         const int32_t *block_table,
+                                         const int32_t *context_lens, float *page_sum,
+                                         float *page_summ, cudaStream_t st);
 cudaError_t launch_page_summaries(const bsa_decode_shape_t &s, const void *k_cache,
                                   const int32_t *block_table, const int32_t *context_lens,
                                   float *page_summ, cudaStream_t st);

@@ -94,7 +94,34 @@ __global__ void __launch_bounds__(kThreads) page_summaries_kernel(
   block_mean<uint16_t>(base, nrows, d, d, ps + ((size_t)phys * Hk + h) * d, red);
 }
 
+// grid (R, H_kv), d threads: eq.(11) for the key each request just appended.
+__global__ void page_summaries_append_kernel(const uint16_t *__restrict__ kc,
+                                             const int32_t *__restrict__ bt,
+                                             const int32_t *__restrict__ lens,
+                                             float *__restrict__ psum, float *__restrict__ ps,
+                                             int max_pages, int Hk, int page, int d) {
+  const int rho = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int n = lens[rho];  // keys after the append; the new one sits at n - 1
+  if (n < 1 || c >= d) return;
+  const int p = (n - 1) / page, slot = (n - 1) % page;
+  const size_t row = (size_t)bt[(size_t)rho * max_pages + p] * Hk + h;
+  const float k = bf16_to_f32(kc[(row * page + slot) * d + c]);
+  const float sum = slot == 0 ? k : psum[row * d + c] + k;  // s <- s + k_t (a new page starts at k)
+  psum[row * d + c] = sum;
+  ps[row * d + c] = sum / (float)(slot + 1);                 // c = s / r
+}
+
 }  // namespace
+
+cudaError_t launch_page_summaries_append(const bsa_decode_shape_t &s, const void *k_cache,
+                                         const int32_t *block_table,
+                                         const int32_t *context_lens, float *page_sum,
+                                         float *page_summ, cudaStream_t st) {
+  page_summaries_append_kernel<<<dim3(s.num_reqs, s.num_kv_heads), s.head_dim, 0, st>>>(
+      static_cast<const uint16_t *>(k_cache), block_table, context_lens, page_sum, page_summ,
+      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
                                    cudaStream_t st) {

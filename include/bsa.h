@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 2
+#define BSA_VERSION 3
 
 typedef enum {
   BSA_OK = 0,
@@ -244,6 +244,23 @@ bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const vo
 bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_cache,
                                 const int32_t *block_table, const int32_t *context_lens,
                                 float *page_summ, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Streaming page summaries — [P2] §3.1 eq.(11): the summary of the block still
+ *   being filled is cache state kept as a vector sum and a count,
+ *   s <- s + k_t, c = s / r.  Call after every request appended one key (already
+ *   written to k_cache at position context_lens[rho] - 1): the page holding it
+ *   gets s <- s + k (s <- k when the key opens the page, r = 1) and
+ *   c = s / r, r = the page's key count.  Other pages are untouched.
+ *   page_sum  : [P, H_kv, d] fp32 running sums (the state; a page's sum must be
+ *               valid for its keys before the append, e.g. built by appending
+ *               from an empty page);
+ *   page_summ : [P, H_kv, d] fp32 means, as bsa_page_summaries writes them.
+ *   context_lens : [R] int32, counts after the append (>= 1; 0 skips a request).
+ * ------------------------------------------------------------------------- */
+bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const void *k_cache,
+                                       const int32_t *block_table, const int32_t *context_lens,
+                                       float *page_sum, float *page_summ, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * a6. Paged sparse decode — [P2] §2.2 (decode reads the summaries, O(N_k d_r),

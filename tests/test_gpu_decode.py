@@ -83,3 +83,29 @@ def test_decode_every_page_selected_matches_dense():
     torch.cuda.synchronize()
     check_decode(x, 64, o.float().cpu().numpy(), lse.cpu().numpy(), sel.cpu().numpy(),
                  cnt.cpu().numpy(), range(2), 4)
+
+
+def test_streaming_page_summaries_follow_eq11():
+    # Keys appended one per step from empty pages (eq.(11): s <- s + k, c = s / r);
+    # the lengths cross page boundaries (page 64) in both directions.
+    final = np.array([63, 64, 65, 130, 1, 200])
+    x = synth.gen_decode(final, 4, 2, 128, 64, seed=51, max_pages=4)
+    q, kc, vc, bt, cl = _upload(x)
+    P, Hk, page, d = kc.shape
+    psum = torch.zeros(P, Hk, d, dtype=torch.float32, device="cuda")
+    summ = torch.zeros(P, Hk, d, dtype=torch.float32, device="cuda")
+    for t in range(int(final.max())):
+        lens_t = np.where(t < final, t + 1, 0).astype(np.int32)   # 0: no append this step
+        bsa.page_summaries_append(kc, bt, torch.as_tensor(lens_t, device="cuda"), psum, summ)
+    torch.cuda.synchronize()
+    batch = bsa.page_summaries(kc, bt, cl)
+    sg, bg = summ.cpu().numpy(), batch.cpu().numpy()
+    kf = synth.bf16_bits_to_f32(x.k_cache).astype(np.float64)
+    for rho, n in enumerate(final):
+        for p in range((n + 63) // 64):
+            phys = int(x.block_table[rho, p])
+            keys = kf[phys, :, :min(64, n - p * 64)]        # the page's valid keys, in order
+            for h in range(Hk):
+                want = oracle.streaming_summary(keys[h])[-1]
+                assert np.abs(sg[phys, h] - want).max() < 1e-5
+                assert np.abs(sg[phys, h] - bg[phys, h]).max() < 1e-5
