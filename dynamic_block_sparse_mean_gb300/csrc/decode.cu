@@ -320,6 +320,7 @@ BSA_DEV void bar_warps_wait(uint32_t bar, uint32_t parity, volatile int32_t *abo
   ok = __all_sync(0xffffffffu, ok);
 }
 
+template <int G>
 __global__ void __launch_bounds__(kDecThreads, 1)
     dec_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const DecParams p) {
@@ -521,9 +522,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       tc_fence_after();
       uint32_t r[16];
       tmem_ld16(tmem + lane_base + kColS + 16 * b, r);
-      float x[kMaxG];
+      float x[G];
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
+      for (int g = 0; g < G; ++g) {
         x[g] = valid ? __uint_as_float(r[g]) * p.scale_log2 : -INFINITY;
         float m = x[g];
 #pragma unroll
@@ -534,26 +535,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_MX + b));
       bar_warps_wait(bar(B_MX + b), (i / 2) & 1, abort_flag, p.status, ok);
       if (!ok) break;
-      float M[kMaxG], l[kMaxG];
+      float M[G], l[G];
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
+      for (int g = 0; g < G; ++g) {
         M[g] = fmaxf(fmaxf(red_m[(b * 4 + 0) * 16 + g], red_m[(b * 4 + 1) * 16 + g]),
                      fmaxf(red_m[(b * 4 + 2) * 16 + g], red_m[(b * 4 + 3) * 16 + g]));
         // a unit's first page always holds a valid key, so M is finite
-        const float pg = g < p.G ? fast_exp2(x[g] - M[g]) : 0.f;
+        const float pg = fast_exp2(x[g] - M[g]);
         l[g] = pg;
         const __nv_bfloat16 pb = __float2bfloat16_rn(pg);
         const uint32_t off = t_panel + (uint32_t)g * 128u + ((t_chunk ^ (uint32_t)(g & 7)) << 4) + t_in;
         *reinterpret_cast<__nv_bfloat16 *>(sm + kOffP + b * kPBytes + off) = pb;
       }
-      // Rows 8-15 of P^T are never written: they only feed columns of O^T that are
-      // never read (likewise rows 8-15 of the staged queries).
+      // Rows G-15 of P^T are never written: they only feed columns of O^T that are
+      // never read (likewise rows G-15 of the staged queries).
       fence_proxy_async_smem();  // P^T is read by the tensor cores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + b));
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
+      for (int g = 0; g < G; ++g) {
         float sum = l[g];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
@@ -566,23 +567,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (!ok) break;
       tc_fence_after();
       tmem_ld16(tmem + lane_base + kColO + 16 * b, r);
-      float *po = p.part_o + (size_t)u * p.G * kD;
+      float *po = p.part_o + (size_t)u * G * kD;
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g)
-        if (g < p.G) po[g * kD + t] = __uint_as_float(r[g]);
+      for (int g = 0; g < G; ++g) po[g * kD + t] = __uint_as_float(r[g]);
       bar_warps_wait(bar(B_LS + b), (i / 2) & 1, abort_flag, p.status, ok);
       if (!ok) break;
-      if (t < p.G) {
+      if (t < G) {
         float lsum = 0.f, mt = 0.f;
 #pragma unroll
-        for (int g = 0; g < kMaxG; ++g)
+        for (int g = 0; g < G; ++g)
           if (g == t) {
             lsum = red_l[(b * 4 + 0) * 16 + g] + red_l[(b * 4 + 1) * 16 + g] +
                    red_l[(b * 4 + 2) * 16 + g] + red_l[(b * 4 + 3) * 16 + g];
             mt = M[g];
           }
-        p.part_ml[((size_t)u * p.G + t) * 2] = mt;
-        p.part_ml[((size_t)u * p.G + t) * 2 + 1] = lsum;
+        p.part_ml[((size_t)u * G + t) * 2] = mt;
+        p.part_ml[((size_t)u * G + t) * 2 + 1] = lsum;
       }
       tc_fence_before();
     }
@@ -744,10 +744,12 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
   p.nchunk = nchunk;
   p.units = (int)units;
   p.oob_page = (int)zpages;
-  e = cudaFuncSetAttribute(dec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  auto *kern = G == 1 ? dec_tc_kernel<1> : G == 2 ? dec_tc_kernel<2> : G == 4 ? dec_tc_kernel<4>
+                                                                              : dec_tc_kernel<8>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<size_t>((size_t)num_sms(), units);
-  e = launch_dependent(dec_tc_kernel, dim3(grid), dim3(kDecThreads), kDecSmem, st, mq, mk, mv, p);
+  e = launch_dependent(kern, dim3(grid), dim3(kDecThreads), kDecSmem, st, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
   return launch_dependent(dec_merge_kernel, dim3(s.num_kv_heads, s.num_reqs), dim3(G * kD), 0, st,
                           part_ml, part_o, sel_counts, static_cast<uint16_t *>(o), lse,
