@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();    // Q, K, V and the worklist may come from earlier launches
 
   const int total_units = __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.npairs;
   const uint32_t smQ = sbase + C::kOffQ, smK = sbase + C::kOffK, smV = sbase + C::kOffV;
@@ -758,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp < 8 && (warp % 4) == 0 && lane == 0) bulk_wait_all();  // output stores done
+  grid_dep_launch();  // the next launch may be scheduled; it waits for this grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -802,8 +804,8 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   if (e != cudaSuccess) return e;
   const long long max_units = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks * p.npairs;
   const int grid = (int)std::min<long long>(num_sms(), std::max<long long>(1, max_units));
-  attn_tc_kernel<D, BK><<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError();
+  return launch_dependent(attn_tc_kernel<D, BK>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, mq,
+                          mk, mv, mo, p);
 }
 
 }  // namespace

@@ -120,28 +120,19 @@ __global__ void __launch_bounds__(kThreads) route_scores_kernel(
   }
 }
 
-struct Cand {
-  float v;
-  int idx;
-};
-
-BSA_DEV bool better(const Cand &a, const Cand &b) {
-  return a.v > b.v || (a.v == b.v && a.idx < b.idx);
+// Order-preserving map of a float score onto uint32 (larger score, larger key;
+// -0 and +0 map alike, as they compare equal).
+BSA_DEV uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-BSA_DEV Cand warp_best(Cand c) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Cand o;
-    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
-    o.idx = __shfl_xor_sync(0xffffffffu, c.idx, off);
-    if (better(o, c)) c = o;
-  }
-  return c;
-}
-
-// One warp per router row: forced blocks, then top-k / eq.(7) threshold, then sort.
-// Dynamic shared memory: N_q floats of scores, N_q bytes of flags, k_max ints.
+// One warp per router row: forced blocks, then top-k / eq.(7) threshold, then the
+// row in ascending order.  The dynamic picks are the k_dyn largest candidates under
+// (score desc, index asc), found by a radix select on order-preserving keys (8 bits
+// per pass from the top; it stops once the bin of the k-th key holds exactly the
+// keys still needed), then written with the forced blocks in one ordered pass.
+// Dynamic shared memory: N_q floats of scores, a 256-bin histogram, N_q flag bytes.
 __global__ void __launch_bounds__(32) route_select_kernel(
     const float *__restrict__ S, const int32_t *__restrict__ cu, int32_t *__restrict__ J,
     int32_t *__restrict__ counts, int Nq, int Hk, int b, int mode, int k_max, int k_min,
@@ -149,12 +140,13 @@ __global__ void __launch_bounds__(32) route_select_kernel(
     const int32_t *__restrict__ global_blocks) {
   extern __shared__ uint8_t sm[];
   float *sc = reinterpret_cast<float *>(sm);
-  int32_t *ids = reinterpret_cast<int32_t *>(sm + (size_t)Nq * 4);
-  uint8_t *taken = sm + (size_t)Nq * 4 + (size_t)(k_max + 2) * 4;
+  int32_t *hist = reinterpret_cast<int32_t *>(sm + (size_t)Nq * 4);
+  uint8_t *taken = sm + (size_t)Nq * 4 + 256 * 4;
   const int lane = threadIdx.x;
   const int row = blockIdx.x;
   const int r = row % Nq, h = (row / Nq) % Hk, i = row / (Nq * Hk);
   (void)h;
+  grid_dep_wait();  // the scores come from the previous launch
   const int n = cu[i + 1] - cu[i];
   const int nb = (n + b - 1) / b;
   int32_t *Jrow = J + (size_t)row * k_max;
@@ -178,14 +170,10 @@ __global__ void __launch_bounds__(32) route_select_kernel(
     if (gb >= 0 && gb < r) taken[gb] = 1;
   }
   __syncwarp();
-  int nhist = 0;  // forced history blocks (j < r), listed first in ids
-  for (int j0 = 0; j0 < r; j0 += 32) {
-    const int j = j0 + lane;
-    const bool f = j < r && taken[j];
-    const unsigned m = __ballot_sync(0xffffffffu, f);
-    if (f) ids[nhist + __popc(m & ((1u << lane) - 1u))] = j;
-    nhist += __popc(m);
-  }
+  int nhist = 0;  // forced history blocks (j < r)
+  for (int j = lane; j < r; j += 32) nhist += taken[j] ? 1 : 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) nhist += __shfl_xor_sync(0xffffffffu, nhist, off);
   const int nforced = nhist + 1;  // + the diagonal
   const int ncand = r - nhist;
 
@@ -209,41 +197,86 @@ __global__ void __launch_bounds__(32) route_select_kernel(
   }
   k_dyn = max(0, min(k_dyn, ncand));
 
-  // Local best among this lane's strided candidates.
-  auto local_best = [&]() {
-    Cand c{-INFINITY, 0x7fffffff};
-    for (int j = lane; j < r; j += 32)
-      if (!taken[j]) {
-        const Cand o{sc[j], j};
-        if (c.idx == 0x7fffffff || better(o, c)) c = o;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k_dyn;  // dynamic picks still to place at or below the current bin
+  if (k_dyn > 0 && k_dyn < ncand) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int e = lane; e < 256; e += 32) hist[e] = 0;
+      __syncwarp();
+      for (int j = lane; j < r; j += 32)
+        if (!taken[j]) {
+          const uint32_t kk = order_key(sc[j]);
+          if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
+        }
+      __syncwarp();
+      // lane l owns bins 255 - 8l .. 248 - 8l (descending); counts from the top
+      int loc[8], tot = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        loc[q] = hist[255 - 8 * lane - q];
+        tot += loc[q];
       }
-    return c;
-  };
-  Cand mine = local_best();
-  for (int k = 0; k < k_dyn; ++k) {
-    const Cand w = warp_best(mine);
-    if (lane == 0) ids[nforced + k] = w.idx;
-    if ((w.idx & 31) == lane) {
-      taken[w.idx] = 1;
-      mine = local_best();
+      int incl = tot;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int excl = incl - tot;
+      int bin = -1, above = 0, inbin = 0;
+      if (excl < remaining && incl >= remaining) {
+        int acc = excl;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (bin < 0 && acc + loc[q] >= remaining) {
+            bin = 255 - 8 * lane - q;
+            above = acc;
+            inbin = loc[q];
+          }
+          acc += loc[q];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, bin >= 0)) - 1;
+      bin = __shfl_sync(0xffffffffu, bin, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      inbin = __shfl_sync(0xffffffffu, inbin, src);
+      remaining -= above;
+      prefix |= (uint32_t)bin << shift;
+      mask |= 0xFFu << shift;
+      __syncwarp();  // every lane has read hist before the next pass clears it
+      // the k-th key's bin holds exactly the keys still needed: all are picked
+      if (inbin == remaining) break;
     }
-    __syncwarp();
   }
-  if (lane == 0) ids[nhist] = r;
-  __syncwarp();
-  const int cnt = nforced + k_dyn;
-  // Rank sort (ids are distinct) into ascending order.
-  for (int e = lane; e < k_max; e += 32) {
-    if (e < cnt) {
-      const int v = ids[e];
-      int rank = 0;
-      for (int f = 0; f < cnt; ++f) rank += ids[f] < v ? 1 : 0;
-      Jrow[rank] = v;
-    } else {
-      Jrow[e] = -1;
+  // One ordered pass: forced blocks, candidates above the k-th key's bin, and the
+  // first `remaining` candidates inside it (ties to the lower block index).
+  int w = 0, eq_seen = 0;
+  for (int j0 = 0; j0 <= r; j0 += 32) {
+    const int j = j0 + lane;
+    bool keep = false, eq = false;
+    if (j < r) {
+      if (taken[j]) {
+        keep = true;
+      } else if (k_dyn >= ncand) {
+        keep = k_dyn > 0;
+      } else if (k_dyn > 0) {
+        const uint32_t kk = order_key(sc[j]) & mask;
+        keep = kk > prefix;
+        eq = kk == prefix;
+      }
+    } else if (j == r) {
+      keep = true;  // the diagonal
     }
+    const unsigned em = __ballot_sync(0xffffffffu, eq);
+    if (eq) keep = eq_seen + __popc(em & ((1u << lane) - 1u)) < remaining;
+    eq_seen += __popc(em);
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    if (keep) Jrow[w + __popc(km & ((1u << lane) - 1u))] = j;
+    w += __popc(km);
   }
-  if (lane == 0) counts[row] = cnt;
+  for (int e = w + lane; e < k_max; e += 32) Jrow[e] = -1;
+  if (lane == 0) counts[row] = w;
+  grid_dep_launch();
 }
 
 }  // namespace
@@ -275,17 +308,16 @@ cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, cons
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = s.num_seqs * s.num_kv_heads * s.max_blocks;
-  const size_t sm = (size_t)s.max_blocks * 5 + (size_t)(p.k_max + 2) * 4 + 16;
+  const size_t sm = (size_t)s.max_blocks * 5 + 256 * 4 + 16;
   if (sm > 48 * 1024) {
     e = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
   }
-  route_select_kernel<<<rows, 32, sm, st>>>(S, s.cu_seqlens, J, counts, s.max_blocks,
-                                            s.num_kv_heads, s.block, p.mode, p.k_max, p.k_min,
-                                            p.tau_delta, p.force_sink, p.window, p.num_global,
-                                            p.global_blocks);
-  return cudaGetLastError();
+  return launch_dependent(route_select_kernel, dim3(rows), dim3(32), sm, st, S, s.cu_seqlens, J,
+                          counts, s.max_blocks, s.num_kv_heads, s.block, p.mode, p.k_max,
+                          p.k_min, p.tau_delta, p.force_sink, p.window, p.num_global,
+                          p.global_blocks);
 }
 
 }  // namespace bsa

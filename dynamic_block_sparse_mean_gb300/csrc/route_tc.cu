@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();    // Q, C and the split come from earlier launches
   const int total = p.B * p.Hk * p.Nq;
   const uint32_t smQ = sbase + C::kOffQ, smA = sbase + C::kOffA;
   const int heads_per_chunk = 256 / p.b;
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  grid_dep_launch();  // the next launch may be scheduled; it waits for this grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // C [rows, d] fp32 -> three bf16 planes [3, rows, d] with c = hi + mid + lo exactly
 // up to the last bf16 rounding (residuals of bf16 rounding are exact in fp32).
 __global__ void split3_kernel(const float *__restrict__ C, uint16_t *__restrict__ C3, size_t n) {
+  grid_dep_wait();  // C comes from the previous launch
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
     const float c = C[e];
@@ -283,6 +286,7 @@ __global__ void split3_kernel(const float *__restrict__ C, uint16_t *__restrict_
     C3[n + e] = *reinterpret_cast<const uint16_t *>(&mid);
     C3[2 * n + e] = *reinterpret_cast<const uint16_t *>(&lo);
   }
+  grid_dep_launch();
 }
 
 template <int D>
@@ -292,7 +296,10 @@ cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float 
   const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
   uint16_t *C3 = static_cast<uint16_t *>(ws);
   const size_t n = rows * D;
-  split3_kernel<<<(unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(C, C3, n);
+  cudaError_t e0 = launch_dependent(split3_kernel,
+                                    dim3((unsigned)std::min<size_t>((n + 255) / 256, 4096)),
+                                    dim3(256), 0, st, C, C3, n);
+  if (e0 != cudaSuccess) return e0;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int G = s.num_heads / s.num_kv_heads;
@@ -314,8 +321,8 @@ cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float 
                            Cf::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<size_t>(num_sms(), std::max<size_t>(1, rows));
-  route_tc_kernel<D><<<grid, kThreads, Cf::kSmemBytes, st>>>(mq, mc, p);
-  return cudaGetLastError();
+  return launch_dependent(route_tc_kernel<D>, dim3(grid), dim3(kThreads), Cf::kSmemBytes, st, mq,
+                          mc, p);
 }
 
 }  // namespace

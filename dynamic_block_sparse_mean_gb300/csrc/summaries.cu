@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kThreads) block_summaries_kernel(
     const T *__restrict__ K, const int32_t *__restrict__ cu, float *__restrict__ C, int T_tok,
     int Nq, int Hk, int d, int b) {
   extern __shared__ float red[];
+  grid_dep_wait();  // K may come from the previous launch
   const int j = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
   const int s0 = cu[i], n = cu[i + 1] - s0;
   const int lo = j * b;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kThreads) block_summaries_kernel(
   float *out = C + (((size_t)i * Hk + h) * Nq + j) * d;
   const T *base = K + ((size_t)h * T_tok + s0 + lo) * d;
   block_mean<T>(base, nrows, d, d, out, red);
+  grid_dep_launch();
 }
 
 // grid (max_pages_per_req, R, H_kv): one CTA per (logical page p, request, KV head).
@@ -128,9 +130,9 @@ cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C
   const dim3 grid(s.max_blocks, s.num_seqs, s.num_kv_heads);
   if (s.dtype == BSA_BF16) {
     const size_t sm = (size_t)(kThreads / (s.head_dim / 8)) * s.head_dim * sizeof(float);
-    block_summaries_kernel<uint16_t><<<grid, kThreads, sm, st>>>(
-        static_cast<const uint16_t *>(K), s.cu_seqlens, C, s.total_tokens, s.max_blocks,
-        s.num_kv_heads, s.head_dim, s.block);
+    return launch_dependent(block_summaries_kernel<uint16_t>, grid, dim3(kThreads), sm, st,
+                            static_cast<const uint16_t *>(K), s.cu_seqlens, C, s.total_tokens,
+                            s.max_blocks, s.num_kv_heads, s.head_dim, s.block);
   } else {
     const size_t sm = (size_t)(kThreads / (s.head_dim / 4)) * s.head_dim * sizeof(float);
     block_summaries_kernel<float><<<grid, kThreads, sm, st>>>(

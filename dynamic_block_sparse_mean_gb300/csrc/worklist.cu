@@ -21,6 +21,7 @@ constexpr int kScanThreads = 1024;
 __global__ void wl_rows_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ counts,
                                const int32_t *__restrict__ cu, int32_t *__restrict__ code,
                                int32_t *dev_status, int nrows, int Nq, int Hk, int b, int k_max) {
+  grid_dep_wait();  // J and counts may come from the previous launch
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
     const int r = row % Nq, i = row / (Nq * Hk);
@@ -57,6 +58,7 @@ __global__ void wl_rows_kernel(const int32_t *__restrict__ J, const int32_t *__r
     if (err) set_status(dev_status, err);
     code[row] = err ? -1 : c;
   }
+  grid_dep_launch();
 }
 
 BSA_DEV int bucket_of(int len) {  // capacity max(4, pow2 >= len): 256 -> 0, ..., 4 -> 6
@@ -68,86 +70,110 @@ BSA_DEV int bucket_of(int len) {  // capacity max(4, pow2 >= len): 256 -> 0, ...
   return s;
 }
 
+// Exclusive scan over the block of N values per thread at once (warp shuffles,
+// then a scan of the 32 warp totals): v becomes each thread's exclusive prefix,
+// tot the block totals.
+template <int N>
+BSA_DEV void block_scan_n(int (&v)[N], int (&tot)[N], int (*wsum)[N]) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int inc[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    inc[k] = v[k];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc[k], off);
+      if (lane >= off) inc[k] += y;
+    }
+  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < N; ++k) wsum[warp][k] = inc[k];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      int w = wsum[lane][k], x = w;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      wsum[lane][k] = x - w;  // exclusive prefix of this warp
+      if (lane == 31) wsum[32][k] = x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    v[k] = inc[k] - v[k] + wsum[warp][k];
+    tot[k] = wsum[32][k];
+  }
+}
+
+// One CTA: row_ptr by prefix sum of the row lengths, and the work list: a stable
+// counting sort of rows by capacity bucket, largest bucket first.  Thread t owns
+// a contiguous chunk of rows.
 __global__ void __launch_bounds__(kScanThreads) wl_scan_kernel(
     const int32_t *__restrict__ code, int32_t *__restrict__ row_ptr, int32_t *__restrict__ work,
     int32_t *__restrict__ bucket_off, int nrows) {
-  __shared__ int32_t hist[BSA_NUM_BUCKETS][kScanThreads];
-  __shared__ int32_t lsum[kScanThreads];
-  __shared__ int32_t btot[BSA_NUM_BUCKETS + 1];
+  grid_dep_wait();  // the row codes come from the previous launch
+  constexpr int NB = BSA_NUM_BUCKETS;
+  __shared__ int wsum[33][NB + 1];
   const int t = threadIdx.x;
   const int chunk = (nrows + kScanThreads - 1) / kScanThreads;
   const int lo = min(nrows, t * chunk), hi = min(nrows, lo + chunk);
-  int sum = 0;
-  int h[BSA_NUM_BUCKETS];
+  int v[NB + 1];  // v[0]: length sum; v[1 + s]: rows in bucket s
 #pragma unroll
-  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) h[s] = 0;
+  for (int k = 0; k <= NB; ++k) v[k] = 0;
   for (int row = lo; row < hi; ++row) {
     const int c = code[row];
     const int len = c < 0 ? 1 : c;
-    sum += len;
+    v[0] += len;
     if (len > 0) {
-      const int s = bucket_of(len);
+      const int sb = bucket_of(len);
 #pragma unroll
-      for (int q = 0; q < BSA_NUM_BUCKETS; ++q) h[q] += (q == s) ? 1 : 0;
+      for (int q = 0; q < NB; ++q) v[1 + q] += (q == sb) ? 1 : 0;
     }
   }
-  lsum[t] = sum;
+  int tot[NB + 1];
+  block_scan_n<NB + 1>(v, tot, wsum);
+  int bstart[NB];
+  int acc = 0;
 #pragma unroll
-  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) hist[s][t] = h[s];
-  __syncthreads();
-  // Exclusive scans: lengths over threads, and bucket counts over (bucket, thread).
+  for (int q = 0; q < NB; ++q) {
+    bstart[q] = acc;
+    acc += tot[1 + q];
+  }
   if (t == 0) {
-    int acc = 0;
-    for (int k = 0; k < kScanThreads; ++k) {
-      const int v = lsum[k];
-      lsum[k] = acc;
-      acc += v;
-    }
-    row_ptr[nrows] = acc;
-  }
-  if (t >= 32 && t < 32 + BSA_NUM_BUCKETS) {
-    const int s = t - 32;
-    int acc = 0;
-    for (int k = 0; k < kScanThreads; ++k) {
-      const int v = hist[s][k];
-      hist[s][k] = acc;
-      acc += v;
-    }
-    btot[s] = acc;
-  }
-  __syncthreads();
-  if (t == 0) {
-    int acc = 0;
-    for (int s = 0; s < BSA_NUM_BUCKETS; ++s) {
-      bucket_off[s] = acc;
-      const int v = btot[s];
-      btot[s] = acc;
-      acc += v;
-    }
-    bucket_off[BSA_NUM_BUCKETS] = acc;
-  }
-  __syncthreads();
-  int off = lsum[t];
-  int pos[BSA_NUM_BUCKETS];
+    row_ptr[nrows] = tot[0];
 #pragma unroll
-  for (int s = 0; s < BSA_NUM_BUCKETS; ++s) pos[s] = btot[s] + hist[s][t];
+    for (int q = 0; q < NB; ++q) bucket_off[q] = bstart[q];
+    bucket_off[NB] = acc;
+  }
+  int off = v[0];
+  int pos[NB];
+#pragma unroll
+  for (int q = 0; q < NB; ++q) pos[q] = bstart[q] + v[1 + q];
   for (int row = lo; row < hi; ++row) {
     const int c = code[row];
     const int len = c < 0 ? 1 : c;
     row_ptr[row] = off;
     off += len;
     if (len > 0) {
-      const int s = bucket_of(len);
+      const int sb = bucket_of(len);
 #pragma unroll
-      for (int q = 0; q < BSA_NUM_BUCKETS; ++q)
-        if (q == s) work[pos[q]++] = row;
+      for (int q = 0; q < NB; ++q)
+        if (q == sb) work[pos[q]++] = row;
     }
   }
+  grid_dep_launch();
 }
 
 __global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ code,
                                const int32_t *__restrict__ row_ptr, int32_t *__restrict__ col_idx,
                                int nrows, int Nq, int k_max) {
+  grid_dep_wait();  // codes and row_ptr come from the previous launches
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
     const int c = code[row];
@@ -160,6 +186,7 @@ __global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__r
     const int32_t *Jr = J + (size_t)row * k_max;
     for (int e = 0; e < c; ++e) out[e] = Jr[e];
   }
+  grid_dep_launch();
 }
 
 // Density 1 (every causal block): row r of a sequence with nb blocks holds 0..r.
@@ -225,16 +252,15 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
   const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
   int32_t *code = static_cast<int32_t *>(ws);
   const int blocks = min(4 * num_sms(), (nrows + 255) / 256);
-  wl_rows_kernel<<<max(blocks, 1), 256, 0, st>>>(J, counts, s.cu_seqlens, code, dev_status, nrows,
-                                                 s.max_blocks, s.num_kv_heads, s.block, k_max);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(wl_rows_kernel, dim3(max(blocks, 1)), dim3(256), 0, st, J,
+                                   counts, s.cu_seqlens, code, dev_status, nrows, s.max_blocks,
+                                   s.num_kv_heads, s.block, k_max);
   if (e != cudaSuccess) return e;
-  wl_scan_kernel<<<1, kScanThreads, 0, st>>>(code, row_ptr, work, bucket_off, nrows);
-  e = cudaGetLastError();
+  e = launch_dependent(wl_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, code, row_ptr, work,
+                       bucket_off, nrows);
   if (e != cudaSuccess) return e;
-  wl_fill_kernel<<<max(blocks, 1), 256, 0, st>>>(J, code, row_ptr, col_idx, nrows, s.max_blocks,
-                                                 k_max);
-  return cudaGetLastError();
+  return launch_dependent(wl_fill_kernel, dim3(max(blocks, 1)), dim3(256), 0, st, J, code,
+                          row_ptr, col_idx, nrows, s.max_blocks, k_max);
 }
 
 size_t causal_worklist_capacity(const bsa_shape_t &s) {
