@@ -57,6 +57,7 @@ import itertools
 import math
 
 import numpy as np
+import torch
 
 TOPK = 0
 THRESHOLD = 1
@@ -345,6 +346,51 @@ def attention(Q, K, V, cu_seqlens, b: int, G: int, J, counts, scale=None, rows=N
     if rows is None:
         rows = all_rows(cu_seqlens, b, Hk)
     return attention_rows(Q, K, V, cu_seqlens, b, G, J, counts, rows, scale, multiset)
+
+
+def attention_backward(Q, K, V, cu_seqlens, b: int, G: int, J, counts, dO, scale=None):
+    """Gradients dQ, dK, dV of the sparse attention for the upstream gradient dO
+    (float64), the backward of the same plain definition as `attention`: per
+    sequence and KV head the allowed-key mask {s : block(s) in J_r, s <= t} is
+    built explicitly, the masked softmax attention of every query head of the group
+    is formed, and torch autograd (a library primitive) differentiates
+    sum(O * dO).  dK and dV sum over the group's query heads (GQA).  Training needs
+    this backward ([P2] §2.2 training paragraph; [P3] verification: gradients of
+    the fixed-candidate kernel against the dense-then-mask reference)."""
+    H, T, d = Q.shape
+    Hk = K.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dQ = np.zeros((H, T, d))
+    dK = np.zeros((Hk, T, d))
+    dV = np.zeros((Hk, T, d))
+    for i, (s0, n, nb) in enumerate(seq_info(cu_seqlens, b)):
+        if n == 0:
+            continue
+        for h in range(Hk):
+            allowed = np.zeros((n, n), dtype=bool)
+            for r in range(nb):
+                cnt = int(counts[i, h, r])
+                sel = [int(x) for x in J[i, h, r, :cnt]] or [r]
+                keys = np.zeros(n, dtype=bool)
+                for j in set(sel):
+                    keys[j * b:min(n, (j + 1) * b)] = True
+                for t in range(r * b, min(n, (r + 1) * b)):
+                    allowed[t] = keys & (np.arange(n) <= t)
+            mask = torch.from_numpy(allowed)
+            k = torch.tensor(np.asarray(K[h, s0:s0 + n], dtype=np.float64), requires_grad=True)
+            v = torch.tensor(np.asarray(V[h, s0:s0 + n], dtype=np.float64), requires_grad=True)
+            for hq in range(h * G, (h + 1) * G):
+                q = torch.tensor(np.asarray(Q[hq, s0:s0 + n], dtype=np.float64), requires_grad=True)
+                sc = (q @ k.T) * scale
+                sc = sc.masked_fill(~mask, float("-inf"))
+                o = torch.softmax(sc, dim=-1) @ v
+                g = torch.from_numpy(np.asarray(dO[hq, s0:s0 + n], dtype=np.float64))
+                gq, gk, gv = torch.autograd.grad((o * g).sum(), (q, k, v))
+                dQ[hq, s0:s0 + n] = gq.numpy()
+                dK[h, s0:s0 + n] += gk.numpy()
+                dV[h, s0:s0 + n] += gv.numpy()
+    return dQ, dK, dV
 
 
 def causal_all_blocks(cu_seqlens, b: int, Hk: int):

@@ -273,6 +273,53 @@ def test_coverage_matches_library_logsumexp_and_limits():
     assert (Cb[ok] >= C[ok] - 1e-12).all()
 
 
+def test_backward_matches_central_differences():
+    # d/dx sum(O * dO) by central differences of the forward oracle, for random
+    # entries of Q, K and V (independent of autograd).
+    x, Q, K, V = _inputs([150, 70], 4, 2, 8, 32, seed=61)
+    G, b = 2, 32
+    Jo, co, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 2)
+    rng = np.random.default_rng(62)
+    dO = rng.normal(size=Q.shape)
+    dQ, dK, dV = oracle.attention_backward(Q, K, V, x.cu_seqlens, b, G, Jo, co, dO)
+
+    def loss(Q_, K_, V_):
+        O, _ = oracle.attention(Q_, K_, V_, x.cu_seqlens, b, G, Jo, co)
+        return float((O * dO).sum())
+
+    eps = 1e-6
+    for name, A, grad in (("q", Q, dQ), ("k", K, dK), ("v", V, dV)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(n)) for n in A.shape)
+            Ap, Am = A.copy(), A.copy()
+            Ap[idx] += eps
+            Am[idx] -= eps
+            args_p = {"q": (Ap, K, V), "k": (Q, Ap, V), "v": (Q, K, Ap)}[name]
+            args_m = {"q": (Am, K, V), "k": (Q, Am, V), "v": (Q, K, Am)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_backward_at_density_one_equals_sdpa_gradients():
+    x, Q, K, V = _inputs([200, 90], 4, 2, 16, 32, seed=63)
+    G, b = 2, 32
+    Ja, ca = oracle.causal_all_blocks(x.cu_seqlens, b, 2)
+    dO = np.random.default_rng(64).normal(size=Q.shape)
+    dQ, dK, dV = oracle.attention_backward(Q, K, V, x.cu_seqlens, b, G, Ja, ca, dO)
+    for i in range(len(x.cu_seqlens) - 1):
+        s0, s1 = int(x.cu_seqlens[i]), int(x.cu_seqlens[i + 1])
+        q = torch.tensor(Q[:, s0:s1], requires_grad=True)
+        k = torch.tensor(K[:, s0:s1], requires_grad=True)
+        v = torch.tensor(V[:, s0:s1], requires_grad=True)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[None], k.repeat_interleave(G, dim=0)[None], v.repeat_interleave(G, dim=0)[None],
+            is_causal=True)[0]
+        gq, gk, gv = torch.autograd.grad((o * torch.from_numpy(dO[:, s0:s1])).sum(), (q, k, v))
+        assert np.abs(gq.numpy() - dQ[:, s0:s1]).max() < 1e-11
+        assert np.abs(gk.numpy() - dK[:, s0:s1]).max() < 1e-11
+        assert np.abs(gv.numpy() - dV[:, s0:s1]).max() < 1e-11
+
+
 # ---------------------------------------------------------------- summaries
 
 
