@@ -28,9 +28,8 @@ ROUTE_THRESHOLD = 1
 
 __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "PrefillPlan",
            "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
-           "attention_fwd", "causal_worklist", "coverage", "page_summaries", "page_summaries_append",
-           "decode_paged",
-           "check_status", "library_path"]
+           "attention_fwd", "attention_bwd", "causal_worklist", "coverage", "page_summaries",
+           "page_summaries_append", "decode_paged", "check_status", "library_path"]
 
 
 def library_path() -> str:
@@ -204,6 +203,24 @@ def attention_fwd(q, k, v, wl: Worklist, shape: PrefillShape, dev_status, scale:
         ctypes.byref(s), _p(q), _p(k), _p(v), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work),
         _p(wl.bucket_off), float(scale), _p(out), _p(lse), _p(dev_status), _stream()))
     return out, lse
+
+
+def attention_bwd(q, k, v, o, do, lse, wl: Worklist, shape: PrefillShape, scale: float = 0.0,
+                  dq=None, dk=None, dv=None, ws=None):
+    """dQ, dK, dV of the sparse attention for the upstream gradient do, reusing the
+    forward's worklist and lse (bsa_attention_bwd)."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    s = shape.c()
+    if ws is None:
+        n = int(_lib.lib().bsa_attention_bwd_workspace_size(ctypes.byref(s)))
+        ws = torch.empty(max(256, n), dtype=torch.uint8, device=q.device)
+    check("bsa_attention_bwd", _lib.lib().bsa_attention_bwd(
+        ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(wl.row_ptr),
+        _p(wl.col_idx), _p(wl.work), _p(wl.bucket_off), float(scale), _p(dq), _p(dk), _p(dv),
+        _p(ws), ws.numel(), _stream()))
+    return dq, dk, dv
 
 
 def causal_worklist(shape: PrefillShape, device, wl: Worklist | None = None, ws=None) -> Worklist:

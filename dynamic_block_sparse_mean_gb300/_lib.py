@@ -63,6 +63,9 @@ PROTOTYPES = {
     "bsa_build_worklist": (I32, [ctypes.POINTER(Shape), I32, V, V, V, V, V, V, V, V, SZ, V]),
     "bsa_build_worklist_noalloc": (I32, [ctypes.POINTER(Shape), I32, V, V, V, V, V, V, V, V]),
     "bsa_attention_fwd": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, V, V, F32, V, V, V, V]),
+    "bsa_attention_bwd_workspace_size": (SZ, [ctypes.POINTER(Shape)]),
+    "bsa_attention_bwd": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, V, V, V, V, V, F32, V, V, V,
+                                V, SZ, V]),
     "bsa_causal_worklist_capacity": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),

@@ -160,6 +160,30 @@ bsa_status_t bsa_build_worklist_noalloc(const bsa_shape_t *shape, int32_t k_max,
                                        bucket_off, dev_status, scratch, stream));
 }
 
+size_t bsa_attention_bwd_workspace_size(const bsa_shape_t *shape) {
+  if (!shape_ok(shape)) return 0;
+  return bsa::attention_bwd_workspace_bytes(*shape);
+}
+
+bsa_status_t bsa_attention_bwd(const bsa_shape_t *shape, const void *Q, const void *K,
+                               const void *V, const void *O, const void *dO, const float *lse,
+                               const int32_t *row_ptr, const int32_t *col_idx,
+                               const int32_t *work, const int32_t *bucket_off,
+                               float softmax_scale, void *dQ, void *dK, void *dV, void *ws,
+                               size_t ws_bytes, cudaStream_t stream) {
+  if (!shape_ok(shape) || Q == nullptr || K == nullptr || V == nullptr || O == nullptr ||
+      dO == nullptr || lse == nullptr || row_ptr == nullptr || col_idx == nullptr ||
+      work == nullptr || bucket_off == nullptr || dQ == nullptr || dK == nullptr ||
+      dV == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < bsa::attention_bwd_workspace_bytes(*shape))
+    return BSA_ERR_WORKSPACE;
+  const float scale =
+      softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)shape->head_dim);
+  return launched(bsa::launch_attention_bwd(*shape, Q, K, V, O, dO, lse, row_ptr, col_idx, work,
+                                            bucket_off, scale, dQ, dK, dV, ws, stream));
+}
+
 size_t bsa_causal_worklist_capacity(const bsa_shape_t *shape) {
   if (!shape_ok(shape)) return 0;
   return bsa::causal_worklist_capacity(*shape);

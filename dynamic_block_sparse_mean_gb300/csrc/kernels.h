@@ -67,6 +67,14 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
                             cudaStream_t st);
+// Backward of the sparse attention (attn_bwd.cu).
+size_t attention_bwd_workspace_bytes(const bsa_shape_t &s);
+cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void *K,
+                                 const void *V, const void *O, const void *dO, const float *lse,
+                                 const int32_t *row_ptr, const int32_t *col_idx,
+                                 const int32_t *work, const int32_t *bucket_off, float scale,
+                                 void *dQ, void *dK, void *dV, void *ws, cudaStream_t st);
+
 // Density-1 worklist (every causal block) and coverage of eq.(10) (worklist.cu).
 size_t causal_worklist_capacity(const bsa_shape_t &s);
 cudaError_t launch_causal_worklist(const bsa_shape_t &s, int32_t *row_ptr, int32_t *col_idx,

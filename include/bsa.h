@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 3
+#define BSA_VERSION 4
 
 typedef enum {
   BSA_OK = 0,
@@ -286,6 +286,28 @@ bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
                               float *lse, int32_t *sel, int32_t *sel_counts,
                               int32_t *dev_status, void *ws, size_t ws_bytes,
                               cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward of the sparse attention, for training ([P2] §2.2 training paragraph:
+ *   keep the index and the softmax statistics; [P3] verification of forward output
+ *   and gradients against the dense-then-mask reference).  Given the forward's
+ *   worklist (same J), its output O and lse, and the upstream gradient dO, returns
+ *   dQ, dK, dV of the forward of bsa_attention_fwd (same masks, same scale: <= 0
+ *   means 1/sqrt(d)).  P is recomputed from lse; nothing is re-routed.  dK and dV
+ *   sum the contributions of every query row and query head that selected a key
+ *   block (GQA).  FP32 arithmetic on the SIMT pipes (a correctness-first path).
+ *   Q, dQ, O, dO : [H, T, d];  K, V, dK, dV : [H_kv, T, d];  element type shape->dtype.
+ *   lse          : [H, T] fp32 from the forward.
+ *   ws           : at least bsa_attention_bwd_workspace_size() bytes, 256-aligned;
+ *                  contents are overwritten (fp32 dK / dV accumulators).
+ * ------------------------------------------------------------------------- */
+size_t bsa_attention_bwd_workspace_size(const bsa_shape_t *shape);
+bsa_status_t bsa_attention_bwd(const bsa_shape_t *shape, const void *Q, const void *K,
+                               const void *V, const void *O, const void *dO, const float *lse,
+                               const int32_t *row_ptr, const int32_t *col_idx,
+                               const int32_t *work, const int32_t *bucket_off,
+                               float softmax_scale, void *dQ, void *dK, void *dV, void *ws,
+                               size_t ws_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Density-1 worklist — every causal block: row r of a sequence holds blocks
