@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-quality", action="store_true",
                     help="skip the coverage / planted-recall / density-1 leg")
     ap.add_argument("--decode-only", action="store_true",
@@ -300,6 +301,43 @@ def router_quality(res, w, device):
     return out
 
 
+def bench_backward(res, w, device, reps=3):
+    """Outside the timed loop: the backward (bsa_attention_bwd) on the forward's
+    worklist and lse with a seeded upstream gradient; FLOPs are 2.5x the forward's
+    tile count (recomputed QK^T, dP = dO V^T, dV, dQ, dK: five b x b x d products
+    per tile against the forward's two)."""
+    import dynamic_block_sparse_mean_gb300 as bsa
+    plan, q, k, v = res["plan"], res["q"], res["k"], res["v"]
+    plan.attend(q, k, v)
+    g = torch.Generator(device="cpu").manual_seed(1007)
+    do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(device=device, dtype=q.dtype)
+    s = plan.shape.c()
+    import ctypes
+    from dynamic_block_sparse_mean_gb300 import _lib
+    n = int(_lib.lib().bsa_attention_bwd_workspace_size(ctypes.byref(s)))
+    ws = torch.empty(max(256, n), dtype=torch.uint8, device=device)
+    dq, dk, dv = bsa.attention_bwd(q, k, v, plan.out, do, plan.lse, plan.wl, plan.shape, ws=ws)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        bsa.attention_bwd(q, k, v, plan.out, do, plan.lse, plan.wl, plan.shape, dq=dq, dk=dk,
+                          dv=dv, ws=ws)
+    t1.record()
+    torch.cuda.synchronize(device)
+    bsa.check_status(plan.status)
+    ms = t0.elapsed_time(t1) / reps
+    flops = 2.5 * res["flops"]
+    tf = flops / (ms * 1e-3) / 1e12
+    # FP32 FFMA peak: 152 SMs x 128 lanes x 2 FLOP x the maximum SM clock
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peak = sms * 128 * 2 * 2.07e9 / 1e12
+    del dq, dk, dv, ws, do
+    return {"ms": ms, "tflops": tf, "flops_per_call": flops,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak,
+                         "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x 2070 MHz"}}
+
+
 def bench_e2e(res, steps, device):
     """Same metric through PrefillPlan.run with host (pinned) buffers: every step
     copies Q, K, V host -> device and reads O back device -> host."""
@@ -499,6 +537,7 @@ def run_native(args):
                 "algorithmic_flops_per_launch": res["flops"],
                 "compulsory_bytes_per_launch": res["attn_bytes"]}
     quality = router_quality(res, w, device) if not args.no_quality else None
+    backward = bench_backward(res, w, device) if not args.no_backward else None
     e2e = None
     if not args.no_e2e:
         e_ms, bi, bo = bench_e2e(res, max(3, min(args.steps, 20)), device)
@@ -540,6 +579,7 @@ def run_native(args):
         "e2e": e2e,
         "decode": dec,
         "router_quality": quality,
+        "backward": backward,
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
