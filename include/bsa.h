@@ -71,8 +71,10 @@ enum { BSA_ROUTE_TOPK = 0, BSA_ROUTE_THRESHOLD = 1 };
 /* Shape of a packed prefill batch ([P2] section 1, problem statement). */
 typedef struct {
   int32_t num_seqs;          /* B                                              */
-  int32_t total_tokens;      /* T = cu_seqlens[B]                              */
-  int32_t max_seqlen;        /* max_i n_i                                      */
+  int32_t total_tokens;      /* T = cu_seqlens[B] >= 1 (a batch without tokens
+                                is rejected: BSA_ERR_INVALID_ARG); single
+                                sequences may be empty (n_i = 0)             */
+  int32_t max_seqlen;        /* max_i n_i >= 1                                 */
   int32_t num_heads;         /* H query heads                                  */
   int32_t num_kv_heads;      /* H_kv; H % H_kv == 0, G = H / H_kv (GQA)        */
   int32_t head_dim;          /* d_h: 64 or 128                                 */

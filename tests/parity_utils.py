@@ -99,6 +99,45 @@ def check_route_rows(J_gpu, cnt_gpu, J_ora, cnt_ora, g_ora, rows, mode, force_si
     return differing
 
 
+def worklist_from_oracle(Jo, co, sh, k_max, status):
+    """Build the GPU worklist from the oracle's J and counts (int64 -> int32,
+    -1 padded to k_max)."""
+    J = torch.as_tensor(Jo.astype(np.int32), device="cuda").contiguous()
+    cnt = torch.as_tensor(co.astype(np.int32), device="cuda").contiguous()
+    if J.shape[-1] < k_max:
+        J = torch.nn.functional.pad(J, (0, k_max - J.shape[-1]), value=-1)
+    return bsa.build_worklist(J, cnt, sh, k_max, status)
+
+
+def expected_csr(Jo, co, cu, b):
+    """The CSR row_ptr / col_idx the worklist must hold for the oracle's index:
+    rows past a sequence's end are empty, an empty row inside falls back to {r}."""
+    B, Hk, Nq = co.shape
+    info = oracle.seq_info(cu, b)
+    rp, ci = [0], []
+    for i in range(B):
+        for h in range(Hk):
+            for r in range(Nq):
+                if r < info[i][2]:
+                    ids = [int(v) for v in Jo[i, h, r, :co[i, h, r]]] or [r]
+                    ci += ids
+                rp.append(len(ci))
+    return np.array(rp), np.array(ci)
+
+
+def check_buckets(wl, rp):
+    """Every non-empty row appears once in `work`, in the bucket of its capacity
+    max(4, next power of two of its length), row-id order inside a bucket."""
+    bo = wl.bucket_off.cpu().numpy()
+    work = wl.work.cpu().numpy()[:bo[-1]]
+    lens = np.diff(rp)
+    assert sorted(work.tolist()) == sorted(np.nonzero(lens)[0].tolist())
+    for s in range(7):
+        seg = work[bo[s]:bo[s + 1]]
+        assert all(max(4, 1 << int(np.ceil(np.log2(max(1, lens[w]))))) == 256 >> s for w in seg)
+        assert list(seg) == sorted(seg)
+
+
 def rows_token_mask(cu, b, G, rows, H, T):
     """Boolean [H, T] of the query tokens covered by the given rows."""
     m = np.zeros((H, T), dtype=bool)
@@ -114,6 +153,35 @@ def attention_errors(O_gpu, lse_gpu, O_ora, lse_ora, mask):
     dl = np.abs(lse_gpu[mask] - lse_ora[mask])
     return float(d.max()), float(d.mean()), float(dl.max()), float(np.abs(O_ora[mask]).max()), \
         float(np.abs(lse_ora[mask]).max())
+
+
+def check_decode(x, top_k, o, lse, sel, cnt, reqs, G):
+    """Decode parity for the requests `reqs`: the kept page set (tie-aware, last
+    page always kept), then O and lse within the BF16 tolerances."""
+    q64 = synth.bf16_bits_to_f32(x.q).astype(np.float64)
+    oo, lo, so, co, sc = oracle.decode(q64, BF16View(x.k_cache), BF16View(x.v_cache),
+                                       x.block_table, x.context_lens, x.page_size, top_k,
+                                       reqs=reqs, return_scores=True)
+    Hk = x.k_cache.shape[1]
+    for rho in reqs:
+        for h in range(Hk):
+            n = int(x.context_lens[rho])
+            L = (n + 63) // 64
+            cg = int(cnt[rho, h])
+            assert cg == int(co[rho, h]) == min(top_k, L - 1) + 1
+            sg = [int(v) for v in sel[rho, h, :cg]]
+            assert sg == sorted(set(sg)) and sg[-1] == L - 1
+            assert all(int(v) == -1 for v in sel[rho, h, cg:])
+            dg, do = set(sg[:-1]), set(int(v) for v in so[rho, h, :cg - 1])
+            g = sc[(rho, h)]
+            if dg != do:
+                s_k = min(g[j] for j in do)
+                for j in dg ^ do:
+                    assert abs(g[j] - s_k) <= TIE_BAND
+    rows = np.array(list(reqs))
+    d = np.abs(o[rows].astype(np.float64) - oo[rows])
+    assert d.max() <= BF16_MAX_ABS and d.mean() <= BF16_MEAN_ABS, (d.max(), d.mean())
+    assert np.abs(lse[rows] - lo[rows]).max() <= BF16_LSE_ABS
 
 
 class BF16View:

@@ -63,6 +63,9 @@ def test_host_side_argument_errors(lib):
                                    ctypes.c_void_p(16), null) == 2
     assert lib.bsa_block_summaries(ctypes.byref(_shape(num_heads=3)), ctypes.c_void_p(16),
                                    ctypes.c_void_p(16), null) == 1
+    empty = _shape(total_tokens=0, max_seqlen=0, max_blocks=0)       # a batch without tokens
+    assert lib.bsa_block_summaries(ctypes.byref(empty), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                   null) == 1
     p = _lib.RouteParams(0, 300, 0, 0.0, 0)
     args = [ctypes.c_void_p(16)] * 4
     assert lib.bsa_route(ctypes.byref(s), ctypes.byref(p), *args, null, null, null, 0, null) == 2

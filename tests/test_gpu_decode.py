@@ -6,7 +6,7 @@ import torch
 import dynamic_block_sparse_mean_gb300 as bsa
 import oracle
 from dynamic_block_sparse_mean_gb300 import synth
-from parity_utils import BF16_LSE_ABS, BF16_MAX_ABS, BF16_MEAN_ABS, TIE_BAND, BF16View, dev_tensor
+from parity_utils import BF16View, check_decode, dev_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -15,33 +15,6 @@ def _upload(x):
     return (dev_tensor(x.q, "bf16"), dev_tensor(x.k_cache, "bf16"), dev_tensor(x.v_cache, "bf16"),
             torch.as_tensor(x.block_table, device="cuda"),
             torch.as_tensor(x.context_lens, device="cuda"))
-
-
-def check_decode(x, top_k, o, lse, sel, cnt, reqs, G):
-    q64 = synth.bf16_bits_to_f32(x.q).astype(np.float64)
-    oo, lo, so, co, sc = oracle.decode(q64, BF16View(x.k_cache), BF16View(x.v_cache),
-                                       x.block_table, x.context_lens, x.page_size, top_k,
-                                       reqs=reqs, return_scores=True)
-    Hk = x.k_cache.shape[1]
-    for rho in reqs:
-        for h in range(Hk):
-            n = int(x.context_lens[rho])
-            L = (n + 63) // 64
-            cg = int(cnt[rho, h])
-            assert cg == int(co[rho, h]) == min(top_k, L - 1) + 1
-            sg = [int(v) for v in sel[rho, h, :cg]]
-            assert sg == sorted(set(sg)) and sg[-1] == L - 1
-            assert all(int(v) == -1 for v in sel[rho, h, cg:])
-            dg, do = set(sg[:-1]), set(int(v) for v in so[rho, h, :cg - 1])
-            g = sc[(rho, h)]
-            if dg != do:
-                s_k = min(g[j] for j in do)
-                for j in dg ^ do:
-                    assert abs(g[j] - s_k) <= TIE_BAND
-    rows = np.array(list(reqs))
-    d = np.abs(o[rows].astype(np.float64) - oo[rows])
-    assert d.max() <= BF16_MAX_ABS and d.mean() <= BF16_MEAN_ABS, (d.max(), d.mean())
-    assert np.abs(lse[rows] - lo[rows]).max() <= BF16_LSE_ABS
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])

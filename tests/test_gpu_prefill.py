@@ -8,7 +8,8 @@ import dynamic_block_sparse_mean_gb300 as bsa
 import oracle
 from dynamic_block_sparse_mean_gb300 import synth
 from parity_utils import (BF16_LSE_ABS, BF16_MAX_ABS, BF16_MEAN_ABS, FP32_REL, TIE_BAND,
-                          attention_errors, check_route_rows, oracle_view, shape_of, upload)
+                          attention_errors, check_buckets, check_route_rows, expected_csr,
+                          oracle_view, shape_of, upload, worklist_from_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,28 +66,6 @@ def test_router_matches_oracle_tie_aware(case):
         assert (cn[i, :, nb:] == 0).all()
 
 
-def _worklist_from(Jo, co, sh, k_max, status):
-    J = torch.as_tensor(Jo.astype(np.int32), device="cuda").contiguous()
-    cnt = torch.as_tensor(co.astype(np.int32), device="cuda").contiguous()
-    if J.shape[-1] < k_max:
-        J = torch.nn.functional.pad(J, (0, k_max - J.shape[-1]), value=-1)
-    return bsa.build_worklist(J, cnt, sh, k_max, status)
-
-
-def _expected_csr(Jo, co, cu, b):
-    B, Hk, Nq = co.shape
-    info = oracle.seq_info(cu, b)
-    rp, ci = [0], []
-    for i in range(B):
-        for h in range(Hk):
-            for r in range(Nq):
-                if r < info[i][2]:
-                    ids = [int(v) for v in Jo[i, h, r, :co[i, h, r]]] or [r]
-                    ci += ids
-                rp.append(len(ci))
-    return np.array(rp), np.array(ci)
-
-
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_worklist_csr_and_buckets(case):
     x, q, k, v, sh, params = _run_case(case)
@@ -97,21 +76,12 @@ def test_worklist_csr_and_buckets(case):
     co = co.copy()
     co[0, 0, min(2, co.shape[2] - 1)] = 0       # one empty row: falls back to {r}
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    wl = worklist_from_oracle(Jo, co, sh, params.k_max, status)
     bsa.check_status(status)
-    rp, ci = _expected_csr(Jo, co, x.cu_seqlens, x.block)
+    rp, ci = expected_csr(Jo, co, x.cu_seqlens, x.block)
     assert np.array_equal(wl.row_ptr.cpu().numpy(), rp)
     assert np.array_equal(wl.col_idx.cpu().numpy()[:len(ci)], ci)
-    bo = wl.bucket_off.cpu().numpy()
-    nrows = bo[-1]
-    work = wl.work.cpu().numpy()[:nrows]
-    lens = np.diff(rp)
-    assert sorted(work.tolist()) == sorted(np.nonzero(lens)[0].tolist())
-    caps = [256 >> s for s in range(7)]
-    for s in range(7):
-        seg = work[bo[s]:bo[s + 1]]
-        assert all(max(4, 1 << int(np.ceil(np.log2(max(1, lens[w]))))) == caps[s] for w in seg)
-        assert list(seg) == sorted(seg)
+    check_buckets(wl, rp)
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
@@ -123,7 +93,7 @@ def test_attention_bf16_on_oracle_index(case):
                                 G, params.mode, params.k_max, params.k_min, params.tau_delta,
                                 params.force_sink)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    wl = worklist_from_oracle(Jo, co, sh, params.k_max, status)
     O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
     torch.cuda.synchronize()
     bsa.check_status(status)
@@ -146,7 +116,7 @@ def test_attention_fp32_path(case):
     Jo, co, _, _ = oracle.route(Qo, Ko, x.cu_seqlens, x.block, G, params.mode, params.k_max,
                                 params.k_min, params.tau_delta, params.force_sink)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wl = _worklist_from(Jo, co, sh, params.k_max, status)
+    wl = worklist_from_oracle(Jo, co, sh, params.k_max, status)
     O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
     torch.cuda.synchronize()
     bsa.check_status(status)
@@ -171,7 +141,7 @@ def test_all_causal_blocks_equal_dense_attention():
     sh = shape_of(x, 8, 2)
     Jo, co = oracle.causal_all_blocks(x.cu_seqlens, 64, 2)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wl = _worklist_from(Jo, co, sh, Jo.shape[-1], status)
+    wl = worklist_from_oracle(Jo, co, sh, Jo.shape[-1], status)
     O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
     Oo, lo = oracle.attention(oracle_view(x, "q"), oracle_view(x, "k"), oracle_view(x, "v"),
                               x.cu_seqlens, 64, 4, Jo, co)
@@ -189,7 +159,7 @@ def test_shuffled_tile_order_stays_within_tolerance():
     Jo, co, _, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, 64, 4,
                                 oracle.TOPK, 8)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wl = _worklist_from(Jo, co, sh, 8, status)
+    wl = worklist_from_oracle(Jo, co, sh, 8, status)
     rp = wl.row_ptr.cpu().numpy()
     ci = wl.col_idx.cpu().numpy().copy()
     rng = np.random.default_rng(0)
