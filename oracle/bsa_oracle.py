@@ -43,6 +43,9 @@ Readings where the pages leave a step open (each repeated at its function):
        logsumexp over the allowed keys.
   R-11 decode: pages are the routing blocks; the last logical page is always
        kept and never scored; complete pages 0 .. L-2 are scored.
+  R-16 chunked prefill: a chunk starts on the page grid (the cached prefix is a
+       whole number of pages = routing blocks), so its query blocks are logical
+       blocks prefix / b + q and the result is the single-pass prefill's.
 
 Pins (tests/test_oracle_*.py): dense causal attention through
 torch.nn.functional.scaled_dot_product_attention when every causal block is
@@ -562,6 +565,65 @@ def decode(q, k_cache, v_cache, block_table, context_lens, page: int, top_k: int
     if return_scores:
         return o, lse, sel, cnt, scores
     return o, lse, sel, cnt
+
+
+# ----------------------------------------------------------------------------
+# chunked prefill over a paged cache
+# ----------------------------------------------------------------------------
+
+def chunked_prefill(q_chunk, k_cache, v_cache, block_table, prefix_lens, chunk_cu, b: int,
+                    G: int, mode: int, k_max: int, k_min: int = 0, tau_delta: float = 0.0,
+                    force_sink: bool = False, window: int = 1, global_blocks=(), scale=None):
+    """One chunk of a chunked prefill whose keys and values already sit in the
+    paged cache ([P2] §3.1: block summaries are cache state kept beside the KV
+    cache; the router's logical block ids are mapped to physical pages by the
+    block table; [P2] §2.2: a query block's routing needs only the summaries of
+    its history).
+
+    Sequence i has prefix_lens[i] tokens cached before the chunk and adds the
+    chunk_cu[i+1] - chunk_cu[i] tokens of q_chunk; its context of prefix + n keys
+    and values is read out of the pages block_table[i][0..] (page size b, R-16:
+    the prefix is a multiple of b, so chunk query block q is the logical block
+    r = prefix / b + q).  Everything else is the single-pass definition applied
+    to that context: block-mean summaries, scores, selection (`route`) and the
+    masked attention (`attention`), for the chunk's query blocks only.
+    Returns J [B, H_kv, N_q, k_max] (logical ids, -1 padded), counts [B, H_kv, N_q],
+    O [H, T_chunk, d] and lse [H, T_chunk]; N_q = ceil(max chunk length / b).
+    """
+    q_chunk = np.asarray(q_chunk, dtype=np.float64)
+    H, Tc, d = q_chunk.shape
+    Hk = k_cache.shape[1]
+    cu = np.asarray(chunk_cu, dtype=np.int64)
+    B = len(cu) - 1
+    lens = np.diff(cu)
+    Nq = int(((lens + b - 1) // b).max()) if B else 0
+    J = np.full((B, Hk, Nq, k_max), -1, dtype=np.int64)
+    counts = np.zeros((B, Hk, Nq), dtype=np.int64)
+    O = np.full((H, Tc, d), np.nan)
+    lse = np.full((H, Tc), np.nan)
+    for i in range(B):
+        pre, n, s0 = int(prefix_lens[i]), int(lens[i]), int(cu[i])
+        if n == 0:
+            continue  # an idle sequence: its prefix may end anywhere
+        assert pre % b == 0, "R-16: a chunk starts on the page grid"
+        ctx = pre + n
+        L = (ctx + b - 1) // b
+        phys = np.asarray(block_table[i, :L], dtype=np.int64)
+        Kc = np.stack([_f64(k_cache[phys, h]).reshape(L * b, d)[:ctx] for h in range(Hk)])
+        Vc = np.stack([_f64(v_cache[phys, h]).reshape(L * b, d)[:ctx] for h in range(Hk)])
+        Qc = np.zeros((H, ctx, d))
+        Qc[:, pre:] = q_chunk[:, s0:s0 + n]
+        one = np.array([0, ctx])
+        rows = [(0, h, r) for h in range(Hk) for r in range(pre // b, L)]
+        Jc, cc, _, _ = route(Qc, Kc, one, b, G, mode, k_max, k_min, tau_delta, force_sink,
+                             rows=rows, window=window, global_blocks=global_blocks)
+        Oc, lc = attention(Qc, Kc, Vc, one, b, G, Jc, cc, scale=scale, rows=rows)
+        nq = L - pre // b
+        J[i, :, :nq] = Jc[0, :, pre // b:L]
+        counts[i, :, :nq] = cc[0, :, pre // b:L]
+        O[:, s0:s0 + n] = Oc[:, pre:]
+        lse[:, s0:s0 + n] = lc[:, pre:]
+    return J, counts, O, lse
 
 
 # ----------------------------------------------------------------------------

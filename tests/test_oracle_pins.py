@@ -471,3 +471,59 @@ def test_decode_scores_mean_summaries_and_always_keeps_last_page():
     w = np.exp(s - s.max()) / np.exp(s - s.max()).sum()
     ref = w @ vc.reshape(8, 2)[[2, 3, 6]]
     assert np.abs(o[0, 0] - ref).max() < 1e-12
+
+
+def _paged_from_prompt(K, V, cu, b, seed, garbage=np.nan):
+    """Pages of b tokens holding every sequence's whole prompt, placed by a random
+    permutation; slots past a sequence's end hold `garbage`."""
+    Hk, _, d = K.shape
+    lens = np.diff(cu)
+    pages = (lens + b - 1) // b
+    perm = np.random.default_rng(seed).permutation(int(pages.sum()))
+    kc = np.full((len(perm), Hk, b, d), garbage)
+    vc = np.full((len(perm), Hk, b, d), garbage)
+    bt = np.full((len(lens), int(pages.max())), -1, dtype=np.int64)
+    off = 0
+    for i, (n, L) in enumerate(zip(lens, pages)):
+        bt[i, :L] = perm[off:off + L]
+        off += L
+        for p in range(L):
+            lo, hi = int(cu[i]) + p * b, int(cu[i]) + min(int(n), (p + 1) * b)
+            kc[bt[i, p], :, :hi - lo] = K[:, lo:hi]
+            vc[bt[i, p], :, :hi - lo] = V[:, lo:hi]
+    return kc, vc, bt
+
+
+def test_chunked_prefill_equals_single_pass():
+    """R-16 with [P2] §3.1: a prompt processed chunk by chunk through a paged cache
+    (pages in random physical order, the whole prompt already written, unwritten
+    page slots NaN) gives for every chunk the single-pass router rows and outputs:
+    later keys and unwritten slots never enter, and chunk block q is logical block
+    prefix / b + q.  The second sequence finishes early (an empty chunk)."""
+    b, H, Hk, d = 64, 4, 2, 32
+    G = H // Hk
+    x = synth.gen_prefill([700, 300], H, Hk, d, b, 31, "iid", "fp32")
+    Q, K, V = (getattr(x, n).astype(np.float64) for n in "qkv")
+    cu = x.cu_seqlens
+    Jo, co, _, _ = oracle.route(Q, K, cu, b, G, oracle.TOPK, 4, force_sink=True)
+    Oo, lo = oracle.attention(Q, K, V, cu, b, G, Jo, co)
+    kc, vc, bt = _paged_from_prompt(K, V, cu, b, 5)
+    bounds = [[0, 256, 640, 700], [0, 64, 300, 300]]
+    for step in range(3):
+        pre = [bd[step] for bd in bounds]
+        lens = [bd[step + 1] - bd[step] for bd in bounds]
+        ccu = np.concatenate([[0], np.cumsum(lens)])
+        qc = np.concatenate([Q[:, cu[i] + pre[i]: cu[i] + pre[i] + lens[i]] for i in range(2)],
+                            axis=1)
+        Jc, cc, Oc, lc = oracle.chunked_prefill(qc, kc, vc, bt, pre, ccu, b, G, oracle.TOPK, 4,
+                                                force_sink=True)
+        for i in range(2):
+            nq = (lens[i] + b - 1) // b
+            r0 = pre[i] // b
+            assert np.array_equal(cc[i, :, :nq], co[i, :, r0:r0 + nq])
+            assert np.array_equal(Jc[i, :, :nq], Jo[i, :, r0:r0 + nq])
+            assert (cc[i, :, nq:] == 0).all()
+            sl = slice(cu[i] + pre[i], cu[i] + pre[i] + lens[i])
+            got = slice(ccu[i], ccu[i + 1])
+            assert np.allclose(Oc[:, got], Oo[:, sl], rtol=0, atol=1e-12)
+            assert np.allclose(lc[:, got], lo[:, sl], rtol=0, atol=1e-12)
