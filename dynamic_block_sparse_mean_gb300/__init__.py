@@ -29,7 +29,9 @@ ROUTE_THRESHOLD = 1
 __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "PrefillPlan",
            "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
            "attention_fwd", "attention_bwd", "causal_worklist", "coverage", "page_summaries",
-           "page_summaries_append", "decode_paged", "check_status", "library_path"]
+           "page_summaries_append", "decode_paged", "check_status", "library_path",
+           "PagedKVCache", "Chunk", "ChunkPlan", "chunk_append", "route_chunk",
+           "build_worklist_chunk", "attention_chunk"]
 
 
 def library_path() -> str:
@@ -323,6 +325,175 @@ class PrefillPlan:
             self._dense_wl = causal_worklist(self.shape, q.device)
         Od, ld = attention_fwd(q, k, v, self._dense_wl, self.shape, self.status, scale)
         return coverage(self.lse, ld, self.shape), Od, ld
+
+
+# ---------------------------------------------------------------- chunked prefill
+
+
+@dataclass
+class PagedKVCache:
+    """Paged KV cache with its page summaries (bsa_kv_cache_t): k_cache, v_cache
+    [P, H_kv, 64, d] bf16; page_summ [P, H_kv, d] fp32 page means and, optionally,
+    page_sum the running sums that streaming decode appends continue from;
+    block_table [B, max_pages] int32 physical page of each logical block."""
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    page_summ: torch.Tensor
+    block_table: torch.Tensor
+    page_sum: torch.Tensor | None = None
+
+    PAGE = 64
+
+    @staticmethod
+    def allocate(num_phys_pages: int, num_kv_heads: int, head_dim: int, block_table,
+                 device="cuda", with_sums: bool = True) -> "PagedKVCache":
+        P, Hk, d = num_phys_pages, num_kv_heads, head_dim
+        z = lambda *sh, dt: torch.zeros(*sh, dtype=dt, device=device)  # noqa: E731
+        return PagedKVCache(z(P, Hk, 64, d, dt=torch.bfloat16), z(P, Hk, 64, d, dt=torch.bfloat16),
+                            z(P, Hk, d, dt=torch.float32),
+                            torch.as_tensor(block_table, dtype=torch.int32, device=device),
+                            z(P, Hk, d, dt=torch.float32) if with_sums else None)
+
+    def c(self, chunk: "Chunk") -> _lib.KVCache:
+        return _lib.KVCache(self.k_cache.data_ptr(), self.v_cache.data_ptr(),
+                            self.page_summ.data_ptr(),
+                            None if self.page_sum is None else self.page_sum.data_ptr(),
+                            self.block_table.data_ptr(), chunk.prefix_lens.data_ptr(),
+                            self.block_table.shape[1], self.k_cache.shape[0],
+                            chunk.max_context_blocks)
+
+
+@dataclass
+class Chunk:
+    """One chunk of a chunked prefill: `shape` packs the tokens each sequence adds
+    (block 64, bf16), `prefix_lens` [B] int32 the tokens already cached (multiples
+    of 64), max_context_blocks >= every ceil((prefix + n) / 64)."""
+    shape: PrefillShape
+    prefix_lens: torch.Tensor
+    max_context_blocks: int
+
+    @staticmethod
+    def make(prefix_lens_host, chunk_lens_host, num_heads: int, num_kv_heads: int,
+             head_dim: int, device="cuda", max_context_blocks: int | None = None) -> "Chunk":
+        pre = np.asarray(prefix_lens_host, dtype=np.int64)
+        lens = np.asarray(chunk_lens_host, dtype=np.int64)
+        cu = np.zeros(len(lens) + 1, dtype=np.int64)
+        cu[1:] = np.cumsum(lens)
+        shape = PrefillShape.make(cu, num_heads, num_kv_heads, head_dim, 64, torch.bfloat16,
+                                  device)
+        if max_context_blocks is None:
+            max_context_blocks = int(((pre + lens + 63) // 64).max())
+        return Chunk(shape, torch.as_tensor(pre.astype(np.int32), device=device),
+                     max_context_blocks)
+
+
+def chunk_append(k, v, chunk: Chunk, cache: PagedKVCache, dev_status):
+    """Write the chunk's keys / values (k, v [H_kv, T, d]) into their pages and
+    summarise those pages (bsa_chunk_append)."""
+    s, c = chunk.shape.c(), cache.c(chunk)
+    check("bsa_chunk_append", _lib.lib().bsa_chunk_append(
+        ctypes.byref(s), ctypes.byref(c), _p(k), _p(v), _p(dev_status), _stream()))
+
+
+def route_chunk_workspace_bytes(chunk: Chunk, cache: PagedKVCache, params: RouteParams) -> int:
+    s, c, p = chunk.shape.c(), cache.c(chunk), params.c()
+    return int(_lib.lib().bsa_route_chunk_workspace_size(ctypes.byref(s), ctypes.byref(c),
+                                                         ctypes.byref(p)))
+
+
+def route_chunk(q, chunk: Chunk, cache: PagedKVCache, params: RouteParams, dev_status, J=None,
+                counts=None, scores=None, ws=None):
+    """J [B, H_kv, N_q, k_max] logical block ids and counts of the chunk's query
+    blocks, routed against the cached page summaries (bsa_route_chunk)."""
+    sh, dev = chunk.shape, q.device
+    if J is None:
+        J = torch.empty(sh.num_seqs, sh.num_kv_heads, sh.max_blocks, params.k_max,
+                        dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty(sh.num_seqs, sh.num_kv_heads, sh.max_blocks, dtype=torch.int32,
+                             device=dev)
+    if ws is None:
+        ws = torch.empty(max(256, route_chunk_workspace_bytes(chunk, cache, params)),
+                         dtype=torch.uint8, device=dev)
+    s, c, p = sh.c(), cache.c(chunk), params.c(dev)
+    check("bsa_route_chunk", _lib.lib().bsa_route_chunk(
+        ctypes.byref(s), ctypes.byref(c), ctypes.byref(p), _p(q), _p(J), _p(counts), _p(scores),
+        _p(dev_status), _p(ws), ws.numel(), _stream()))
+    return J, counts
+
+
+def build_worklist_chunk(J, counts, chunk: Chunk, cache: PagedKVCache, k_max: int, dev_status,
+                         wl: Worklist | None = None, ws=None) -> Worklist:
+    dev, rows = J.device, chunk.shape.num_rows
+    if wl is None:
+        wl = Worklist(torch.empty(rows + 1, dtype=torch.int32, device=dev),
+                      torch.empty(max(1, rows * k_max), dtype=torch.int32, device=dev),
+                      torch.empty(max(1, rows), dtype=torch.int32, device=dev),
+                      torch.empty(NUM_BUCKETS + 1, dtype=torch.int32, device=dev))
+    s, c = chunk.shape.c(), cache.c(chunk)
+    if ws is None:
+        n = int(_lib.lib().bsa_worklist_workspace_size(ctypes.byref(s), k_max))
+        ws = torch.empty(max(256, n), dtype=torch.uint8, device=dev)
+    check("bsa_build_worklist_chunk", _lib.lib().bsa_build_worklist_chunk(
+        ctypes.byref(s), ctypes.byref(c), k_max, _p(J), _p(counts), _p(wl.row_ptr),
+        _p(wl.col_idx), _p(wl.work), _p(wl.bucket_off), _p(dev_status), _p(ws), ws.numel(),
+        _stream()))
+    return wl
+
+
+def attention_chunk(q, wl: Worklist, chunk: Chunk, cache: PagedKVCache, dev_status,
+                    scale: float = 0.0, out=None, lse=None, want_lse: bool = True):
+    """O [H, T, d] bf16 and lse [H, T] fp32 of the chunk's queries over the
+    selected cache pages (bsa_attention_chunk)."""
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(chunk.shape.num_heads, chunk.shape.total_tokens, dtype=torch.float32,
+                          device=q.device)
+    s, c = chunk.shape.c(), cache.c(chunk)
+    check("bsa_attention_chunk", _lib.lib().bsa_attention_chunk(
+        ctypes.byref(s), ctypes.byref(c), _p(q), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work),
+        _p(wl.bucket_off), float(scale), _p(out), _p(lse), _p(dev_status), _stream()))
+    return out, lse
+
+
+class ChunkPlan:
+    """Buffers of one chunk shape, allocated once; run() enqueues the four calls of
+    a chunked-prefill step (append, route, worklist, attention) on the current
+    stream."""
+
+    LAUNCHES = {"append": 1, "route": 3, "worklist": 3, "attention": 1}
+
+    def __init__(self, chunk: Chunk, cache: PagedKVCache, route: RouteParams, device="cuda"):
+        self.chunk, self.cache, self.params = chunk, cache, route
+        sh, dev = chunk.shape, device
+        self.J = torch.empty(sh.num_seqs, sh.num_kv_heads, sh.max_blocks, route.k_max,
+                             dtype=torch.int32, device=dev)
+        self.counts = torch.empty(sh.num_seqs, sh.num_kv_heads, sh.max_blocks, dtype=torch.int32,
+                                  device=dev)
+        self.route_ws = torch.empty(max(256, route_chunk_workspace_bytes(chunk, cache, route)),
+                                    dtype=torch.uint8, device=dev)
+        rows = sh.num_rows
+        self.wl = Worklist(torch.empty(rows + 1, dtype=torch.int32, device=dev),
+                           torch.empty(max(1, rows * route.k_max), dtype=torch.int32, device=dev),
+                           torch.empty(max(1, rows), dtype=torch.int32, device=dev),
+                           torch.empty(NUM_BUCKETS + 1, dtype=torch.int32, device=dev))
+        s = sh.c()
+        self.wl_ws = torch.empty(max(256, int(_lib.lib().bsa_worklist_workspace_size(
+            ctypes.byref(s), route.k_max))), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(sh.num_heads, sh.total_tokens, sh.head_dim, dtype=torch.bfloat16,
+                               device=dev)
+        self.lse = torch.empty(sh.num_heads, sh.total_tokens, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, q, k, v, scale: float = 0.0):
+        ch, ca = self.chunk, self.cache
+        chunk_append(k, v, ch, ca, self.status)
+        route_chunk(q, ch, ca, self.params, self.status, J=self.J, counts=self.counts,
+                    ws=self.route_ws)
+        build_worklist_chunk(self.J, self.counts, ch, ca, self.params.k_max, self.status,
+                             wl=self.wl, ws=self.wl_ws)
+        return attention_chunk(q, self.wl, ch, ca, self.status, scale, out=self.out, lse=self.lse)
 
 
 # ---------------------------------------------------------------- decode

@@ -15,7 +15,7 @@ BSA_OK = 0
 STATUS_NAMES = {
     0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED", 3: "BSA_ERR_WORKSPACE",
     4: "BSA_ERR_LAUNCH", 16: "BSA_ERR_INDEX_RANGE", 17: "BSA_ERR_INDEX_ORDER",
-    18: "BSA_ERR_COUNT", 19: "BSA_ERR_TIMEOUT",
+    18: "BSA_ERR_COUNT", 19: "BSA_ERR_TIMEOUT", 20: "BSA_ERR_CACHE",
 }
 BSA_BF16, BSA_FP32 = 0, 1
 NUM_BUCKETS = 7
@@ -48,6 +48,14 @@ class DecodeShape(ctypes.Structure):
                 ("num_phys_pages", ctypes.c_int32), ("top_k", ctypes.c_int32)]
 
 
+class KVCache(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("page_summ", ctypes.c_void_p), ("page_sum", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("prefix_lens", ctypes.c_void_p),
+                ("max_pages_per_req", ctypes.c_int32), ("num_phys_pages", ctypes.c_int32),
+                ("max_context_blocks", ctypes.c_int32)]
+
+
 V = ctypes.c_void_p
 SZ = ctypes.c_size_t
 I32 = ctypes.c_int32
@@ -69,6 +77,15 @@ PROTOTYPES = {
     "bsa_causal_worklist_capacity": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),
+    "bsa_chunk_append": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache), V, V, V, V]),
+    "bsa_route_chunk_workspace_size": (SZ, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache),
+                                            ctypes.POINTER(RouteParams)]),
+    "bsa_route_chunk": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache),
+                              ctypes.POINTER(RouteParams), V, V, V, V, V, V, SZ, V]),
+    "bsa_build_worklist_chunk": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache), I32, V, V,
+                                       V, V, V, V, V, V, SZ, V]),
+    "bsa_attention_chunk": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache), V, V, V, V, V,
+                                  F32, V, V, V, V]),
     "bsa_page_summaries": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V]),
     "bsa_page_summaries_append": (I32, [ctypes.POINTER(DecodeShape), V, V, V, V, V, V]),
     "bsa_decode_workspace_size": (SZ, [ctypes.POINTER(DecodeShape)]),

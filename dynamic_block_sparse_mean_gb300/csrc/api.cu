@@ -48,6 +48,44 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bsa_status_t launched(cudaError_t e) { return e == cudaSuccess ? BSA_OK : BSA_ERR_LAUNCH; }
 
+// Router parameters: BSA_OK or the status the call returns.
+bsa_status_t route_params_status(const bsa_route_params_t &p) {
+  if (p.mode != BSA_ROUTE_TOPK && p.mode != BSA_ROUTE_THRESHOLD) return BSA_ERR_INVALID_ARG;
+  if (p.k_max < 1 || p.k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
+  if (p.mode == BSA_ROUTE_THRESHOLD && (p.k_min < 0 || !(p.tau_delta >= 0.f) || !isfinite(p.tau_delta)))
+    return BSA_ERR_INVALID_ARG;
+  if (p.num_global < 0 || p.num_global > BSA_MAX_GLOBAL ||
+      (p.num_global > 0 && p.global_blocks == nullptr))
+    return BSA_ERR_INVALID_ARG;
+  if (p.window > p.k_max ||
+      (p.window > 1 ? p.window : 1) + p.num_global + (p.force_sink ? 1 : 0) > p.k_max)
+    return BSA_ERR_INVALID_ARG;
+  return BSA_OK;
+}
+
+// A chunk over a paged cache: BSA_OK or the status the call returns.  The page
+// is the routing block (64 tokens); a page's first row, (phys * H_kv + h) * 64,
+// must fit in int32; a score row of N_k entries must fit the select kernel's
+// shared memory.
+bsa_status_t chunk_status(const bsa_shape_t *s, const bsa_kv_cache_t *c) {
+  if (!shape_ok(s) || c == nullptr || c->k_cache == nullptr || c->v_cache == nullptr ||
+      c->page_summ == nullptr || c->block_table == nullptr || c->prefix_lens == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (s->dtype != BSA_BF16 || s->block != 64 || (s->head_dim != 64 && s->head_dim != 128))
+    return BSA_ERR_UNSUPPORTED;
+  if (c->max_pages_per_req < 1 || c->num_phys_pages < 1 || c->max_context_blocks < s->max_blocks ||
+      c->max_context_blocks > c->max_pages_per_req)
+    return BSA_ERR_INVALID_ARG;
+  if ((long long)c->num_phys_pages * s->num_kv_heads * 64 > INT32_MAX ||
+      (long long)s->num_seqs * s->num_kv_heads * c->max_context_blocks > (1LL << 30) ||
+      (long long)c->max_context_blocks * 5 + 1040 > 227 * 1024)
+    return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(c->k_cache) || !aligned16(c->v_cache) || !aligned16(c->page_summ) ||
+      (c->page_sum != nullptr && !aligned16(c->page_sum)))
+    return BSA_ERR_INVALID_ARG;
+  return BSA_OK;
+}
+
 bool decode_ok(const bsa_decode_shape_t *s) {
   return s != nullptr && s->num_reqs >= 1 && s->num_heads >= 1 && s->num_kv_heads >= 1 &&
          s->num_heads % s->num_kv_heads == 0 && s->max_pages_per_req >= 1 &&
@@ -78,6 +116,7 @@ const char *bsa_status_string(bsa_status_t s) {
     case BSA_ERR_INDEX_ORDER: return "index row not strictly increasing";
     case BSA_ERR_COUNT: return "row count outside [0, k_max]";
     case BSA_ERR_TIMEOUT: return "bounded barrier wait timed out";
+    case BSA_ERR_CACHE: return "chunk prefix off the page grid, or page outside the cache";
   }
   return "unknown status";
 }
@@ -103,25 +142,14 @@ bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *param
       counts == nullptr)
     return BSA_ERR_INVALID_ARG;
   if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
-  if (params->mode != BSA_ROUTE_TOPK && params->mode != BSA_ROUTE_THRESHOLD)
-    return BSA_ERR_INVALID_ARG;
-  if (params->k_max < 1 || params->k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
-  if (params->mode == BSA_ROUTE_THRESHOLD &&
-      (params->k_min < 0 || !(params->tau_delta >= 0.f) || !isfinite(params->tau_delta)))
-    return BSA_ERR_INVALID_ARG;
-  if (params->num_global < 0 || params->num_global > BSA_MAX_GLOBAL ||
-      (params->num_global > 0 && params->global_blocks == nullptr))
-    return BSA_ERR_INVALID_ARG;
-  if (params->window > params->k_max ||
-      (params->window > 1 ? params->window : 1) + params->num_global +
-              (params->force_sink ? 1 : 0) > params->k_max)
-    return BSA_ERR_INVALID_ARG;
+  const bsa_status_t ps = route_params_status(*params);
+  if (ps != BSA_OK) return ps;
   if (!aligned16(Q) || !aligned16(C)) return BSA_ERR_INVALID_ARG;
   const size_t need = bsa::route_workspace_bytes(*shape, *params);
   if (ws == nullptr || ws_bytes < need) return BSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return BSA_ERR_INVALID_ARG;
-  return launched(bsa::launch_route(*shape, *params, Q, C, J, counts, scores, dev_status, ws,
-                                    stream));
+  return launched(bsa::launch_route(*shape, *params, Q, C, nullptr, J, counts, scores,
+                                    dev_status, ws, stream));
 }
 
 size_t bsa_worklist_workspace_size(const bsa_shape_t *shape, int32_t k_max) {
@@ -207,6 +235,75 @@ bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
   if (!shape_ok(shape) || lse_sparse == nullptr || lse_dense == nullptr || C == nullptr)
     return BSA_ERR_INVALID_ARG;
   return launched(bsa::launch_coverage(*shape, lse_sparse, lse_dense, C, stream));
+}
+
+bsa_status_t bsa_chunk_append(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                              const void *K, const void *V, int32_t *dev_status,
+                              cudaStream_t stream) {
+  const bsa_status_t cs = chunk_status(shape, cache);
+  if (cs != BSA_OK) return cs;
+  if (K == nullptr || V == nullptr || dev_status == nullptr) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V)) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_chunk_append(*shape, *cache, K, V, dev_status, stream));
+}
+
+size_t bsa_route_chunk_workspace_size(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                      const bsa_route_params_t *params) {
+  if (chunk_status(shape, cache) != BSA_OK || params == nullptr) return 0;
+  return bsa::route_workspace_bytes(*shape, *params, cache);
+}
+
+bsa_status_t bsa_route_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                             const bsa_route_params_t *params, const void *Q, int32_t *J,
+                             int32_t *counts, float *scores, int32_t *dev_status, void *ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  const bsa_status_t cs = chunk_status(shape, cache);
+  if (cs != BSA_OK) return cs;
+  if (params == nullptr || Q == nullptr || J == nullptr || counts == nullptr ||
+      dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  const bsa_status_t ps = route_params_status(*params);
+  if (ps != BSA_OK) return ps;
+  if (!aligned16(Q)) return BSA_ERR_INVALID_ARG;
+  const size_t need = bsa::route_workspace_bytes(*shape, *params, cache);
+  if (ws == nullptr || ws_bytes < need) return BSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_route(*shape, *params, Q, nullptr, cache, J, counts, scores,
+                                    dev_status, ws, stream));
+}
+
+bsa_status_t bsa_build_worklist_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                      int32_t k_max, const int32_t *J, const int32_t *counts,
+                                      int32_t *row_ptr, int32_t *col_idx, int32_t *work,
+                                      int32_t *bucket_off, int32_t *dev_status, void *ws,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  const bsa_status_t cs = chunk_status(shape, cache);
+  if (cs != BSA_OK) return cs;
+  if (J == nullptr || counts == nullptr || row_ptr == nullptr || col_idx == nullptr ||
+      work == nullptr || bucket_off == nullptr || dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (k_max < 1 || k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < bsa::worklist_workspace_bytes(*shape, k_max))
+    return BSA_ERR_WORKSPACE;
+  return launched(bsa::launch_worklist(*shape, k_max, J, counts, row_ptr, col_idx, work,
+                                       bucket_off, dev_status, ws, stream, cache));
+}
+
+bsa_status_t bsa_attention_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                 const void *Q, const int32_t *row_ptr, const int32_t *col_idx,
+                                 const int32_t *work, const int32_t *bucket_off,
+                                 float softmax_scale, void *O, float *lse, int32_t *dev_status,
+                                 cudaStream_t stream) {
+  const bsa_status_t cs = chunk_status(shape, cache);
+  if (cs != BSA_OK) return cs;
+  if (Q == nullptr || row_ptr == nullptr || col_idx == nullptr || work == nullptr ||
+      bucket_off == nullptr || O == nullptr || dev_status == nullptr)
+    return BSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(O)) return BSA_ERR_INVALID_ARG;
+  if (!isfinite(softmax_scale)) return BSA_ERR_INVALID_ARG;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)shape->head_dim);
+  return launched(bsa::launch_attention_chunk(*shape, *cache, Q, row_ptr, col_idx, work,
+                                              bucket_off, scale, O, lse, dev_status, stream));
 }
 
 bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const void *K,

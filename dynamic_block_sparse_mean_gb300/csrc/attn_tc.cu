@@ -94,14 +94,29 @@ struct AttnParams {
   uint16_t *O;
   float *lse;
   int32_t *status;
+  // Chunked prefill over a paged cache (CHUNK kernels only): tokens cached before
+  // each sequence's chunk, the block table and its row length.
+  const int32_t *qoff;
+  const int32_t *bt;
+  int maxp;
   int T, H, Hk, G, Nq, mtiles, npairs;
   float scale_log2;
 };
 
+// A work unit: logical block r of the row (the diagonal) and, in a chunk, its
+// query block qb in the packed Q / O (r = qb + the blocks cached before the
+// chunk); without a cache both are r.
 struct Unit {
-  int row, r, h, i, s0, n, kv0, nkv, pair, nt;
+  int row, r, qb, h, i, s0, n, kv0, nkv, pair, nt;
 };
 
+template <bool CHUNK>
+BSA_DEV int qblock(const Unit &x) {
+  if constexpr (CHUNK) return x.qb;
+  return x.r;
+}
+
+template <bool CHUNK>
 BSA_DEV Unit decode_unit(const AttnParams &p, int u) {
   Unit x;
   const int slot = u / p.npairs;
@@ -110,12 +125,32 @@ BSA_DEV Unit decode_unit(const AttnParams &p, int u) {
   x.r = x.row % p.Nq;
   x.h = (x.row / p.Nq) % p.Hk;
   x.i = x.row / (p.Nq * p.Hk);
+  if constexpr (CHUNK) {
+    x.qb = x.r;
+    x.r += __ldg(p.qoff + x.i) / 64;
+  }
   x.s0 = __ldg(p.cu + x.i);
   x.n = __ldg(p.cu + x.i + 1) - x.s0;
   x.kv0 = __ldg(p.row_ptr + x.row);
   x.nkv = __ldg(p.row_ptr + x.row + 1) - x.kv0;
   x.nt = min(2, p.mtiles - 2 * x.pair);
   return x;
+}
+
+// Tensor coordinates (token row, head) of the K / V tile of entry jb of a unit's
+// row: the packed [H_kv, T, d] layout, or in a chunk the page the block table
+// names in the cache viewed as rows of [P * H_kv * 64, d] (the page index is
+// clamped to the table; a physical id outside the cache reads zeros).
+template <bool CHUNK, int BK>
+BSA_DEV int2 kv_coord(const AttnParams &p, const Unit &w, int jb) {
+  const int j = __ldg(p.col_idx + w.kv0 + jb);
+  if constexpr (CHUNK) {
+    const int pg = min(max(j, 0), p.maxp - 1);
+    const int phys = __ldg(p.bt + (size_t)w.i * p.maxp + pg);
+    return make_int2((phys * p.Hk + w.h) * 64, 0);
+  } else {
+    return make_int2(w.s0 + j * BK, w.h);
+  }
 }
 
 // High word of every shared-memory descriptor used here: stride byte offset
@@ -352,7 +387,7 @@ BSA_DEV float exp_step(uint32_t tS, uint64_t scale2, uint64_t negm, const int (&
   return lo_of(acc) + hi_of(acc);
 }
 
-template <int D, int BK>
+template <int D, int BK, bool CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -418,10 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < C::NS; ++s) issuedK[s] = issuedV[s] = -1;
       bool ok = true;
       Unit nx;
-      if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
+      if (blockIdx.x < total_units) nx = decode_unit<CHUNK>(p, blockIdx.x);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
         const Unit x = nx;
-        if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
+        if (u + (int)gridDim.x < total_units) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
         if (!(ok = mbar_wait(bar(C::B_QEMPTY), (ucount & 1) ^ 1, abort_flag, p.status))) break;
         mbar_arrive_expect_tx(bar(C::B_QFULL), x.nt * C::kQTile);
         issuedQ = ucount & 1;
@@ -429,13 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int hq0 = x.h * p.G + ((2 * x.pair + t) * 128) / BK;
           for (int pn = 0; pn < C::kPanels; ++pn)
             tma_load_3d(smQ + t * C::kQTile + pn * 16384, &tmQ, bar(C::B_QFULL), pn * 64,
-                        x.s0 + x.r * BK, hq0);
+                        x.s0 + qblock<CHUNK>(x) * BK, hq0);
         }
         const bool has_next = u + (int)gridDim.x < total_units;
         if (has_next)  // the next unit's queries come from HBM: start them towards L2 now
           for (int t = 0; t < nx.nt; ++t)
             for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_prefetch_l2_3d(&tmQ, pn * 64, nx.s0 + nx.r * BK,
+              tma_prefetch_l2_3d(&tmQ, pn * 64, nx.s0 + qblock<CHUNK>(nx) * BK,
                                  nx.h * p.G + ((2 * nx.pair + t) * 128) / BK);
         const int nsteps = (x.nkv + BPS - 1) / BPS;
         const int nsteps_next = has_next ? (nx.nkv + BPS - 1) / BPS : 0;
@@ -445,10 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < BPS; ++e) {
             const int jb = min(s * BPS + e, w.nkv - 1);
-            const int y = w.s0 + __ldg(p.col_idx + w.kv0 + jb) * BK;
+            const int2 y = kv_coord<CHUNK, BK>(p, w, jb);
             for (int pn = 0; pn < C::kPanels; ++pn) {
-              tma_prefetch_l2_3d(&tmK, pn * 64, y, w.h);
-              tma_prefetch_l2_3d(&tmV, pn * 64, y, w.h);
+              tma_prefetch_l2_3d(&tmK, pn * 64, y.x, y.y);
+              tma_prefetch_l2_3d(&tmV, pn * 64, y.x, y.y);
             }
           }
         };
@@ -459,12 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_step(x, s + kPrefetch);
           else if (s + kPrefetch - nsteps < nsteps_next)
             prefetch_step(nx, s + kPrefetch - nsteps);
-          int y[BPS];
+          int2 y[BPS];
 #pragma unroll
-          for (int e = 0; e < BPS; ++e) {
-            const int jb = min(s * BPS + e, x.nkv - 1);  // a missing block repeats the last one
-            y[e] = x.s0 + __ldg(p.col_idx + x.kv0 + jb) * BK;
-          }
+          for (int e = 0; e < BPS; ++e)  // a missing block repeats the last one
+            y[e] = kv_coord<CHUNK, BK>(p, x, min(s * BPS + e, x.nkv - 1));
           const int st = stp % C::NS;
           const uint32_t ph = ((stp / C::NS) & 1) ^ 1;
           if (!(ok = mbar_wait(bar(C::B_KEMPTY + st), ph, abort_flag, p.status))) break;
@@ -474,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < BPS; ++e)
             for (int pn = 0; pn < C::kPanels; ++pn)
               tma_load_3d(smK + st * C::kStage + pn * C::kPanel + e * BK * 128, &tmK,
-                          bar(C::B_KFULL + st), pn * 64, y[e], x.h);
+                          bar(C::B_KFULL + st), pn * 64, y[e].x, y[e].y);
           if (!(ok = mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.status))) break;
           mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::kStage);
           issuedV[st] = ph ^ 1;
@@ -482,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < BPS; ++e)
             for (int pn = 0; pn < C::kPanels; ++pn)
               tma_load_3d(smV + st * C::kStage + pn * C::kPanel + e * BK * 128, &tmV,
-                          bar(C::B_VFULL + st), pn * 64, y[e], x.h);
+                          bar(C::B_VFULL + st), pn * 64, y[e].x, y[e].y);
         }
       }
       if (!ok) {  // let every copy already in flight land before the CTA leaves
@@ -526,10 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (acc || kk > 0) ? 1u : 0u);
       };
       Unit nx;
-      if (blockIdx.x < total_units) nx = decode_unit(p, blockIdx.x);
+      if (blockIdx.x < total_units) nx = decode_unit<CHUNK>(p, blockIdx.x);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
         const Unit x = nx;
-        if (u + (int)gridDim.x < total_units) nx = decode_unit(p, u + gridDim.x);  // prefetch
+        if (u + (int)gridDim.x < total_units) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
         const int nsteps = (x.nkv + BPS - 1) / BPS;
         if (!(ok = mbar_wait(bar(C::B_QFULL), ucount & 1, abort_flag, p.status))) break;
         tc_fence_after();
@@ -618,14 +651,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit nx;
     int nx_diag = -1;
     if (blockIdx.x < total_units) {
-      nx = decode_unit(p, blockIdx.x);
+      nx = decode_unit<CHUNK>(p, blockIdx.x);
       nx_diag = diag_of(nx);
     }
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit x = nx;
       const int diag_j = nx_diag;
       const bool has_next = u + (int)gridDim.x < total_units;
-      if (has_next) nx = decode_unit(p, u + gridDim.x);  // prefetch
+      if (has_next) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
       if (t >= x.nt) {
         if (has_next) nx_diag = diag_of(nx);
         continue;
@@ -635,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_valid = grow < p.G * BK;
       const int hq = x.h * p.G + grow / BK;
       const int tok_in_blk = grow % BK;
-      const int tq = x.r * BK + tok_in_blk;            // sequence-relative query position
+      const int tq = qblock<CHUNK>(x) * BK + tok_in_blk;  // query position in the packed Q
       float m_used = -INFINITY, l = 0.f;
       for (int s = 0; s < nsteps; ++s, ++kstep) {
         // Column limits of the two 64-column halves of this step: keys past the
@@ -723,7 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // through shared memory and tensor stores (one 64-column half at a time, in
       // the 128-byte-swizzled layout of the store box); other tiles (sequence
       // tails, partial groups) store their valid rows directly.
-      const bool via_tma = (2 * x.pair + t + 1) * 128 <= p.G * BK && (x.r + 1) * BK <= x.n;
+      const bool via_tma =
+          (2 * x.pair + t + 1) * 128 <= p.G * BK && (qblock<CHUNK>(x) + 1) * BK <= x.n;
       if (via_tma) {
         const uint32_t stg = sbase + C::kOffStageO + t * C::kStageO;
         const bool elected = wq == 0 && lane == 0;
@@ -741,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar(C::B_OSTAGED + t));
           if (elected) {
             if (!(ok = mbar_wait(bar(C::B_OSTAGED + t), ostage & 1, abort_flag, p.status))) break;
-            tma_store_3d(&tmO, stg, hh * 64, x.s0 + x.r * BK,
+            tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
                          x.h * p.G + ((2 * x.pair + t) * 128) / BK);
             bulk_commit();
             bulk_wait_read();
@@ -769,19 +803,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK>
+// cache == nullptr: K / V packed [H_kv, T, d]; otherwise a chunk over the paged
+// cache (block 64 = the page), K / V read from its pages.
+template <int D, int BK, bool CHUNK>
 cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const void *V,
-                      const int32_t *row_ptr, const int32_t *col_idx, const int32_t *work,
-                      const int32_t *bucket_off, float scale, void *O, float *lse,
-                      int32_t *dev_status, cudaStream_t st) {
+                      const bsa_kv_cache_t *cache, const int32_t *row_ptr,
+                      const int32_t *col_idx, const int32_t *work, const int32_t *bucket_off,
+                      float scale, void *O, float *lse, int32_t *dev_status, cudaStream_t st) {
   using C = Cfg<D, BK>;
   CUtensorMap mq, mk, mv;
   CUtensorMap mo;
-  if (!make_tmap_3d_bf16(&mo, O, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
-      !make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
-      !make_tmap_3d_bf16(&mk, K, D, s.total_tokens, s.num_kv_heads, 64, BK, 1) ||
-      !make_tmap_3d_bf16(&mv, V, D, s.total_tokens, s.num_kv_heads, 64, BK, 1))
-    return cudaErrorInvalidValue;
+  bool ok = make_tmap_3d_bf16(&mo, O, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK) &&
+            make_tmap_3d_bf16(&mq, Q, D, s.total_tokens, s.num_heads, 64, BK, 128 / BK);
+  if constexpr (CHUNK) {
+    const uint64_t rows = (uint64_t)cache->num_phys_pages * s.num_kv_heads * 64;
+    ok = ok && make_tmap_3d_bf16(&mk, cache->k_cache, D, rows, 1, 64, 64, 1) &&
+         make_tmap_3d_bf16(&mv, cache->v_cache, D, rows, 1, 64, 64, 1);
+  } else {
+    ok = ok && make_tmap_3d_bf16(&mk, K, D, s.total_tokens, s.num_kv_heads, 64, BK, 1) &&
+         make_tmap_3d_bf16(&mv, V, D, s.total_tokens, s.num_kv_heads, 64, BK, 1);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   AttnParams p;
   p.cu = s.cu_seqlens;
   p.row_ptr = row_ptr;
@@ -791,6 +833,9 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   p.O = static_cast<uint16_t *>(O);
   p.lse = lse;
   p.status = dev_status;
+  p.qoff = CHUNK ? cache->prefix_lens : nullptr;
+  p.bt = CHUNK ? cache->block_table : nullptr;
+  p.maxp = CHUNK ? cache->max_pages_per_req : 0;
   p.T = s.total_tokens;
   p.H = s.num_heads;
   p.Hk = s.num_kv_heads;
@@ -799,13 +844,13 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   p.mtiles = (p.G * BK + 127) / 128;
   p.npairs = (p.mtiles + 1) / 2;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, BK>,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, BK, CHUNK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long max_units = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks * p.npairs;
   const int grid = (int)std::min<long long>(num_sms(), std::max<long long>(1, max_units));
-  return launch_dependent(attn_tc_kernel<D, BK>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, mq,
-                          mk, mv, mo, p);
+  return launch_dependent(attn_tc_kernel<D, BK, CHUNK>, dim3(grid), dim3(kThreads),
+                          C::kSmemBytes, st, mq, mk, mv, mo, p);
 }
 
 }  // namespace
@@ -815,16 +860,27 @@ cudaError_t launch_attention_tc(const bsa_shape_t &s, const void *Q, const void 
                                 const int32_t *work, const int32_t *bucket_off, float scale,
                                 void *O, float *lse, int32_t *dev_status, cudaStream_t st) {
   if (s.head_dim == 64 && s.block == 64)
-    return launch_tc<64, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse,
-                             dev_status, st);
+    return launch_tc<64, 64, false>(s, Q, K, V, nullptr, row_ptr, col_idx, work, bucket_off,
+                                    scale, O, lse, dev_status, st);
   if (s.head_dim == 64 && s.block == 128)
-    return launch_tc<64, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse,
-                              dev_status, st);
+    return launch_tc<64, 128, false>(s, Q, K, V, nullptr, row_ptr, col_idx, work, bucket_off,
+                                     scale, O, lse, dev_status, st);
   if (s.head_dim == 128 && s.block == 64)
-    return launch_tc<128, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse,
-                              dev_status, st);
-  return launch_tc<128, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse,
-                             dev_status, st);
+    return launch_tc<128, 64, false>(s, Q, K, V, nullptr, row_ptr, col_idx, work, bucket_off,
+                                     scale, O, lse, dev_status, st);
+  return launch_tc<128, 128, false>(s, Q, K, V, nullptr, row_ptr, col_idx, work, bucket_off,
+                                    scale, O, lse, dev_status, st);
+}
+
+cudaError_t launch_attention_chunk(const bsa_shape_t &s, const bsa_kv_cache_t &cache,
+                                   const void *Q, const int32_t *row_ptr, const int32_t *col_idx,
+                                   const int32_t *work, const int32_t *bucket_off, float scale,
+                                   void *O, float *lse, int32_t *dev_status, cudaStream_t st) {
+  if (s.head_dim == 64)
+    return launch_tc<64, 64, true>(s, Q, nullptr, nullptr, &cache, row_ptr, col_idx, work,
+                                   bucket_off, scale, O, lse, dev_status, st);
+  return launch_tc<128, 64, true>(s, Q, nullptr, nullptr, &cache, row_ptr, col_idx, work,
+                                  bucket_off, scale, O, lse, dev_status, st);
 }
 
 }  // namespace bsa

@@ -22,6 +22,14 @@ BSA_DEV void set_status(int32_t *status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// A chunk of n > 0 tokens that follows `prefix` cached tokens is usable when the
+// prefix is whole blocks of b and the context fits in Nk blocks (computed without
+// forming prefix + n, which a bad prefix could overflow).  A sequence adding no
+// tokens is idle: its prefix is not looked at.
+BSA_DEV bool chunk_ok(int prefix, int n, int b, int Nk) {
+  return n == 0 || (prefix >= 0 && prefix % b == 0 && prefix / b <= Nk - (n + b - 1) / b);
+}
+
 BSA_DEV float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 BSA_DEV uint32_t pack_bf16x2(float lo, float hi) {

@@ -40,9 +40,11 @@ bool make_tmap_3d_bf16(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d
 
 // a2 on the tensor cores (route_tc.cu): exact fp32 scores from bf16 Q and the
 // three-way bf16 split of the fp32 summaries; writes S[row][j] for j < r.
-size_t route_tc_workspace_bytes(const bsa_shape_t &s);
-cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C, float *S,
-                                   void *ws, int32_t *dev_status, cudaStream_t st);
+// cache != nullptr: a chunked prefill, summaries gathered from the paged cache.
+size_t route_tc_workspace_bytes(const bsa_shape_t &s, const bsa_kv_cache_t *cache);
+cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C,
+                                   const bsa_kv_cache_t *cache, float *S, void *ws,
+                                   int32_t *dev_status, cudaStream_t st);
 
 // a1 and the decode page summaries (summaries.cu)
 cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
@@ -54,19 +56,24 @@ cudaError_t launch_page_summaries_append(const bsa_decode_shape_t &s, const void
 cudaError_t launch_page_summaries(const bsa_decode_shape_t &s, const void *k_cache,
                                   const int32_t *block_table, const int32_t *context_lens,
                                   float *page_summ, cudaStream_t st);
+cudaError_t launch_chunk_append(const bsa_shape_t &s, const bsa_kv_cache_t &cache, const void *K,
+                                const void *V, int32_t *dev_status, cudaStream_t st);
 
 // a2 + a3 (route.cu)
-size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &p);
+// cache != nullptr: a chunked prefill (C unused, summaries from the cache).
+size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &p,
+                             const bsa_kv_cache_t *cache = nullptr);
 cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
-                         const float *C, int32_t *J, int32_t *counts, float *scores,
-                         int32_t *dev_status, void *ws, cudaStream_t st);
+                         const float *C, const bsa_kv_cache_t *cache, int32_t *J,
+                         int32_t *counts, float *scores, int32_t *dev_status, void *ws,
+                         cudaStream_t st);
 
 // a4 (worklist.cu)
 size_t worklist_workspace_bytes(const bsa_shape_t &s, int32_t k_max);
 cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *J,
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
-                            cudaStream_t st);
+                            cudaStream_t st, const bsa_kv_cache_t *cache = nullptr);
 // Backward of the sparse attention (attn_bwd.cu).
 size_t attention_bwd_workspace_bytes(const bsa_shape_t &s);
 cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void *K,
@@ -89,6 +96,11 @@ cudaError_t launch_attention_tc(const bsa_shape_t &s, const void *Q, const void 
                                 const void *V, const int32_t *row_ptr, const int32_t *col_idx,
                                 const int32_t *work, const int32_t *bucket_off, float scale,
                                 void *O, float *lse, int32_t *dev_status, cudaStream_t st);
+// Chunked prefill: the chunk's queries over the selected pages of the cache.
+cudaError_t launch_attention_chunk(const bsa_shape_t &s, const bsa_kv_cache_t &cache,
+                                   const void *Q, const int32_t *row_ptr, const int32_t *col_idx,
+                                   const int32_t *work, const int32_t *bucket_off, float scale,
+                                   void *O, float *lse, int32_t *dev_status, cudaStream_t st);
 cudaError_t launch_attention_simt_f32(const bsa_shape_t &s, const void *Q, const void *K,
                                       const void *V, const int32_t *row_ptr,
                                       const int32_t *col_idx, const int32_t *work,

@@ -132,30 +132,39 @@ BSA_DEV uint32_t order_key(float v) {
 // (score desc, index asc), found by a radix select on order-preserving keys (8 bits
 // per pass from the top; it stops once the bin of the k-th key holds exactly the
 // keys still needed), then written with the forced blocks in one ordered pass.
-// Dynamic shared memory: N_q floats of scores, a 256-bin histogram, N_q flag bytes.
+// Row (i, h, qb) selects for logical block r = qb, or in a chunked prefill
+// qb + the blocks cached before the chunk (qoff: cached tokens per sequence);
+// S rows hold Nk scores.
+// Dynamic shared memory: Nk floats of scores, a 256-bin histogram, Nk flag bytes.
 __global__ void __launch_bounds__(32) route_select_kernel(
-    const float *__restrict__ S, const int32_t *__restrict__ cu, int32_t *__restrict__ J,
-    int32_t *__restrict__ counts, int Nq, int Hk, int b, int mode, int k_max, int k_min,
-    float tau_delta, int force_sink, int window, int num_global,
-    const int32_t *__restrict__ global_blocks) {
+    const float *__restrict__ S, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ qoff, int32_t *__restrict__ J, int32_t *__restrict__ counts,
+    int Nq, int Nk, int Hk, int b, int mode, int k_max, int k_min, float tau_delta,
+    int force_sink, int window, int num_global, const int32_t *__restrict__ global_blocks) {
   extern __shared__ uint8_t sm[];
   float *sc = reinterpret_cast<float *>(sm);
-  int32_t *hist = reinterpret_cast<int32_t *>(sm + (size_t)Nq * 4);
-  uint8_t *taken = sm + (size_t)Nq * 4 + 256 * 4;
+  int32_t *hist = reinterpret_cast<int32_t *>(sm + (size_t)Nk * 4);
+  uint8_t *taken = sm + (size_t)Nk * 4 + 256 * 4;
   const int lane = threadIdx.x;
   const int row = blockIdx.x;
-  const int r = row % Nq, h = (row / Nq) % Hk, i = row / (Nq * Hk);
-  (void)h;
+  const int qb = row % Nq, i = row / (Nq * Hk);
   grid_dep_wait();  // the scores come from the previous launch
   const int n = cu[i + 1] - cu[i];
   const int nb = (n + b - 1) / b;
+  int r = qb;
+  bool ok = true;
+  if (qoff != nullptr) {
+    const int pre = qoff[i];
+    ok = chunk_ok(pre, n, b, Nk);
+    if (ok) r += pre / b;
+  }
   int32_t *Jrow = J + (size_t)row * k_max;
-  if (r >= nb) {
+  if (!ok || qb >= nb) {
     for (int e = lane; e < k_max; e += 32) Jrow[e] = -1;
     if (lane == 0) counts[row] = 0;
     return;
   }
-  const float *Srow = S + (size_t)row * Nq;
+  const float *Srow = S + (size_t)row * Nk;
   // Forced blocks F_r (union routing: local window, global list, sink, diagonal)
   // are marked `taken` so the dynamic choice never spends budget on them; a block
   // named by several branches is kept once.
@@ -282,23 +291,28 @@ __global__ void __launch_bounds__(32) route_select_kernel(
 }  // namespace
 
 // Workspace: [bf16 split of C, BF16 path only][score matrix, unless the caller
-// passes its own `scores` buffer].
-size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &) {
-  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s) : 0;
-  return split + (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * s.max_blocks * sizeof(float);
+// passes its own `scores` buffer].  With a cache (chunked prefill) the summaries
+// come from its pages and score rows hold N_k entries.
+size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &,
+                             const bsa_kv_cache_t *cache) {
+  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s, cache) : 0;
+  const size_t Nk = cache != nullptr ? cache->max_context_blocks : s.max_blocks;
+  return split + (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * Nk * sizeof(float);
 }
 
 cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
-                         const float *C, int32_t *J, int32_t *counts, float *scores,
-                         int32_t *dev_status, void *ws, cudaStream_t st) {
-  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s) : 0;
+                         const float *C, const bsa_kv_cache_t *cache, int32_t *J,
+                         int32_t *counts, float *scores, int32_t *dev_status, void *ws,
+                         cudaStream_t st) {
+  const size_t split = s.dtype == BSA_BF16 ? route_tc_workspace_bytes(s, cache) : 0;
   float *S = scores != nullptr ? scores
                                : reinterpret_cast<float *>(static_cast<char *>(ws) + split);
   const int G = s.num_heads / s.num_kv_heads;
+  const int Nk = cache != nullptr ? cache->max_context_blocks : s.max_blocks;
   const dim3 grid(s.max_blocks, s.num_kv_heads, s.num_seqs);
   cudaError_t e;
   if (s.dtype == BSA_BF16) {
-    e = launch_route_scores_tc(s, Q, C, S, ws, dev_status, st);
+    e = launch_route_scores_tc(s, Q, C, cache, S, ws, dev_status, st);
     if (e != cudaSuccess) return e;
   } else {
     route_scores_kernel<float><<<grid, kThreads, 0, st>>>(
@@ -308,16 +322,16 @@ cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, cons
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = s.num_seqs * s.num_kv_heads * s.max_blocks;
-  const size_t sm = (size_t)s.max_blocks * 5 + 256 * 4 + 16;
+  const size_t sm = (size_t)Nk * 5 + 256 * 4 + 16;
   if (sm > 48 * 1024) {
     e = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
   }
-  return launch_dependent(route_select_kernel, dim3(rows), dim3(32), sm, st, S, s.cu_seqlens, J,
-                          counts, s.max_blocks, s.num_kv_heads, s.block, p.mode, p.k_max,
-                          p.k_min, p.tau_delta, p.force_sink, p.window, p.num_global,
-                          p.global_blocks);
+  return launch_dependent(route_select_kernel, dim3(rows), dim3(32), sm, st, S, s.cu_seqlens,
+                          cache != nullptr ? cache->prefix_lens : nullptr, J, counts,
+                          s.max_blocks, Nk, s.num_kv_heads, s.block, p.mode, p.k_max, p.k_min,
+                          p.tau_delta, p.force_sink, p.window, p.num_global, p.global_blocks);
 }
 
 }  // namespace bsa

@@ -53,29 +53,41 @@ struct RCfg {
 
 struct RouteTcParams {
   const int32_t *cu;
+  const int32_t *qoff;  // chunked prefill: tokens cached before each chunk (else null)
   float *S;
   int32_t *status;
   int B, Nq, Hk, G, b;
+  int Nk;         // summaries per (sequence, KV head) = row length of S (N_q without a cache)
   int nch;        // query chunks per row: ceil(G*b / 256)
 };
 
+// Router row: query block qb of sequence i and KV head h (its queries in the packed
+// Q), logical block r = qb (+ the cached blocks before a chunk) scored against
+// summaries 0 .. r-1.
 struct RUnit {
-  int i, h, r, s0, nvalid;
+  int i, h, r, qb, s0, nvalid;
   bool valid;
 };
 
 BSA_DEV RUnit runit(const RouteTcParams &p, int u) {
   RUnit x;
   const int BH = p.B * p.Hk;
-  x.r = p.Nq - 1 - u / BH;
+  x.qb = p.Nq - 1 - u / BH;
   const int ih = u % BH;
   x.i = ih / p.Hk;
   x.h = ih % p.Hk;
   x.s0 = __ldg(p.cu + x.i);
   const int n = __ldg(p.cu + x.i + 1) - x.s0;
   const int nb = (n + p.b - 1) / p.b;
-  x.valid = x.r >= 1 && x.r < nb;
-  x.nvalid = min(p.b, n - x.r * p.b);
+  bool ok = true;
+  x.r = x.qb;
+  if (p.qoff != nullptr) {
+    const int pre = __ldg(p.qoff + x.i);
+    ok = chunk_ok(pre, n, p.b, p.Nk);
+    if (ok) x.r += pre / p.b;
+  }
+  x.valid = ok && x.r >= 1 && x.qb < nb;
+  x.nvalid = min(p.b, n - x.qb * p.b);
   return x;
 }
 
@@ -141,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const RUnit x = runit(p, u);
         if (!x.valid) continue;
         const int nmt = (x.r + 127) / 128;
-        const int crow = (x.i * p.Hk + x.h) * p.Nq;
+        const int crow = (x.i * p.Hk + x.h) * p.Nk;
         for (int ch = 0; ok && ch < p.nch; ++ch, ++qi) {
           const int qs = qi % kQStages;
           if (!(ok = mbar_wait(bar(C::B_QEMPTY + qs), ((qi / kQStages) & 1) ^ 1, abort_flag, p.status)))
@@ -150,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lastQ[qs] = (qi / kQStages) & 1;
           for (int pn = 0; pn < C::kPanels; ++pn)
             tma_load_3d(smQ + qs * C::kQStage + pn * 32768, &tmQ, bar(C::B_QFULL + qs), pn * 64,
-                        x.s0 + x.r * p.b, x.h * p.G + ch * heads_per_chunk);
+                        x.s0 + x.qb * p.b, x.h * p.G + ch * heads_per_chunk);
           for (int mt = 0; ok && mt < nmt; ++mt)
             for (int part = 2; ok && part >= 0; --part)
               for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const RUnit x = runit(p, u);
       if (!x.valid) continue;
       const int nmt = (x.r + 127) / 128;
-      float *Srow = p.S + ((size_t)(x.i * p.Hk + x.h) * p.Nq + x.r) * p.Nq;
+      float *Srow = p.S + ((size_t)(x.i * p.Hk + x.h) * p.Nq + x.qb) * p.Nk;
       const bool full = x.nvalid == p.b;
       for (int ch = 0; ok && ch < p.nch; ++ch) {
         const int ncols = chunk_cols(p, ch);
@@ -289,16 +301,68 @@ __global__ void split3_kernel(const float *__restrict__ C, uint16_t *__restrict_
   grid_dep_launch();
 }
 
+// Chunked prefill: the page summaries of every context block, gathered through
+// the block table into rows (i, h, j < N_k) and split three ways as split3_kernel
+// does; blocks past a sequence's context, and every block of a sequence whose
+// prefix is unusable (flagged here), are zero.
+__global__ void gather_split3_kernel(const float *__restrict__ ps, const int32_t *__restrict__ bt,
+                                     const int32_t *__restrict__ prefix,
+                                     const int32_t *__restrict__ cu, uint16_t *__restrict__ C3,
+                                     int32_t *status, int Hk, int Nk, int d, int maxp, int P, int b,
+                                     size_t n) {
+  grid_dep_wait();  // the summaries may come from the previous launch
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = e / d;
+    const int c = (int)(e % d);
+    const int j = (int)(row % Nk);
+    const int ih = (int)(row / Nk);
+    const int h = ih % Hk, i = ih / Hk;
+    const int pre = prefix[i], len = cu[i + 1] - cu[i];
+    float v = 0.f;
+    if (len == 0) {
+      // an idle sequence: no rows
+    } else if (chunk_ok(pre, len, b, Nk)) {
+      if (j < pre / b + (len + b - 1) / b) {
+        const int phys = bt[(size_t)i * maxp + j];
+        if (phys >= 0 && phys < P)
+          v = ps[((size_t)phys * Hk + h) * d + c];
+        else if (c == 0)
+          set_status(status, BSA_ERR_CACHE);
+      }
+    } else if (j == 0 && h == 0 && c == 0) {
+      set_status(status, BSA_ERR_CACHE);
+    }
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    C3[e] = *reinterpret_cast<const uint16_t *>(&hi);
+    C3[n + e] = *reinterpret_cast<const uint16_t *>(&mid);
+    C3[2 * n + e] = *reinterpret_cast<const uint16_t *>(&lo);
+  }
+  grid_dep_launch();
+}
+
+// C == nullptr: a chunk over the paged cache (summaries gathered from it).
 template <int D>
-cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float *S, void *ws,
-                     int32_t *dev_status, cudaStream_t st) {
+cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C,
+                     const bsa_kv_cache_t *cache, float *S, void *ws, int32_t *dev_status,
+                     cudaStream_t st) {
   using Cf = RCfg<D>;
-  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  const int Nk = cache != nullptr ? cache->max_context_blocks : s.max_blocks;
+  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * Nk;
   uint16_t *C3 = static_cast<uint16_t *>(ws);
   const size_t n = rows * D;
-  cudaError_t e0 = launch_dependent(split3_kernel,
-                                    dim3((unsigned)std::min<size_t>((n + 255) / 256, 4096)),
-                                    dim3(256), 0, st, C, C3, n);
+  const dim3 sgrid((unsigned)std::min<size_t>((n + 255) / 256, 4096));
+  cudaError_t e0 =
+      cache != nullptr
+          ? launch_dependent(gather_split3_kernel, sgrid, dim3(256), 0, st, cache->page_summ,
+                             cache->block_table, cache->prefix_lens, s.cu_seqlens, C3,
+                             dev_status, s.num_kv_heads, Nk, D, cache->max_pages_per_req,
+                             cache->num_phys_pages, s.block, n)
+          : launch_dependent(split3_kernel, sgrid, dim3(256), 0, st, C, C3, n);
   if (e0 != cudaSuccess) return e0;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -309,6 +373,8 @@ cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float 
     return cudaErrorInvalidValue;
   RouteTcParams p;
   p.cu = s.cu_seqlens;
+  p.qoff = cache != nullptr ? cache->prefix_lens : nullptr;
+  p.Nk = Nk;
   p.S = S;
   p.status = dev_status;
   p.B = s.num_seqs;
@@ -327,15 +393,17 @@ cudaError_t launch_d(const bsa_shape_t &s, const void *Q, const float *C, float 
 
 }  // namespace
 
-size_t route_tc_workspace_bytes(const bsa_shape_t &s) {
-  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+size_t route_tc_workspace_bytes(const bsa_shape_t &s, const bsa_kv_cache_t *cache) {
+  const int Nk = cache != nullptr ? cache->max_context_blocks : s.max_blocks;
+  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * Nk;
   return ((rows * s.head_dim * 3 * sizeof(uint16_t)) + 255) & ~(size_t)255;
 }
 
-cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C, float *S,
-                                   void *ws, int32_t *dev_status, cudaStream_t st) {
-  if (s.head_dim == 64) return launch_d<64>(s, Q, C, S, ws, dev_status, st);
-  return launch_d<128>(s, Q, C, S, ws, dev_status, st);
+cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C,
+                                   const bsa_kv_cache_t *cache, float *S, void *ws,
+                                   int32_t *dev_status, cudaStream_t st) {
+  if (s.head_dim == 64) return launch_d<64>(s, Q, C, cache, S, ws, dev_status, st);
+  return launch_d<128>(s, Q, C, cache, S, ws, dev_status, st);
 }
 
 }  // namespace bsa

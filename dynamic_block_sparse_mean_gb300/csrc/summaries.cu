@@ -113,7 +113,74 @@ __global__ void page_summaries_append_kernel(const uint16_t *__restrict__ kc,
   ps[row * d + c] = sum / (float)(slot + 1);                 // c = s / r
 }
 
+// Chunked prefill, grid (N_q, B, H_kv): one CTA per (chunk block q, sequence i,
+// KV head h) copies the block's keys and values into its page — block q of the
+// chunk is logical block prefix_i / 64 + q — zeroing the page slots past the
+// chunk's end, and writes the page's key mean and sum ("2.1 · 粗粒度选择" §3.1,
+// eq.(11): a summary is the running sum of the page's keys over their count).
+__global__ void __launch_bounds__(kThreads) chunk_append_kernel(
+    const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
+    const int32_t *__restrict__ cu, const int32_t *__restrict__ prefix,
+    const int32_t *__restrict__ bt, uint16_t *__restrict__ kc, uint16_t *__restrict__ vc,
+    float *__restrict__ ps, float *__restrict__ psum, int32_t *status, int T_tok, int Hk, int d,
+    int maxp, int P, int Nk) {
+  extern __shared__ float red[];
+  grid_dep_wait();  // K and V may come from the previous launch
+  const int q = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
+  const int s0 = cu[i], n = cu[i + 1] - s0;
+  const int lo = q * 64;
+  if (lo >= n) return;
+  const int pre = prefix[i];
+  const int phys = chunk_ok(pre, n, 64, Nk) ? bt[(size_t)i * maxp + pre / 64 + q] : -1;
+  if (phys < 0 || phys >= P) {
+    if (threadIdx.x == 0) set_status(status, BSA_ERR_CACHE);
+    return;
+  }
+  const int nrows = min(64, n - lo);
+  const size_t src = ((size_t)h * T_tok + s0 + lo) * d;
+  const size_t dst = ((size_t)phys * Hk + h) * 64 * d;
+  const int vecs = d / 8, rgroups = kThreads / vecs;
+  const int vec = threadIdx.x % vecs, rg = threadIdx.x / vecs;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int row = rg; row < 64; row += rgroups) {
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+    if (row < nrows) {
+      kv = __ldg(reinterpret_cast<const uint4 *>(K + src + (size_t)row * d) + vec);
+      vv = __ldg(reinterpret_cast<const uint4 *>(V + src + (size_t)row * d) + vec);
+      Vec16<uint16_t>::add(kv, acc);
+    }
+    reinterpret_cast<uint4 *>(kc + dst + (size_t)row * d)[vec] = kv;
+    reinterpret_cast<uint4 *>(vc + dst + (size_t)row * d)[vec] = vv;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rg * d + vec * 8 + e] = acc[e];
+  __syncthreads();
+  float *out = ps + ((size_t)phys * Hk + h) * d;
+  for (int c = threadIdx.x; c < d; c += kThreads) {
+    float sum = 0.f;
+    for (int g = 0; g < rgroups; ++g) sum += red[g * d + c];
+    out[c] = sum / (float)nrows;
+    if (psum != nullptr) psum[((size_t)phys * Hk + h) * d + c] = sum;
+  }
+  grid_dep_launch();
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_append(const bsa_shape_t &s, const bsa_kv_cache_t &c, const void *K,
+                                const void *V, int32_t *dev_status, cudaStream_t st) {
+  const dim3 grid(s.max_blocks, s.num_seqs, s.num_kv_heads);
+  const size_t sm = (size_t)(kThreads / (s.head_dim / 8)) * s.head_dim * sizeof(float);
+  return launch_dependent(chunk_append_kernel, grid, dim3(kThreads), sm, st,
+                          static_cast<const uint16_t *>(K), static_cast<const uint16_t *>(V),
+                          s.cu_seqlens, c.prefix_lens, c.block_table,
+                          static_cast<uint16_t *>(c.k_cache), static_cast<uint16_t *>(c.v_cache),
+                          c.page_summ, c.page_sum, dev_status, s.total_tokens, s.num_kv_heads,
+                          s.head_dim, c.max_pages_per_req, c.num_phys_pages,
+                          c.max_context_blocks);
+}
 
 cudaError_t launch_page_summaries_append(const bsa_decode_shape_t &s, const void *k_cache,
                                          const int32_t *block_table,

@@ -16,18 +16,34 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 
+// Logical block of row (i, h, qb): qb, or in a chunked prefill qb + the blocks
+// cached before the chunk (qoff: cached tokens per sequence); -1 when the row is
+// not one (past the sequence's end, or the sequence's prefix is unusable).
+BSA_DEV int row_block(const int32_t *__restrict__ cu, const int32_t *__restrict__ qoff, int row,
+                      int Nq, int Nk, int Hk, int b, int32_t *dev_status) {
+  const int qb = row % Nq, i = row / (Nq * Hk);
+  const int n = cu[i + 1] - cu[i];
+  if (qb >= (n + b - 1) / b) return -1;
+  if (qoff == nullptr) return qb;
+  const int pre = qoff[i];
+  if (!chunk_ok(pre, n, b, Nk)) {
+    if (qb == 0 && (row / Nq) % Hk == 0) set_status(dev_status, BSA_ERR_CACHE);
+    return -1;
+  }
+  return qb + pre / b;
+}
+
 // Row code: 0 = not a row (past the sequence end); c > 0 = copy c ids from J;
 // -1 = the row holds only its diagonal block (empty row, or a malformed row).
 __global__ void wl_rows_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ counts,
-                               const int32_t *__restrict__ cu, int32_t *__restrict__ code,
-                               int32_t *dev_status, int nrows, int Nq, int Hk, int b, int k_max) {
+                               const int32_t *__restrict__ cu, const int32_t *__restrict__ qoff,
+                               int32_t *__restrict__ code, int32_t *dev_status, int nrows, int Nq,
+                               int Nk, int Hk, int b, int k_max) {
   grid_dep_wait();  // J and counts may come from the previous launch
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
-    const int r = row % Nq, i = row / (Nq * Hk);
-    const int n = cu[i + 1] - cu[i];
-    const int nb = (n + b - 1) / b;
-    if (r >= nb) {
+    const int r = row_block(cu, qoff, row, Nq, Nk, Hk, b, dev_status);
+    if (r < 0) {
       code[row] = 0;
       continue;
     }
@@ -172,15 +188,16 @@ __global__ void __launch_bounds__(kScanThreads) wl_scan_kernel(
 
 __global__ void wl_fill_kernel(const int32_t *__restrict__ J, const int32_t *__restrict__ code,
                                const int32_t *__restrict__ row_ptr, int32_t *__restrict__ col_idx,
-                               int nrows, int Nq, int k_max) {
+                               const int32_t *__restrict__ cu, const int32_t *__restrict__ qoff,
+                               int nrows, int Nq, int Nk, int Hk, int b, int k_max) {
   grid_dep_wait();  // codes and row_ptr come from the previous launches
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
     const int c = code[row];
     if (c == 0) continue;
     int32_t *out = col_idx + row_ptr[row];
-    if (c < 0) {
-      out[0] = row % Nq;
+    if (c < 0) {  // the diagonal: the row's logical block
+      out[0] = row_block(cu, qoff, row, Nq, Nk, Hk, b, nullptr);
       continue;
     }
     const int32_t *Jr = J + (size_t)row * k_max;
@@ -248,19 +265,22 @@ size_t worklist_workspace_bytes(const bsa_shape_t &s, int32_t) {
 cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *J,
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
-                            cudaStream_t st) {
+                            cudaStream_t st, const bsa_kv_cache_t *cache) {
   const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
   int32_t *code = static_cast<int32_t *>(ws);
   const int blocks = min(4 * num_sms(), (nrows + 255) / 256);
+  const int32_t *qoff = cache != nullptr ? cache->prefix_lens : nullptr;
+  const int Nk = cache != nullptr ? cache->max_context_blocks : s.max_blocks;
   cudaError_t e = launch_dependent(wl_rows_kernel, dim3(max(blocks, 1)), dim3(256), 0, st, J,
-                                   counts, s.cu_seqlens, code, dev_status, nrows, s.max_blocks,
-                                   s.num_kv_heads, s.block, k_max);
+                                   counts, s.cu_seqlens, qoff, code, dev_status, nrows,
+                                   s.max_blocks, Nk, s.num_kv_heads, s.block, k_max);
   if (e != cudaSuccess) return e;
   e = launch_dependent(wl_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, code, row_ptr, work,
                        bucket_off, nrows);
   if (e != cudaSuccess) return e;
   return launch_dependent(wl_fill_kernel, dim3(max(blocks, 1)), dim3(256), 0, st, J, code,
-                          row_ptr, col_idx, nrows, s.max_blocks, k_max);
+                          row_ptr, col_idx, s.cu_seqlens, qoff, nrows, s.max_blocks, Nk,
+                          s.num_kv_heads, s.block, k_max);
 }
 
 size_t causal_worklist_capacity(const bsa_shape_t &s) {

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 4
+#define BSA_VERSION 5
 
 typedef enum {
   BSA_OK = 0,
@@ -54,7 +54,10 @@ typedef enum {
   BSA_ERR_INDEX_RANGE = 16,  /* a J entry outside [0, r]                 (device) */
   BSA_ERR_INDEX_ORDER = 17,  /* a J row not strictly increasing          (device) */
   BSA_ERR_COUNT = 18,        /* counts[row] outside [0, k_max]           (device) */
-  BSA_ERR_TIMEOUT = 19       /* a bounded barrier wait ran out           (device) */
+  BSA_ERR_TIMEOUT = 19,      /* a bounded barrier wait ran out           (device) */
+  BSA_ERR_CACHE = 20         /* chunk prefix off the page grid, context past the
+                                block table, or a physical page id outside
+                                [0, num_phys_pages)                      (device) */
 } bsa_status_t;
 
 typedef enum { BSA_BF16 = 0, BSA_FP32 = 1 } bsa_dtype_t;
@@ -337,6 +340,89 @@ bsa_status_t bsa_build_causal_worklist(const bsa_shape_t *shape, int32_t *row_pt
  * ------------------------------------------------------------------------- */
 bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
                           const float *lse_dense, float *C, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Chunked prefill over a paged KV cache — [P2] §3.1 (block summaries are cache
+ *   state kept beside the KV cache and updated as keys arrive, eq.(11); the
+ *   router emits logical block ids that a block table maps to physical pages)
+ *   and §2.2 (routing a query block needs only the summaries of its history).
+ *   A prompt is processed chunk by chunk: each chunk's keys and values are
+ *   appended to the cache with their page summaries (bsa_chunk_append), its query
+ *   blocks are routed against the summaries of every earlier block, cached or in
+ *   the chunk (bsa_route_chunk), and the selected pages are attended
+ *   (bsa_build_worklist_chunk, bsa_attention_chunk).  For every token of the
+ *   chunk the result is that of a single-pass prefill of the whole prompt.
+ *
+ *   Conventions of the calls below:
+ *   - `shape` describes the CHUNK: cu_seqlens over the chunk's packed tokens,
+ *     n_i = tokens sequence i adds (0 allowed), max_blocks = ceil(max n_i / 64);
+ *     dtype BSA_BF16, block 64 (the page size), head_dim 64 or 128.
+ *   - prefix_i = cache->prefix_lens[i] tokens are already cached.  When n_i > 0
+ *     it must be a multiple of 64, so chunk query block q of sequence i is
+ *     logical block r = prefix_i / 64 + q, and ceil((prefix_i + n_i) / 64) <=
+ *     max_context_blocks; a sequence breaking either rule contributes no rows
+ *     and sets BSA_ERR_CACHE in dev_status.  A sequence with n_i = 0 is idle
+ *     (its prefix may end anywhere, e.g. a finished prompt).
+ *   - J, counts, row_ptr and work are indexed by (i, h, q) like a prefill of the
+ *     chunk; J holds logical block ids 0 .. r (routing, forced blocks and union
+ *     parameters exactly as bsa_route with r the logical block).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  void *k_cache;               /* [P, H_kv, 64, d] bf16                                */
+  void *v_cache;               /* [P, H_kv, 64, d] bf16                                */
+  float *page_summ;            /* [P, H_kv, d] fp32 page means c = s / r_p (eq.(11))   */
+  float *page_sum;             /* nullable; [P, H_kv, d] fp32 running sums s (eq.(11)),
+                                  the state bsa_page_summaries_append continues from   */
+  const int32_t *block_table;  /* [B, max_pages_per_req] physical page of each logical
+                                  block of each sequence                              */
+  const int32_t *prefix_lens;  /* [B] tokens cached before this chunk                 */
+  int32_t max_pages_per_req;   /* columns of block_table                              */
+  int32_t num_phys_pages;      /* P                                                   */
+  int32_t max_context_blocks;  /* N_k: >= max_i ceil((prefix_i + n_i) / 64), and
+                                  max_blocks <= N_k <= max_pages_per_req              */
+} bsa_kv_cache_t;
+
+/* Append the chunk's keys and values to their pages and summarise those pages:
+ *   key/value t of sequence i goes to page block_table[i][(prefix_i + t) / 64],
+ *   slot t % 64; slots of the chunk's last page past its end are zeroed.  For
+ *   every page the chunk wrote, page_summ = mean of its keys (and page_sum = their
+ *   sum, when given).  Physical ids outside [0, P) are skipped (BSA_ERR_CACHE).
+ *   K, V : [H_kv, T, d] bf16, the chunk packed as in a prefill.               */
+bsa_status_t bsa_chunk_append(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                              const void *K, const void *V, int32_t *dev_status,
+                              cudaStream_t stream);
+
+/* Route the chunk's query blocks against the cached page summaries (eq.(6),
+ *   eq.(7)): score g[i,h,q,j] = max over the group's query heads and the valid
+ *   tokens of chunk block q of Q . page_summ[block_table[i][j], h] for j < r.
+ *   Q      : [H, T, d] bf16 (the chunk).  J, counts : as bsa_route, rows (i, h, q).
+ *   scores : nullable; [B, H_kv, N_q, N_k] fp32 receives g for j < r.
+ *   ws     : bsa_route_chunk_workspace_size() bytes, 256-byte aligned.        */
+size_t bsa_route_chunk_workspace_size(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                      const bsa_route_params_t *params);
+bsa_status_t bsa_route_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                             const bsa_route_params_t *params, const void *Q, int32_t *J,
+                             int32_t *counts, float *scores, int32_t *dev_status, void *ws,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/* Worklist of a chunk: bsa_build_worklist with row (i, h, q) validated against
+ *   its logical block r (entries in [0, r]; an empty row becomes {r}).
+ *   ws : bsa_worklist_workspace_size(shape, k_max) bytes.                     */
+bsa_status_t bsa_build_worklist_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                      int32_t k_max, const int32_t *J, const int32_t *counts,
+                                      int32_t *row_ptr, int32_t *col_idx, int32_t *work,
+                                      int32_t *bucket_off, int32_t *dev_status, void *ws,
+                                      size_t ws_bytes, cudaStream_t stream);
+
+/* Sparse attention of the chunk's queries over the selected pages (eqs.(1)-(5)
+ *   as bsa_attention_fwd; the causal mask inside the diagonal block r).  K and V
+ *   tiles are read from the cache pages the block table names.
+ *   Q, O : [H, T, d] bf16 (the chunk);  lse : [H, T] fp32 (nullable).         */
+bsa_status_t bsa_attention_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
+                                 const void *Q, const int32_t *row_ptr, const int32_t *col_idx,
+                                 const int32_t *work, const int32_t *bucket_off,
+                                 float softmax_scale, void *O, float *lse, int32_t *dev_status,
+                                 cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status_t status);
