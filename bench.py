@@ -53,6 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
+    ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill leg")
     ap.add_argument("--no-quality", action="store_true",
                     help="skip the coverage / planted-recall / density-1 leg")
     ap.add_argument("--decode-only", action="store_true",
@@ -240,7 +241,7 @@ def bench_prefill(w, steps, warmup, device, world, sampler):
     eff = accounting.effective_pairs(J, counts, x.cu_seqlens, w.block, G) * 4.0 * w.head_dim
     tiles = counts[counts > 0]
     launches = sum(bsa.PrefillPlan.LAUNCHES.values()) * steps
-    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, stages=st, flops=flops,
+    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, steps=steps, stages=st, flops=flops,
                eff_flops=eff, clocks=clocks, launches=launches, T=T,
                tiles={"min": int(tiles.min()), "mean": float(tiles.mean()), "max": int(tiles.max()),
                       "total": int(counts.sum())},
@@ -336,6 +337,69 @@ def bench_backward(res, w, device, reps=3):
             "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak,
                          "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x 2070 MHz"}}
+
+
+def bench_chunked(res, w, device, chunk_tokens=8192, reps=3):
+    """Outside the timed loop: the same prompt batch as a chunked prefill over a
+    paged KV cache whose pages sit in a random physical order.  Each step every
+    sequence appends up to chunk_tokens tokens (bsa_chunk_append), routes them
+    against the cached page summaries (bsa_route_chunk), and attends the selected
+    pages (bsa_build_worklist_chunk, bsa_attention_chunk).  Reports the whole
+    prompt's time over all chunks, TFLOP/s on the single-pass tile count, and
+    whether the chunked index equals the single-pass one."""
+    import dynamic_block_sparse_mean_gb300 as bsa
+    if w.block != 64:
+        return {"skipped": f"chunks use 64-token pages; this workload's block is {w.block}"}
+    x, q, k, v, plan = res["x"], res["q"], res["k"], res["v"], res["plan"]
+    cu = np.asarray(x.cu_seqlens, dtype=np.int64)
+    lens = np.diff(cu)
+    pages = (lens + 63) // 64
+    perm = np.random.default_rng(2024).permutation(int(pages.sum()))
+    bt = np.full((len(lens), int(pages.max())), -1, dtype=np.int32)
+    off = 0
+    for i, L in enumerate(pages):
+        bt[i, :L] = perm[off:off + L]
+        off += int(L)
+    cache = bsa.PagedKVCache.allocate(len(perm), w.num_kv_heads, w.head_dim, bt, device=device)
+    nsteps = int((lens.max() + chunk_tokens - 1) // chunk_tokens)
+    steps = []
+    for s in range(nsteps):
+        pre = np.minimum(s * chunk_tokens, lens)
+        n = np.minimum(chunk_tokens, lens - pre)
+        idx = np.concatenate([np.arange(cu[i] + pre[i], cu[i] + pre[i] + n[i])
+                              for i in range(len(lens))])
+        ti = torch.as_tensor(idx, device=device)
+        chunk = bsa.Chunk.make(pre, n, w.num_heads, w.num_kv_heads, w.head_dim, device=device,
+                               max_context_blocks=int(pages.max()))
+        steps.append((bsa.ChunkPlan(chunk, cache, plan.params, device=device), pre, n,
+                      q[:, ti].contiguous(), k[:, ti].contiguous(), v[:, ti].contiguous()))
+    for cp, _, _, qc, kc, vc in steps:
+        cp.run(qc, kc, vc)
+    torch.cuda.synchronize(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        for cp, _, _, qc, kc, vc in steps:
+            cp.run(qc, kc, vc)
+    t1.record()
+    torch.cuda.synchronize(device)
+    for cp, *_ in steps:
+        bsa.check_status(cp.status)
+    ms = t0.elapsed_time(t1) / reps
+    J1, c1 = plan.J.cpu().numpy(), plan.counts.cpu().numpy()
+    same = True
+    for cp, pre, n, *_ in steps:
+        Jc, cc = cp.J.cpu().numpy(), cp.counts.cpu().numpy()
+        for i in range(len(lens)):
+            nq, r0 = int((n[i] + 63) // 64), int(pre[i] // 64)
+            same &= bool(np.array_equal(cc[i, :, :nq], c1[i, :, r0:r0 + nq]) and
+                         np.array_equal(Jc[i, :, :nq], J1[i, :, r0:r0 + nq]))
+    del steps, cache
+    return {"chunk_tokens": chunk_tokens, "chunks": nsteps, "ms": ms,
+            "tflops": res["flops"] / (ms * 1e-3) / 1e12,
+            "single_pass_ms": res["total_ms"] / res["steps"],
+            "index_equals_single_pass": same,
+            "launches_per_prompt": nsteps * sum(bsa.ChunkPlan.LAUNCHES.values())}
 
 
 def bench_e2e(res, steps, device):
@@ -538,6 +602,7 @@ def run_native(args):
                 "compulsory_bytes_per_launch": res["attn_bytes"]}
     quality = router_quality(res, w, device) if not args.no_quality else None
     backward = bench_backward(res, w, device) if not args.no_backward else None
+    chunked = bench_chunked(res, w, device) if not args.no_chunked else None
     e2e = None
     if not args.no_e2e:
         e_ms, bi, bo = bench_e2e(res, max(3, min(args.steps, 20)), device)
@@ -580,6 +645,7 @@ def run_native(args):
         "decode": dec,
         "router_quality": quality,
         "backward": backward,
+        "chunked_prefill": chunked,
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }

@@ -103,3 +103,45 @@ def test_host_side_argument_errors(lib):
                                 ctypes.c_void_p(16), null, ctypes.c_void_p(16), ctypes.c_void_p(16),
                                 null, null, 0, null) == 2
     assert lib.bsa_decode_workspace_size(ctypes.byref(ds)) > 0
+
+
+def test_chunk_calls_reject_bad_cache_descriptors(lib):
+    null, p16 = None, ctypes.c_void_p(16)
+    s = _shape()                                            # block 64, d 64, bf16, N_q 16
+
+    def cache(**kw):
+        base = dict(k_cache=16, v_cache=16, page_summ=16, page_sum=None, block_table=16,
+                    prefix_lens=16, max_pages_per_req=32, num_phys_pages=100,
+                    max_context_blocks=16)
+        base.update(kw)
+        return _lib.KVCache(**base)
+
+    def append(sh, c):
+        return lib.bsa_chunk_append(ctypes.byref(sh), ctypes.byref(c), p16, p16, p16, null)
+
+    assert append(s, cache(prefix_lens=None)) == 1
+    assert append(s, cache(max_context_blocks=15)) == 1       # below the chunk's N_q
+    assert append(s, cache(max_context_blocks=33)) == 1       # past the block table
+    assert append(_shape(dtype=1), cache()) == 2              # the cache is bf16
+    assert append(_shape(block=128, max_blocks=8), cache()) == 2   # page = block = 64
+    assert append(s, cache(num_phys_pages=1 << 26)) == 2      # page rows past int32
+    assert append(s, cache(k_cache=24)) == 1                  # 16-byte alignment
+    assert lib.bsa_chunk_append(ctypes.byref(s), ctypes.byref(cache()), p16, p16, null,
+                                null) == 1                    # dev_status missing
+    p = _lib.RouteParams(0, 4, 0, 0.0, 0, 1, 0, None)
+    c = cache()
+    need = lib.bsa_route_chunk_workspace_size(ctypes.byref(s), ctypes.byref(c), ctypes.byref(p))
+    split = (1 * 2 * 16 * 64 * 3 * 2 + 255) // 256 * 256
+    assert need == split + 1 * 2 * 16 * 16 * 4
+    args = [p16] * 4
+    assert lib.bsa_route_chunk(ctypes.byref(s), ctypes.byref(c), ctypes.byref(p), *args, p16,
+                               null, 0, null) == 3
+    bad_p = _lib.RouteParams(0, 300, 0, 0.0, 0, 1, 0, None)
+    assert lib.bsa_route_chunk(ctypes.byref(s), ctypes.byref(c), ctypes.byref(bad_p), *args, p16,
+                               p16, 1 << 20, null) == 2
+    wl = [p16] * 7
+    assert lib.bsa_build_worklist_chunk(ctypes.byref(s), ctypes.byref(c), 4, *wl, null, 0,
+                                        null) == 3
+    a = [p16] * 5
+    assert lib.bsa_attention_chunk(ctypes.byref(s), ctypes.byref(c), *a, ctypes.c_float(0.0), p16,
+                                   null, null, null) == 1     # dev_status missing
