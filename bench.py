@@ -241,8 +241,8 @@ def bench_prefill(w, steps, warmup, device, world, sampler):
     eff = accounting.effective_pairs(J, counts, x.cu_seqlens, w.block, G) * 4.0 * w.head_dim
     tiles = counts[counts > 0]
     launches = sum(bsa.PrefillPlan.LAUNCHES.values()) * steps
-    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, steps=steps, stages=st, flops=flops,
-               eff_flops=eff, clocks=clocks, launches=launches, T=T,
+    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, steps=steps, stages=st,
+               flops=flops, eff_flops=eff, clocks=clocks, launches=launches, T=T,
                tiles={"min": int(tiles.min()), "mean": float(tiles.mean()), "max": int(tiles.max()),
                       "total": int(counts.sum())},
                router_flops=accounting.router_flops(x.cu_seqlens, w.block, w.num_heads, w.head_dim),
