@@ -304,9 +304,10 @@ def router_quality(res, w, device):
 
 def bench_backward(res, w, device, reps=3):
     """Outside the timed loop: the backward (bsa_attention_bwd) on the forward's
-    worklist and lse with a seeded upstream gradient; FLOPs are 2.5x the forward's
-    tile count (recomputed QK^T, dP = dO V^T, dV, dQ, dK: five b x b x d products
-    per tile against the forward's two)."""
+    worklist and lse with a seeded upstream gradient; algorithmic FLOPs are 2.5x the
+    forward's tile count (recomputed QK^T, dP = dO V^T, dV, dQ, dK: five b x b x d
+    products per tile against the forward's two).  The tensor-core path executes
+    seven (its dQ and dK / dV passes each recompute QK^T and dO V^T)."""
     import dynamic_block_sparse_mean_gb300 as bsa
     plan, q, k, v = res["plan"], res["q"], res["k"], res["v"]
     plan.attend(q, k, v)
@@ -329,11 +330,18 @@ def bench_backward(res, w, device, reps=3):
     ms = t0.elapsed_time(t1) / reps
     flops = 2.5 * res["flops"]
     tf = flops / (ms * 1e-3) / 1e12
+    del dq, dk, dv, ws, do
+    if w.head_dim == 128:  # the tensor-core path (BF16, head_dim 128)
+        peaks, src = measured_peaks()
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        return {"ms": ms, "tflops": tf, "flops_per_call": flops, "path": "tcgen05",
+                "executed_flops_per_call": 3.5 * res["flops"],
+                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                             "frac": tf / peak, "peak_source": f"{src} bf16 burst"}}
     # FP32 FFMA peak: 152 SMs x 128 lanes x 2 FLOP x the maximum SM clock
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     peak = sms * 128 * 2 * 2.07e9 / 1e12
-    del dq, dk, dv, ws, do
-    return {"ms": ms, "tflops": tf, "flops_per_call": flops,
+    return {"ms": ms, "tflops": tf, "flops_per_call": flops, "path": "simt",
             "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak,
                          "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x 2070 MHz"}}

@@ -208,7 +208,7 @@ def attention_fwd(q, k, v, wl: Worklist, shape: PrefillShape, dev_status, scale:
 
 
 def attention_bwd(q, k, v, o, do, lse, wl: Worklist, shape: PrefillShape, scale: float = 0.0,
-                  dq=None, dk=None, dv=None, ws=None):
+                  dq=None, dk=None, dv=None, ws=None, dev_status=None):
     """dQ, dK, dV of the sparse attention for the upstream gradient do, reusing the
     forward's worklist and lse (bsa_attention_bwd)."""
     dq = torch.empty_like(q) if dq is None else dq
@@ -218,10 +218,12 @@ def attention_bwd(q, k, v, o, do, lse, wl: Worklist, shape: PrefillShape, scale:
     if ws is None:
         n = int(_lib.lib().bsa_attention_bwd_workspace_size(ctypes.byref(s)))
         ws = torch.empty(max(256, n), dtype=torch.uint8, device=q.device)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
     check("bsa_attention_bwd", _lib.lib().bsa_attention_bwd(
         ctypes.byref(s), _p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(wl.row_ptr),
         _p(wl.col_idx), _p(wl.work), _p(wl.bucket_off), float(scale), _p(dq), _p(dk), _p(dv),
-        _p(ws), ws.numel(), _stream()))
+        _p(dev_status), _p(ws), ws.numel(), _stream()))
     return dq, dk, dv
 
 

@@ -73,7 +73,7 @@ PROTOTYPES = {
     "bsa_attention_fwd": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, V, V, F32, V, V, V, V]),
     "bsa_attention_bwd_workspace_size": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_attention_bwd": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, V, V, V, V, V, F32, V, V, V,
-                                V, SZ, V]),
+                                V, V, SZ, V]),
     "bsa_causal_worklist_capacity": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),

@@ -197,19 +197,28 @@ bsa_status_t bsa_attention_bwd(const bsa_shape_t *shape, const void *Q, const vo
                                const void *V, const void *O, const void *dO, const float *lse,
                                const int32_t *row_ptr, const int32_t *col_idx,
                                const int32_t *work, const int32_t *bucket_off,
-                               float softmax_scale, void *dQ, void *dK, void *dV, void *ws,
-                               size_t ws_bytes, cudaStream_t stream) {
+                               float softmax_scale, void *dQ, void *dK, void *dV,
+                               int32_t *dev_status, void *ws, size_t ws_bytes,
+                               cudaStream_t stream) {
   if (!shape_ok(shape) || Q == nullptr || K == nullptr || V == nullptr || O == nullptr ||
       dO == nullptr || lse == nullptr || row_ptr == nullptr || col_idx == nullptr ||
       work == nullptr || bucket_off == nullptr || dQ == nullptr || dK == nullptr ||
-      dV == nullptr)
+      dV == nullptr || dev_status == nullptr)
     return BSA_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ))
+    return BSA_ERR_INVALID_ARG;
+  if (bsa::attention_bwd_tc_supported(*shape) &&
+      bsa::causal_worklist_capacity(*shape) > (size_t)INT32_MAX)
+    return BSA_ERR_UNSUPPORTED;
   if (ws == nullptr || ws_bytes < bsa::attention_bwd_workspace_bytes(*shape))
     return BSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return BSA_ERR_INVALID_ARG;
   const float scale =
       softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)shape->head_dim);
   return launched(bsa::launch_attention_bwd(*shape, Q, K, V, O, dO, lse, row_ptr, col_idx, work,
-                                            bucket_off, scale, dQ, dK, dV, ws, stream));
+                                            bucket_off, scale, dQ, dK, dV, ws, dev_status,
+                                            stream));
 }
 
 size_t bsa_causal_worklist_capacity(const bsa_shape_t *shape) {

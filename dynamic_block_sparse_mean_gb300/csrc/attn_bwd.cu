@@ -259,10 +259,14 @@ cudaError_t launch_bwd_typed(const bsa_shape_t &s, const void *Q, const void *K,
 
 }  // namespace
 
+// Workspace: D = rowsum(dO * O) [H, T] fp32, then the tensor-core path's key-major
+// index (BF16, head_dim 128) or the SIMT path's fp32 dK / dV accumulators.
 size_t attention_bwd_workspace_bytes(const bsa_shape_t &s) {
   const size_t hrows = (size_t)s.num_heads * s.total_tokens;
   const size_t kv = (size_t)s.num_kv_heads * s.total_tokens * s.head_dim;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  if (attention_bwd_tc_supported(s))
+    return up(hrows * sizeof(float)) + attention_bwd_tc_index_bytes(s);
   return up(hrows * sizeof(float)) + 2 * up(kv * sizeof(float));
 }
 
@@ -270,7 +274,21 @@ cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void
                                  const void *V, const void *O, const void *dO, const float *lse,
                                  const int32_t *row_ptr, const int32_t *col_idx,
                                  const int32_t *work, const int32_t *bucket_off, float scale,
-                                 void *dQ, void *dK, void *dV, void *ws, cudaStream_t st) {
+                                 void *dQ, void *dK, void *dV, void *ws, int32_t *dev_status,
+                                 cudaStream_t st) {
+  if (attention_bwd_tc_supported(s)) {
+    const size_t hrows = (size_t)s.num_heads * s.total_tokens;
+    float *Dv = static_cast<float *>(ws);
+    const int grid = std::max(1, std::min(8 * num_sms(), (int)((hrows * 32 + 255) / 256)));
+    bwd_dot_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t *>(O),
+                                                   static_cast<const uint16_t *>(dO), Dv, hrows,
+                                                   s.head_dim);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    void *index_ws = static_cast<char *>(ws) + ((hrows * sizeof(float) + 255) & ~(size_t)255);
+    return launch_attention_bwd_tc(s, Q, K, V, dO, lse, Dv, row_ptr, col_idx, work, bucket_off,
+                                   scale, dQ, dK, dV, index_ws, dev_status, st);
+  }
   if (s.dtype == BSA_BF16)
     return launch_bwd_typed<uint16_t>(s, Q, K, V, O, dO, lse, row_ptr, col_idx, work, bucket_off,
                                       scale, dQ, dK, dV, ws, st);

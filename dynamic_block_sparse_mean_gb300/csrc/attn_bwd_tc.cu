@@ -1,0 +1,625 @@
+// Backward of the sparse attention on the tensor cores (BF16, head_dim 128): the
+// same gradients as the SIMT path ("2.1 · 粗粒度选择" §2.2: training reuses the
+// forward's index and softmax statistics; the forward of §1.2 eqs.(1)-(5)), as
+// tcgen05 MMAs on 64-key tiles with fp32 accumulators in TMEM:
+//   S = Q K^T,  dP = dO V^T                     (M = 128 query rows, N = 64 keys)
+//   P = exp(S * scale - lse),  dS = P (dP - D),  D = rowsum(dO * O)
+//   dQ  = scale * dS K       (query-major pass, M = 128 query rows, N = d)
+//   dV^T = dO^T P,  dK^T = scale * Q^T dS   (key-major pass, M = d = 128, N = 64 keys)
+// Two passes so that every output element has one writer and no atomics touch the
+// gradients: the dQ pass walks the forward's worklist (row -> its key blocks); the
+// dK / dV pass walks the transposed index (key block -> the rows that selected
+// it), built here by a count, a scan and an atomic fill.  Both passes recompute S
+// and dP.  Masks are the forward's: the causal triangle inside the diagonal block
+// and query rows past the sequence end or past the KV-head group.
+//
+// Operands sit in shared memory in the 128-byte-swizzled layout TMA writes: a
+// tile of R rows x 64 bf16 columns is R rows of 128 bytes, 16-byte chunk c of row
+// p at p * 128 + ((c ^ (p & 7)) << 4).  Q / dO / K / V tiles come by TMA; P and dS
+// are written by the softmax warps in the same layout, which serves both as a
+// K-major operand (dS of dQ = dS K) and as an MN-major one (P, dS of the
+// key-major products, and K / Q / dO read transposed).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace bsa {
+namespace {
+
+constexpr int kD = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// kind::f16 instruction descriptors: S / dP (A, B K-major, N = 64 keys); dQ
+// (A = dS K-major, B = K MN-major, N = d); dV^T / dK^T (A, B both MN-major).
+constexpr uint32_t kIdescS = idesc_bf16(128, 64, false);
+constexpr uint32_t kIdescDQ = idesc_bf16(128, kD, true);
+constexpr uint32_t kIdescKV = idesc_bf16(128, 64, true) | (1u << 15);
+
+struct BwdTcParams {
+  const int32_t *cu;
+  const int32_t *row_ptr;
+  const int32_t *col_idx;
+  const int32_t *work;
+  const int32_t *bucket_off;
+  const int32_t *kt_ptr;     // key-major index: rows of key block kb at kt_rows[kt_ptr[kb] ..)
+  const int32_t *kt_rows;
+  const int32_t *kt_work;    // key blocks with rows, longest list first
+  const int32_t *kt_bucket;  // kt_bucket[7] = number of such key blocks
+  const float *lse;
+  const float *Dv;
+  uint16_t *dQ;
+  uint16_t *dK;
+  uint16_t *dV;
+  int32_t *status;
+  int T, Hk, G, Nq, mtiles;
+  float scale, scale_log2;
+};
+
+// Row rho of an M-tile of 128 query rows of work row (r, h): rows are the group's
+// G heads x b tokens in that order (the TMA box of Q loads 128 / b heads of b
+// tokens), so tile t, row rho is head h*G + (t*128 + rho) / b, token (..) % b.
+struct QRow {
+  bool valid;    // a query of the sequence inside the group
+  int tok;       // token within the query block
+  size_t idx;    // (head, token) index into [H, T]
+};
+
+template <int BK>
+BSA_DEV QRow qrow(const BwdTcParams &p, int t, int rho, int h, int r, int s0, int n) {
+  QRow q;
+  const int grow = t * 128 + rho;
+  q.tok = grow % BK;
+  q.valid = grow < p.G * BK && r * BK + q.tok < n;
+  q.idx = (size_t)(h * p.G + grow / BK) * p.T + s0 + r * BK + q.tok;
+  return q;
+}
+
+// P and dS of 32 keys of one query row (keys key0 .. key0 + 31 of the block),
+// packed as bf16 pairs; keys past the query on the diagonal, and invalid rows, are 0.
+BSA_DEV void softmax_grad32(const uint32_t (&s)[32], const uint32_t (&dp)[32], bool valid,
+                            bool diag, int key0, int tok, float scale_log2, float lse2, float Drow,
+                            uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float pr[2], ds[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const bool ok = valid && (!diag || key0 + c + e <= tok);
+      pr[e] = ok ? fast_exp2(__uint_as_float(s[c + e]) * scale_log2 - lse2) : 0.f;
+      ds[e] = pr[e] * (__uint_as_float(dp[c + e]) - Drow);
+    }
+    pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
+    dk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+  }
+}
+
+// Four 16-byte chunks (half h of a 128-byte row) into the swizzled tile.
+BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = half * 4 + q;
+    st_shared_v4(base + rho * 128 + ((c ^ (rho & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                 v[4 * q + 3]);
+  }
+}
+
+// S = X Y^T for one 128-row X tile (two 16 KB panels) and one 64-row Y tile
+// (two 8 KB panels), K = d.
+BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk)
+    mma_bf16_ss(d_tmem, sdesc_sw128(x + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                sdesc_sw128(y + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), kIdescS,
+                kk > 0 ? 1u : 0u);
+}
+
+// ---------------------------------------------------------------- key-major index
+
+// Count, per key block, the rows that selected it (entries outside [0, r] skipped).
+__global__ void kt_count_kernel(const int32_t *__restrict__ row_ptr,
+                                const int32_t *__restrict__ col_idx, int nrows, int Nq,
+                                int32_t *__restrict__ cnt) {
+  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
+       row += gridDim.x * blockDim.x) {
+    const int r = row % Nq, base = row - r;
+    for (int e = row_ptr[row]; e < row_ptr[row + 1]; ++e) {
+      const int j = col_idx[e];
+      if (j >= 0 && j <= r) atomicAdd(cnt + base + j, 1);
+    }
+  }
+}
+
+__global__ void kt_fill_kernel(const int32_t *__restrict__ row_ptr,
+                               const int32_t *__restrict__ col_idx, int nrows, int Nq,
+                               const int32_t *__restrict__ kt_ptr, int32_t *__restrict__ cursor,
+                               int32_t *__restrict__ kt_rows) {
+  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
+       row += gridDim.x * blockDim.x) {
+    const int r = row % Nq, base = row - r;
+    for (int e = row_ptr[row]; e < row_ptr[row + 1]; ++e) {
+      const int j = col_idx[e];
+      if (j < 0 || j > r) continue;
+      const int pos = atomicAdd(cursor + base + j, 1);
+      kt_rows[kt_ptr[base + j] + pos] = r;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dQ pass
+
+// One CTA per (work row, M-tile): Q and dO of the tile stay in shared memory;
+// every 64-key tile of the row's blocks comes in by TMA, S and dP go to TMEM,
+// four warps (one query row per thread) turn them into dS in shared memory, and
+// dQ += dS K accumulates in TMEM.  Shared memory (96 KB) and TMEM (256 columns)
+// let two CTAs share an SM.  Warp 4 lane 0 issues the copies and the MMAs.
+namespace dq {
+constexpr int kThreads = 160;
+constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = 81920;  // dS reuses V
+constexpr int kOffBar = 98304;
+constexpr int B_QFULL = 0, B_KVFULL = 1, B_SFULL = 2, B_DSFULL = 3, B_KVFREE = 4, B_DQFULL = 5;
+constexpr int kOffCtl = kOffBar + 64;
+constexpr int kSmemBytes = kOffCtl + 16 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 256;
+}  // namespace dq
+
+template <int BK>
+__global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    const BwdTcParams p) {
+  using namespace dq;
+  constexpr int KT = BK / 64;  // 64-key tiles per block
+  const int u = blockIdx.x;
+  if (u >= __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.mtiles) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (sbase - raw);
+  auto bar = [&](int k) { return sbase + kOffBar + 8u * (uint32_t)k; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffCtl);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + kOffCtl + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_KVFULL), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_DSFULL), 4);
+    mbar_init(bar(B_KVFREE), 1);
+    mbar_init(bar(B_DQFULL), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int t = u % p.mtiles;
+  const int row = __ldg(p.work + u / p.mtiles);
+  const int r = row % p.Nq, h = (row / p.Nq) % p.Hk, i = row / (p.Nq * p.Hk);
+  const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
+  const int kv0 = __ldg(p.row_ptr + row), nsteps = (__ldg(p.row_ptr + row + 1) - kv0) * KT;
+  const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
+                 smV = sbase + kOffV;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      bool ok = true;
+      int kv_issued = -1;
+      const int hq0 = h * p.G + (t * 128) / BK;
+      mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
+      for (int pn = 0; pn < 2; ++pn) {
+        tma_load_3d(smQ + pn * 16384, &tmQ, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
+        tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
+      }
+      for (int s = 0; ok && s < nsteps; ++s) {
+        const int j = __ldg(p.col_idx + kv0 + s / KT);
+        const int y = s0 + j * BK + (s % KT) * 64;
+        if (s > 0 && !(ok = mbar_wait(bar(B_KVFREE), (s - 1) & 1, abort_flag, p.status))) break;
+        mbar_arrive_expect_tx(bar(B_KVFULL), 4 * 8192);
+        kv_issued = s & 1;
+        for (int pn = 0; pn < 2; ++pn) {
+          tma_load_3d(smK + pn * 8192, &tmK, bar(B_KVFULL), pn * 64, y, h);
+          tma_load_3d(smV + pn * 8192, &tmV, bar(B_KVFULL), pn * 64, y, h);
+        }
+        if (!(ok = mbar_wait(bar(B_KVFULL), s & 1, abort_flag, p.status))) break;
+        kv_issued = -1;
+        if (s == 0 && !(ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status))) break;
+        tc_fence_after();
+        mma_xyT(tmem + kColS, smQ, smK);
+        mma_xyT(tmem + kColDP, smDO, smV);
+        mma_commit(bar(B_SFULL));
+        if (!(ok = mbar_wait(bar(B_DSFULL), s & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K: 64 keys in steps of 16
+          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(smV + kk * 32, 16, 1024),
+                      sdesc_sw128(smK + kk * 2048, 8192, 1024), kIdescDQ,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_KVFREE));
+      }
+      mma_commit(bar(B_DQFULL));
+      if (!ok) {  // copies in flight land before the CTA leaves
+        mbar_wait_drain(bar(B_QFULL), 0);
+        if (kv_issued >= 0) mbar_wait_drain(bar(B_KVFULL), kv_issued);
+      }
+      mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int rho = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
+    const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
+    const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      const int j = __ldg(p.col_idx + kv0 + s / KT);
+      const bool diag = j == r;
+      if (!(ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32], dr[32], pk[16], dk[16];
+        tmem_ld32(tmem + lane_base + kColS + half * 32, sr);
+        tmem_ld32(tmem + lane_base + kColDP + half * 32, dr);
+        softmax_grad32(sr, dr, q.valid, diag, (s % KT) * 64 + half * 32, q.tok, p.scale_log2,
+                       lse2, Drow, pk, dk);
+        st_row_half(smV, rho, half, dk);  // V was consumed by dP; dS takes its place
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+    }
+    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
+      tc_fence_after();
+      uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD);
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + kColDQ + c0, rr);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          o[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale,
+                             __uint_as_float(rr[2 * e + 1]) * p.scale);
+        if (q.valid)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[c0 / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- dK / dV pass
+
+// One CTA per (key block, 64-key tile): K and V of the tile stay in shared memory;
+// the query tiles of every row that selected the block stream through a two-stage
+// ring (Q and dO); S and dP of tile n land in one of two TMEM buffers while the
+// softmax warps work on tile n-1, which then feeds dV^T += dO^T P and
+// dK^T += Q^T dS.  192 threads: warps 0-3 softmax and epilogue, warp 4 TMA,
+// warp 5 MMA.  One CTA per SM (192 KB of shared memory, all of TMEM).
+namespace kv {
+constexpr int kThreads = 192;
+constexpr int kOffK = 0, kOffV = 16384, kOffQ = 32768, kOffDO = kOffQ + 2 * 32768;
+constexpr int kOffP = kOffDO + 2 * 32768, kOffDS = kOffP + 16384;
+constexpr int kOffBar = kOffDS + 16384;
+constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_SFREE = 7;
+constexpr int B_PDSFULL = 9, B_PDSFREE = 10, B_DONE = 11;
+constexpr int kOffCtl = kOffBar + 12 * 8;
+constexpr int kSmemBytes = kOffCtl + 16 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kTmemCols = 512;
+}  // namespace kv
+
+template <int BK>
+__global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    const BwdTcParams p) {
+  using namespace kv;
+  constexpr int KT = BK / 64;
+  const int u = blockIdx.x;
+  if (u >= __ldg(p.kt_bucket + BSA_NUM_BUCKETS) * KT) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (sbase - raw);
+  auto bar = [&](int k) { return sbase + kOffBar + 8u * (uint32_t)k; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffCtl);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + kOffCtl + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_KVFULL), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_QFULL + b), 1);
+      mbar_init(bar(B_QEMPTY + b), 1);
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_SFREE + b), 4);
+    }
+    mbar_init(bar(B_PDSFULL), 4);
+    mbar_init(bar(B_PDSFREE), 1);
+    mbar_init(bar(B_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int e = u % KT;
+  const int kb = __ldg(p.kt_work + u / KT);  // (i * H_kv + h) * N_q + j
+  const int j = kb % p.Nq, h = (kb / p.Nq) % p.Hk, i = kb / (p.Nq * p.Hk);
+  const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
+  const int l0 = __ldg(p.kt_ptr + kb), ntiles = (__ldg(p.kt_ptr + kb + 1) - l0) * p.mtiles;
+  const int key_row = s0 + j * BK + e * 64;  // first key of the tile in the packed K / V
+  const uint32_t smK = sbase + kOffK, smV = sbase + kOffV, smQ = sbase + kOffQ,
+                 smDO = sbase + kOffDO, smP = sbase + kOffP, smDS = sbase + kOffDS;
+  auto row_of = [&](int nt) { return __ldg(p.kt_rows + l0 + nt / p.mtiles); };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      int issued[2] = {-1, -1};
+      mbar_arrive_expect_tx(bar(B_KVFULL), 4 * 8192);
+      for (int pn = 0; pn < 2; ++pn) {
+        tma_load_3d(smK + pn * 8192, &tmK, bar(B_KVFULL), pn * 64, key_row, h);
+        tma_load_3d(smV + pn * 8192, &tmV, bar(B_KVFULL), pn * 64, key_row, h);
+      }
+      for (int nt = 0; nt < ntiles; ++nt) {
+        const int st = nt & 1;
+        if (nt >= 2 && !(ok = mbar_wait(bar(B_QEMPTY + st), ((nt - 2) >> 1) & 1, abort_flag,
+                                        p.status)))
+          break;
+        const int r = row_of(nt), t = nt % p.mtiles;
+        const int hq0 = h * p.G + (t * 128) / BK;
+        mbar_arrive_expect_tx(bar(B_QFULL + st), 4 * 16384);
+        issued[st] = (nt >> 1) & 1;
+        for (int pn = 0; pn < 2; ++pn) {
+          tma_load_3d(smQ + st * 32768 + pn * 16384, &tmQ, bar(B_QFULL + st), pn * 64,
+                      s0 + r * BK, hq0);
+          tma_load_3d(smDO + st * 32768 + pn * 16384, &tmDO, bar(B_QFULL + st), pn * 64,
+                      s0 + r * BK, hq0);
+        }
+      }
+      // every copy issued lands before the CTA leaves (on the normal path the MMA
+      // warp has consumed them all; after an abort this waits out the flights)
+      mbar_wait_drain(bar(B_KVFULL), 0);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] >= 0) mbar_wait_drain(bar(B_QFULL + st), issued[st]);
+      (void)ok;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
+      auto kv_products = [&](int nt) {  // dV^T += dO^T P, dK^T += Q^T dS of tile nt
+        const int st = nt & 1;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 128 query rows in steps of 16
+          const uint32_t acc = (nt > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smDO + st * 32768 + kk * 2048, 16384, 1024),
+                      sdesc_sw128(smP + kk * 2048, 16384, 1024), kIdescKV, acc);
+          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smQ + st * 32768 + kk * 2048, 16384, 1024),
+                      sdesc_sw128(smDS + kk * 2048, 16384, 1024), kIdescKV, acc);
+        }
+        mma_commit(bar(B_QEMPTY + st));
+        mma_commit(bar(B_PDSFREE));
+      };
+      for (int nt = 0; ok && nt < ntiles; ++nt) {
+        const int b = nt & 1;
+        if (!(ok = mbar_wait(bar(B_QFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
+        if (nt >= 2 &&
+            !(ok = mbar_wait(bar(B_SFREE + b), ((nt - 2) >> 1) & 1, abort_flag, p.status)))
+          break;
+        tc_fence_after();
+        mma_xyT(tmem + kColS + 64 * b, smQ + b * 32768, smK);
+        mma_xyT(tmem + kColDP + 64 * b, smDO + b * 32768, smV);
+        mma_commit(bar(B_SFULL + b));
+        if (nt >= 1) {
+          if (!(ok = mbar_wait(bar(B_PDSFULL), (nt - 1) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          kv_products(nt - 1);
+        }
+      }
+      if (ok && ntiles > 0 &&
+          (ok = mbar_wait(bar(B_PDSFULL), (ntiles - 1) & 1, abort_flag, p.status))) {
+        tc_fence_after();
+        kv_products(ntiles - 1);
+      }
+      mma_commit(bar(B_DONE));
+      mbar_wait_drain(bar(B_DONE), 0);  // MMAs done before TMEM is freed
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int rho = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    for (int nt = 0; nt < ntiles; ++nt) {
+      const int b = nt & 1;
+      const int r = row_of(nt), t = nt % p.mtiles;
+      const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
+      const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
+      const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
+      const bool diag = r == j;
+      if (!(ok = mbar_wait(bar(B_SFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
+      // P / dS of the previous tile have been consumed by its dK / dV products
+      if (nt >= 1 && !(ok = mbar_wait(bar(B_PDSFREE), (nt - 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32], dr[32], pk[16], dk[16];
+        tmem_ld32(tmem + lane_base + kColS + 64 * b + half * 32, sr);
+        tmem_ld32(tmem + lane_base + kColDP + 64 * b + half * 32, dr);
+        softmax_grad32(sr, dr, q.valid, diag, e * 64 + half * 32, q.tok, p.scale_log2, lse2,
+                       Drow, pk, dk);
+        st_row_half(smP, rho, half, pk);
+        st_row_half(smDS, rho, half, dk);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_SFREE + b));
+        mbar_arrive(bar(B_PDSFULL));
+      }
+    }
+    // epilogue: TMEM lane = head-dim column d, 64 columns = the tile's keys
+    if (ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const int d = rho;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        uint16_t *out = which == 0 ? p.dV : p.dK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        const uint32_t col = which == 0 ? kColDV : kColDK;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + col + c0, rr);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int key = j * BK + e * 64 + c0 + c;  // sequence-relative key position
+            if (key < n) {
+              const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(rr[c]) * mul);
+              out[((size_t)h * p.T + s0 + key) * kD + d] = *reinterpret_cast<const uint16_t *>(&v);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+template <int BK>
+cudaError_t launch_bk(const bsa_shape_t &s, const void *Q, const void *K, const void *V,
+                      const void *dO, BwdTcParams p, cudaStream_t st) {
+  CUtensorMap mq, mdo, mk, mv;
+  if (!make_tmap_3d_bf16(&mq, Q, kD, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
+      !make_tmap_3d_bf16(&mdo, dO, kD, s.total_tokens, s.num_heads, 64, BK, 128 / BK) ||
+      !make_tmap_3d_bf16(&mk, K, kD, s.total_tokens, s.num_kv_heads, 64, 64, 1) ||
+      !make_tmap_3d_bf16(&mv, V, kD, s.total_tokens, s.num_kv_heads, 64, 64, 1))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel<BK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kv::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  bwd_dq_tc_kernel<BK><<<(unsigned)(rows * p.mtiles), dq::kThreads, dq::kSmemBytes, st>>>(
+      mq, mdo, mk, mv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_tc_kernel<BK><<<(unsigned)(rows * (BK / 64)), kv::kThreads, kv::kSmemBytes, st>>>(
+      mq, mdo, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_bwd_tc_supported(const bsa_shape_t &s) {
+  return s.dtype == BSA_BF16 && s.head_dim == kD && (s.block == 64 || s.block == 128);
+}
+
+// [count | cursor | kt_ptr (+1) | kt_work | kt_bucket | kt_rows (one per (row, block)
+// pair of any valid worklist: at most r + 1 per row)]
+size_t attention_bwd_tc_index_bytes(const bsa_shape_t &s) {
+  const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  const size_t pairs = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * (s.max_blocks + 1) / 2;
+  return 3 * up256(rows * 4) + up256((rows + 1) * 4) + up256((BSA_NUM_BUCKETS + 1) * 4) +
+         up256(pairs * 4);
+}
+
+cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const void *K,
+                                    const void *V, const void *dO, const float *lse,
+                                    const float *Dv, const int32_t *row_ptr,
+                                    const int32_t *col_idx, const int32_t *work,
+                                    const int32_t *bucket_off, float scale, void *dQ, void *dK,
+                                    void *dV, void *ws, int32_t *dev_status, cudaStream_t st) {
+  const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
+  char *w = static_cast<char *>(ws);
+  int32_t *cnt = reinterpret_cast<int32_t *>(w);
+  w += up256((size_t)nrows * 4);
+  int32_t *cursor = reinterpret_cast<int32_t *>(w);
+  w += up256((size_t)nrows * 4);
+  int32_t *kt_work = reinterpret_cast<int32_t *>(w);
+  w += up256((size_t)nrows * 4);
+  int32_t *kt_ptr = reinterpret_cast<int32_t *>(w);
+  w += up256(((size_t)nrows + 1) * 4);
+  int32_t *kt_bucket = reinterpret_cast<int32_t *>(w);
+  w += up256((BSA_NUM_BUCKETS + 1) * 4);
+  int32_t *kt_rows = reinterpret_cast<int32_t *>(w);
+
+  // zero counters (count and cursor are adjacent) and the key gradients: a key
+  // block that no row selected keeps dK = dV = 0
+  cudaError_t e = cudaMemsetAsync(cnt, 0, 2 * up256((size_t)nrows * 4), st);
+  if (e != cudaSuccess) return e;
+  const size_t kv_bytes = (size_t)s.num_kv_heads * s.total_tokens * kD * 2;
+  if ((e = cudaMemsetAsync(dK, 0, kv_bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dV, 0, kv_bytes, st)) != cudaSuccess) return e;
+  const int blocks = std::max(1, std::min(4 * num_sms(), (nrows + 255) / 256));
+  kt_count_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, cnt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_length_scan(cnt, kt_ptr, kt_work, kt_bucket, nrows, st)) != cudaSuccess)
+    return e;
+  kt_fill_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, kt_ptr, cursor,
+                                         kt_rows);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  BwdTcParams p;
+  p.cu = s.cu_seqlens;
+  p.row_ptr = row_ptr;
+  p.col_idx = col_idx;
+  p.work = work;
+  p.bucket_off = bucket_off;
+  p.kt_ptr = kt_ptr;
+  p.kt_rows = kt_rows;
+  p.kt_work = kt_work;
+  p.kt_bucket = kt_bucket;
+  p.lse = lse;
+  p.Dv = Dv;
+  p.dQ = static_cast<uint16_t *>(dQ);
+  p.dK = static_cast<uint16_t *>(dK);
+  p.dV = static_cast<uint16_t *>(dV);
+  p.status = dev_status;
+  p.T = s.total_tokens;
+  p.Hk = s.num_kv_heads;
+  p.G = s.num_heads / s.num_kv_heads;
+  p.Nq = s.max_blocks;
+  p.mtiles = (p.G * s.block + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  if (s.block == 64) return launch_bk<64>(s, Q, K, V, dO, p, st);
+  return launch_bk<128>(s, Q, K, V, dO, p, st);
+}
+
+}  // namespace bsa

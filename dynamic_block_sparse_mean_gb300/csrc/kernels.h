@@ -74,13 +74,28 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                             const int32_t *counts, int32_t *row_ptr, int32_t *col_idx,
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
                             cudaStream_t st, const bsa_kv_cache_t *cache = nullptr);
+// Row lengths (>= 0; a negative entry counts as 1) -> CSR offsets, and the rows of
+// non-zero length grouped by capacity bucket, largest first (worklist.cu).
+cudaError_t launch_length_scan(const int32_t *len, int32_t *row_ptr, int32_t *work,
+                               int32_t *bucket_off, int nrows, cudaStream_t st);
+// Tensor-core backward, BF16 with head_dim 128 (attn_bwd_tc.cu): workspace of
+// its key-major index, and the launch given D = rowsum(dO * O) [H, T].
+bool attention_bwd_tc_supported(const bsa_shape_t &s);
+size_t attention_bwd_tc_index_bytes(const bsa_shape_t &s);
+cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const void *K,
+                                    const void *V, const void *dO, const float *lse,
+                                    const float *Dv, const int32_t *row_ptr,
+                                    const int32_t *col_idx, const int32_t *work,
+                                    const int32_t *bucket_off, float scale, void *dQ, void *dK,
+                                    void *dV, void *ws, int32_t *dev_status, cudaStream_t st);
 // Backward of the sparse attention (attn_bwd.cu).
 size_t attention_bwd_workspace_bytes(const bsa_shape_t &s);
 cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void *K,
                                  const void *V, const void *O, const void *dO, const float *lse,
                                  const int32_t *row_ptr, const int32_t *col_idx,
                                  const int32_t *work, const int32_t *bucket_off, float scale,
-                                 void *dQ, void *dK, void *dV, void *ws, cudaStream_t st);
+                                 void *dQ, void *dK, void *dV, void *ws, int32_t *dev_status,
+                                 cudaStream_t st);
 
 // Density-1 worklist (every causal block) and coverage of eq.(10) (worklist.cu).
 size_t causal_worklist_capacity(const bsa_shape_t &s);

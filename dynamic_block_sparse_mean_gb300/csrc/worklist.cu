@@ -283,6 +283,12 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                           s.num_kv_heads, s.block, k_max);
 }
 
+cudaError_t launch_length_scan(const int32_t *len, int32_t *row_ptr, int32_t *work,
+                               int32_t *bucket_off, int nrows, cudaStream_t st) {
+  wl_scan_kernel<<<1, kScanThreads, 0, st>>>(len, row_ptr, work, bucket_off, nrows);
+  return cudaGetLastError();
+}
+
 size_t causal_worklist_capacity(const bsa_shape_t &s) {
   return (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * (s.max_blocks + 1) / 2;
 }

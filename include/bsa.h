@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 5
+#define BSA_VERSION 6
 
 typedef enum {
   BSA_OK = 0,
@@ -300,19 +300,27 @@ bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
  *   dQ, dK, dV of the forward of bsa_attention_fwd (same masks, same scale: <= 0
  *   means 1/sqrt(d)).  P is recomputed from lse; nothing is re-routed.  dK and dV
  *   sum the contributions of every query row and query head that selected a key
- *   block (GQA).  FP32 arithmetic on the SIMT pipes (a correctness-first path).
+ *   block (GQA).
+ *   BF16 with head_dim 128 runs on the tensor cores (tcgen05, fp32 accumulators in
+ *   TMEM): a query-major pass for dQ over the worklist and a key-major pass for dK
+ *   and dV over its transpose (built in the workspace), each gradient element
+ *   written once.  The order in which a key block's rows are summed follows an
+ *   atomic fill, so dK / dV may differ between runs in the last bits.  Other
+ *   shapes (fp32, head_dim 64) run an FP32 SIMT path.
  *   Q, dQ, O, dO : [H, T, d];  K, V, dK, dV : [H_kv, T, d];  element type shape->dtype.
  *   lse          : [H, T] fp32 from the forward.
+ *   dev_status   : see conventions (a bounded wait that ran out).
  *   ws           : at least bsa_attention_bwd_workspace_size() bytes, 256-aligned;
- *                  contents are overwritten (fp32 dK / dV accumulators).
+ *                  contents are overwritten.
  * ------------------------------------------------------------------------- */
 size_t bsa_attention_bwd_workspace_size(const bsa_shape_t *shape);
 bsa_status_t bsa_attention_bwd(const bsa_shape_t *shape, const void *Q, const void *K,
                                const void *V, const void *O, const void *dO, const float *lse,
                                const int32_t *row_ptr, const int32_t *col_idx,
                                const int32_t *work, const int32_t *bucket_off,
-                               float softmax_scale, void *dQ, void *dK, void *dV, void *ws,
-                               size_t ws_bytes, cudaStream_t stream);
+                               float softmax_scale, void *dQ, void *dK, void *dV,
+                               int32_t *dev_status, void *ws, size_t ws_bytes,
+                               cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Density-1 worklist — every causal block: row r of a sequence holds blocks

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.bsa_version() == 5
+    assert lib.bsa_version() == 6
     for code in _lib.STATUS_NAMES:
         assert lib.bsa_status_string(code)
 

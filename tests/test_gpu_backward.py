@@ -18,6 +18,10 @@ CASES = [
     ("bwd_bf16_gqa4_d128_b64", [700, 200], 8, 2, 128, 64, 4, False, "bf16", 2e-2),
     ("bwd_bf16_d128_b128", [600], 4, 1, 128, 128, 3, False, "bf16", 2e-2),
     ("bwd_fp32_d128_b64_tail", [400, 90], 4, 2, 128, 64, 3, True, "fp32", 1e-3),
+    # tensor-core path: one query head per KV head (half of each M-tile masked), and
+    # eight (four M-tiles per row)
+    ("bwd_bf16_g1_d128_b64_sink", [500, 70], 2, 2, 128, 64, 4, True, "bf16", 2e-2),
+    ("bwd_bf16_gqa8_d128_b64", [600, 1], 16, 2, 128, 64, 3, False, "bf16", 2e-2),
 ]
 
 
