@@ -19,6 +19,9 @@
 // are written by the softmax warps in the same layout, which serves both as a
 // K-major operand (dS of dQ = dS K) and as an MN-major one (P, dS of the
 // key-major products, and K / Q / dO read transposed).
+//
+// Both passes run 320 threads: two softmax warpgroups that take alternate tiles
+// (each warp reads the TMEM lanes of its quarter), a TMA warp and an MMA warp.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -95,6 +98,34 @@ BSA_DEV void softmax_grad32(const uint32_t (&s)[32], const uint32_t (&dp)[32], b
 }
 
 // Four 16-byte chunks (half h of a 128-byte row) into the swizzled tile.
+BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[16]);
+BSA_DEV void softmax_grad32(const uint32_t (&s)[32], const uint32_t (&dp)[32], bool valid,
+                            bool diag, int key0, int tok, float scale_log2, float lse2, float Drow,
+                            uint32_t (&pk)[16], uint32_t (&dk)[16]);
+
+// P and dS of the 64 keys of one TMEM S / dP tile row into shared memory (P only
+// when smP != 0).  The second half's loads are in flight while the first half
+// is computed.
+BSA_DEV void tile_grad64(uint32_t tS, uint32_t tDP, uint32_t smP, uint32_t smDS, int rho,
+                         bool valid, bool diag, int key0, int tok, float scale_log2, float lse2,
+                         float Drow) {
+  uint32_t s0[32], d0[32], s1[32], d1[32], pk[16], dk[16];
+  tmem_ld32_async(tS, s0);
+  tmem_ld32_async(tDP, d0);
+  tmem_wait_ld(s0);
+  tmem_wait_ld(d0);
+  tmem_ld32_async(tS + 32, s1);
+  tmem_ld32_async(tDP + 32, d1);
+  softmax_grad32(s0, d0, valid, diag, key0, tok, scale_log2, lse2, Drow, pk, dk);
+  if (smP != 0u) st_row_half(smP, rho, 0, pk);
+  st_row_half(smDS, rho, 0, dk);
+  tmem_wait_ld(s1);
+  tmem_wait_ld(d1);
+  softmax_grad32(s1, d1, valid, diag, key0 + 32, tok, scale_log2, lse2, Drow, pk, dk);
+  if (smP != 0u) st_row_half(smP, rho, 1, pk);
+  st_row_half(smDS, rho, 1, dk);
+}
+
 BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[16]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -148,23 +179,30 @@ __global__ void kt_fill_kernel(const int32_t *__restrict__ row_ptr,
 
 // ---------------------------------------------------------------- dQ pass
 
-// One CTA per (work row, M-tile): Q and dO of the tile stay in shared memory;
-// every 64-key tile of the row's blocks comes in by TMA, S and dP go to TMEM,
-// four warps (one query row per thread) turn them into dS in shared memory, and
-// dQ += dS K accumulates in TMEM.  Shared memory (96 KB) and TMEM (256 columns)
-// let two CTAs share an SM.  Warp 4 lane 0 issues the copies and the MMAs.
+// One CTA per (work row, M-tile), one per SM: Q and dO of the tile stay in shared
+// memory; the 64-key tiles of the row's blocks stream through a three-stage K / V
+// ring.  S and dP of step s land in one of two TMEM buffers while the softmax
+// warps turn step s-1 into dS (two shared-memory buffers), which then feeds
+// dQ += dS K (fp32 in TMEM).  320 threads: two softmax warpgroups (warps 0-3 take
+// the even steps, 4-7 the odd ones; one query row per thread), warp 8 TMA, warp 9
+// MMA.
 namespace dq {
-constexpr int kThreads = 160;
-constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = 81920;  // dS reuses V
-constexpr int kOffBar = 98304;
-constexpr int B_QFULL = 0, B_KVFULL = 1, B_SFULL = 2, B_DSFULL = 3, B_KVFREE = 4, B_DQFULL = 5;
-constexpr int kOffCtl = kOffBar + 64;
+constexpr int kThreads = 320;
+constexpr int NS = 3;
+constexpr int kOffQ = 0, kOffDO = 32768, kOffKV = 65536;  // stage: K (16 KB) then V (16 KB)
+constexpr int kOffDS = kOffKV + NS * 32768;
+constexpr int kOffBar = kOffDS + 2 * 16384;
+constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = B_KVFULL + NS, B_SFULL = B_KVEMPTY + NS;
+constexpr int B_SFREE = B_SFULL + 2, B_DSFULL = B_SFREE + 2, B_DSFREE = B_DSFULL + 2;
+constexpr int B_DQFULL = B_DSFREE + 2;
+constexpr int kOffCtl = kOffBar + (B_DQFULL + 1) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace dq
 
 template <int BK>
-__global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
+__global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const BwdTcParams p) {
@@ -182,15 +220,21 @@ __global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_KVFULL), 1);
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_DSFULL), 4);
-    mbar_init(bar(B_KVFREE), 1);
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(bar(B_KVFULL + st), 1);
+      mbar_init(bar(B_KVEMPTY + st), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_SFREE + b), 4);
+      mbar_init(bar(B_DSFULL + b), 4);
+      mbar_init(bar(B_DSFREE + b), 1);
+    }
     mbar_init(bar(B_DQFULL), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -204,86 +248,121 @@ __global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
   const int r = row % p.Nq, h = (row / p.Nq) % p.Hk, i = row / (p.Nq * p.Hk);
   const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
   const int kv0 = __ldg(p.row_ptr + row), nsteps = (__ldg(p.row_ptr + row + 1) - kv0) * KT;
-  const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
-                 smV = sbase + kOffV;
+  const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smKV = sbase + kOffKV,
+                 smDS = sbase + kOffDS;
 
-  if (warp == 4) {
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int kv_issued = -1;
+      int issued[NS];
+      for (int st = 0; st < NS; ++st) issued[st] = -1;
       const int hq0 = h * p.G + (t * 128) / BK;
       mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
       for (int pn = 0; pn < 2; ++pn) {
         tma_load_3d(smQ + pn * 16384, &tmQ, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
         tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
       }
-      for (int s = 0; ok && s < nsteps; ++s) {
-        const int j = __ldg(p.col_idx + kv0 + s / KT);
-        const int y = s0 + j * BK + (s % KT) * 64;
-        if (s > 0 && !(ok = mbar_wait(bar(B_KVFREE), (s - 1) & 1, abort_flag, p.status))) break;
-        mbar_arrive_expect_tx(bar(B_KVFULL), 4 * 8192);
-        kv_issued = s & 1;
+      for (int s = 0; s < nsteps; ++s) {
+        const int st = s % NS;
+        if (s >= NS &&
+            !(ok = mbar_wait(bar(B_KVEMPTY + st), ((s - NS) / NS) & 1, abort_flag, p.status)))
+          break;
+        const int y = s0 + __ldg(p.col_idx + kv0 + s / KT) * BK + (s % KT) * 64;
+        mbar_arrive_expect_tx(bar(B_KVFULL + st), 4 * 8192);
+        issued[st] = (s / NS) & 1;
+        const uint32_t k = smKV + st * 32768, v = k + 16384;
         for (int pn = 0; pn < 2; ++pn) {
-          tma_load_3d(smK + pn * 8192, &tmK, bar(B_KVFULL), pn * 64, y, h);
-          tma_load_3d(smV + pn * 8192, &tmV, bar(B_KVFULL), pn * 64, y, h);
+          tma_load_3d(k + pn * 8192, &tmK, bar(B_KVFULL + st), pn * 64, y, h);
+          tma_load_3d(v + pn * 8192, &tmV, bar(B_KVFULL + st), pn * 64, y, h);
         }
-        if (!(ok = mbar_wait(bar(B_KVFULL), s & 1, abort_flag, p.status))) break;
-        kv_issued = -1;
-        if (s == 0 && !(ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status))) break;
-        tc_fence_after();
-        mma_xyT(tmem + kColS, smQ, smK);
-        mma_xyT(tmem + kColDP, smDO, smV);
-        mma_commit(bar(B_SFULL));
-        if (!(ok = mbar_wait(bar(B_DSFULL), s & 1, abort_flag, p.status))) break;
-        tc_fence_after();
+      }
+      // every copy issued lands before the CTA leaves
+      mbar_wait_drain(bar(B_QFULL), 0);
+      for (int st = 0; st < NS; ++st)
+        if (issued[st] >= 0) mbar_wait_drain(bar(B_KVFULL + st), issued[st]);
+      (void)ok;
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
+      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 64 keys in steps of 16
+        const int b = s & 1;
+        const uint32_t k = smKV + (s % NS) * 32768;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K: 64 keys in steps of 16
-          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(smV + kk * 32, 16, 1024),
-                      sdesc_sw128(smK + kk * 2048, 8192, 1024), kIdescDQ,
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(smDS + b * 16384 + kk * 32, 16, 1024),
+                      sdesc_sw128(k + kk * 2048, 8192, 1024), kIdescDQ,
                       (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_KVFREE));
+        mma_commit(bar(B_KVEMPTY + s % NS));
+        mma_commit(bar(B_DSFREE + b));
+      };
+      for (int s = 0; ok && s < nsteps; ++s) {
+        const int st = s % NS, b = s & 1;
+        if (!(ok = mbar_wait(bar(B_KVFULL + st), (s / NS) & 1, abort_flag, p.status))) break;
+        if (s >= 2 &&
+            !(ok = mbar_wait(bar(B_SFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
+          break;
+        tc_fence_after();
+        const uint32_t k = smKV + st * 32768, v = k + 16384;
+        mma_xyT(tmem + kColS + 64 * b, smQ, k);
+        mma_xyT(tmem + kColDP + 64 * b, smDO, v);
+        mma_commit(bar(B_SFULL + b));
+        if (s >= 1) {
+          if (!(ok = mbar_wait(bar(B_DSFULL + (b ^ 1)), ((s - 1) >> 1) & 1, abort_flag,
+                               p.status)))
+            break;
+          tc_fence_after();
+          dq_product(s - 1);
+        }
+      }
+      if (ok && nsteps > 0 &&
+          (ok = mbar_wait(bar(B_DSFULL + ((nsteps - 1) & 1)), ((nsteps - 1) >> 1) & 1, abort_flag,
+                          p.status))) {
+        tc_fence_after();
+        dq_product(nsteps - 1);
       }
       mma_commit(bar(B_DQFULL));
-      if (!ok) {  // copies in flight land before the CTA leaves
-        mbar_wait_drain(bar(B_QFULL), 0);
-        if (kv_issued >= 0) mbar_wait_drain(bar(B_KVFULL), kv_issued);
-      }
       mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int rho = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int g = warp / 4, wq = warp % 4;  // warpgroup g takes the steps s = g (mod 2)
+    const int rho = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
     const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
     const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
     bool ok = true;
-    for (int s = 0; s < nsteps; ++s) {
-      const int j = __ldg(p.col_idx + kv0 + s / KT);
-      const bool diag = j == r;
-      if (!(ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status))) break;
+    int j_next = g < nsteps ? __ldg(p.col_idx + kv0 + g / KT) : 0;
+    for (int s = g; s < nsteps; s += 2) {
+      const int b = s & 1;
+      const bool diag = j_next == r;
+      if (s + 2 < nsteps) j_next = __ldg(p.col_idx + kv0 + (s + 2) / KT);
+      if (!(ok = mbar_wait(bar(B_SFULL + b), (s >> 1) & 1, abort_flag, p.status))) break;
+      if (s >= 2 && !(ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
+        break;
       tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32], pk[16], dk[16];
-        tmem_ld32(tmem + lane_base + kColS + half * 32, sr);
-        tmem_ld32(tmem + lane_base + kColDP + half * 32, dr);
-        softmax_grad32(sr, dr, q.valid, diag, (s % KT) * 64 + half * 32, q.tok, p.scale_log2,
-                       lse2, Drow, pk, dk);
-        st_row_half(smV, rho, half, dk);  // V was consumed by dP; dS takes its place
-      }
+      tile_grad64(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b, 0u,
+                  smDS + b * 16384, rho, q.valid, diag, (s % KT) * 64, q.tok, p.scale_log2, lse2,
+                  Drow);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+      if (lane == 0) {
+        mbar_arrive(bar(B_SFREE + b));
+        mbar_arrive(bar(B_DSFULL + b));
+      }
     }
+    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
     if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
       tc_fence_after();
-      uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD);
+      uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + kColDQ + c0, rr);
+        tmem_ld32(tmem + lane_base + kColDQ + 64 * g + c0, rr);
         uint32_t o[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -299,7 +378,7 @@ __global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) {
+  if (warp == 9) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -307,22 +386,24 @@ __global__ void __launch_bounds__(dq::kThreads) bwd_dq_tc_kernel(
 
 // ---------------------------------------------------------------- dK / dV pass
 
-// One CTA per (key block, 64-key tile): K and V of the tile stay in shared memory;
-// the query tiles of every row that selected the block stream through a two-stage
-// ring (Q and dO); S and dP of tile n land in one of two TMEM buffers while the
-// softmax warps work on tile n-1, which then feeds dV^T += dO^T P and
-// dK^T += Q^T dS.  192 threads: warps 0-3 softmax and epilogue, warp 4 TMA,
-// warp 5 MMA.  One CTA per SM (192 KB of shared memory, all of TMEM).
+// One CTA per (key block, 64-key tile), one per SM: K and V of the tile stay in
+// shared memory; the query tiles of every row that selected the block stream
+// through a two-stage ring (Q and dO).  S and dP of tile n land in one of two TMEM
+// buffers while the softmax warps turn tile n-1 into P and dS (two shared-memory
+// buffers each), which then feed dV^T += dO^T P and dK^T += Q^T dS.  320 threads:
+// two softmax warpgroups on alternate tiles (warpgroup 0 writes dV, 1 dK at the
+// end), warp 8 TMA, warp 9 MMA.
 namespace kv {
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kOffK = 0, kOffV = 16384, kOffQ = 32768, kOffDO = kOffQ + 2 * 32768;
-constexpr int kOffP = kOffDO + 2 * 32768, kOffDS = kOffP + 16384;
-constexpr int kOffBar = kOffDS + 16384;
+constexpr int kOffP = kOffDO + 2 * 32768, kOffDS = kOffP + 2 * 16384;
+constexpr int kOffBar = kOffDS + 2 * 16384;
 constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_SFREE = 7;
-constexpr int B_PDSFULL = 9, B_PDSFREE = 10, B_DONE = 11;
-constexpr int kOffCtl = kOffBar + 12 * 8;
+constexpr int B_PDSFULL = 9, B_PDSFREE = 11, B_DONE = 13;
+constexpr int kOffCtl = kOffBar + 14 * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kTmemCols = 512;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace kv
 
 template <int BK>
@@ -349,14 +430,14 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
       mbar_init(bar(B_QEMPTY + b), 1);
       mbar_init(bar(B_SFULL + b), 1);
       mbar_init(bar(B_SFREE + b), 4);
+      mbar_init(bar(B_PDSFULL + b), 4);
+      mbar_init(bar(B_PDSFREE + b), 1);
     }
-    mbar_init(bar(B_PDSFULL), 4);
-    mbar_init(bar(B_PDSFREE), 1);
     mbar_init(bar(B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -375,7 +456,7 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
                  smDO = sbase + kOffDO, smP = sbase + kOffP, smDS = sbase + kOffDS;
   auto row_of = [&](int nt) { return __ldg(p.kt_rows + l0 + nt / p.mtiles); };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
@@ -408,22 +489,22 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
         if (issued[st] >= 0) mbar_wait_drain(bar(B_QFULL + st), issued[st]);
       (void)ok;
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
       auto kv_products = [&](int nt) {  // dV^T += dO^T P, dK^T += Q^T dS of tile nt
-        const int st = nt & 1;
+        const int b = nt & 1;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 128 query rows in steps of 16
           const uint32_t acc = (nt > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smDO + st * 32768 + kk * 2048, 16384, 1024),
-                      sdesc_sw128(smP + kk * 2048, 16384, 1024), kIdescKV, acc);
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smQ + st * 32768 + kk * 2048, 16384, 1024),
-                      sdesc_sw128(smDS + kk * 2048, 16384, 1024), kIdescKV, acc);
+          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smDO + b * 32768 + kk * 2048, 16384, 1024),
+                      sdesc_sw128(smP + b * 16384 + kk * 2048, 16384, 1024), kIdescKV, acc);
+          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smQ + b * 32768 + kk * 2048, 16384, 1024),
+                      sdesc_sw128(smDS + b * 16384 + kk * 2048, 16384, 1024), kIdescKV, acc);
         }
-        mma_commit(bar(B_QEMPTY + st));
-        mma_commit(bar(B_PDSFREE));
+        mma_commit(bar(B_QEMPTY + b));
+        mma_commit(bar(B_PDSFREE + b));
       };
       for (int nt = 0; ok && nt < ntiles; ++nt) {
         const int b = nt & 1;
@@ -436,13 +517,16 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
         mma_xyT(tmem + kColDP + 64 * b, smDO + b * 32768, smV);
         mma_commit(bar(B_SFULL + b));
         if (nt >= 1) {
-          if (!(ok = mbar_wait(bar(B_PDSFULL), (nt - 1) & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait(bar(B_PDSFULL + (b ^ 1)), ((nt - 1) >> 1) & 1, abort_flag,
+                               p.status)))
+            break;
           tc_fence_after();
           kv_products(nt - 1);
         }
       }
       if (ok && ntiles > 0 &&
-          (ok = mbar_wait(bar(B_PDSFULL), (ntiles - 1) & 1, abort_flag, p.status))) {
+          (ok = mbar_wait(bar(B_PDSFULL + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1,
+                          abort_flag, p.status))) {
         tc_fence_after();
         kv_products(ntiles - 1);
       }
@@ -451,58 +535,62 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int rho = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int g = warp / 4, wq = warp % 4;  // warpgroup g takes the tiles nt = g (mod 2)
+    const int rho = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     bool ok = true;
-    for (int nt = 0; nt < ntiles; ++nt) {
+    // the row of this warpgroup's next tile and its statistics are loaded one tile ahead
+    auto stats = [&](int nt, QRow &q, float &lse2, float &Drow, int &r) {
+      r = row_of(nt);
+      q = qrow<BK>(p, nt % p.mtiles, rho, h, r, s0, n);
+      lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
+      Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
+    };
+    QRow qn;
+    float lse_n = 0.f, D_n = 0.f;
+    int r_n = 0;
+    if (g < ntiles) stats(g, qn, lse_n, D_n, r_n);
+    for (int nt = g; nt < ntiles; nt += 2) {
       const int b = nt & 1;
-      const int r = row_of(nt), t = nt % p.mtiles;
-      const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
-      const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
-      const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
-      const bool diag = r == j;
+      const QRow q = qn;
+      const float lse2 = lse_n, Drow = D_n;
+      const bool diag = r_n == j;
+      if (nt + 2 < ntiles) stats(nt + 2, qn, lse_n, D_n, r_n);
       if (!(ok = mbar_wait(bar(B_SFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
-      // P / dS of the previous tile have been consumed by its dK / dV products
-      if (nt >= 1 && !(ok = mbar_wait(bar(B_PDSFREE), (nt - 1) & 1, abort_flag, p.status))) break;
+      // P / dS of tile nt-2 have been consumed by its dK / dV products
+      if (nt >= 2 &&
+          !(ok = mbar_wait(bar(B_PDSFREE + b), ((nt - 2) >> 1) & 1, abort_flag, p.status)))
+        break;
       tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32], pk[16], dk[16];
-        tmem_ld32(tmem + lane_base + kColS + 64 * b + half * 32, sr);
-        tmem_ld32(tmem + lane_base + kColDP + 64 * b + half * 32, dr);
-        softmax_grad32(sr, dr, q.valid, diag, e * 64 + half * 32, q.tok, p.scale_log2, lse2,
-                       Drow, pk, dk);
-        st_row_half(smP, rho, half, pk);
-        st_row_half(smDS, rho, half, dk);
-      }
+      tile_grad64(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b,
+                  smP + b * 16384, smDS + b * 16384, rho, q.valid, diag, e * 64, q.tok,
+                  p.scale_log2, lse2, Drow);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar(B_SFREE + b));
-        mbar_arrive(bar(B_PDSFULL));
+        mbar_arrive(bar(B_PDSFULL + b));
       }
     }
-    // epilogue: TMEM lane = head-dim column d, 64 columns = the tile's keys
+    // epilogue: TMEM lane = head-dim column d, 64 columns = the tile's keys;
+    // warpgroup 0 writes dV, warpgroup 1 dK
     if (ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status)) {
       tc_fence_after();
       const int d = rho;
+      uint16_t *out = g == 0 ? p.dV : p.dK;
+      const float mul = g == 0 ? 1.f : p.scale;
+      const uint32_t col = g == 0 ? kColDV : kColDK;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        uint16_t *out = which == 0 ? p.dV : p.dK;
-        const float mul = which == 0 ? 1.f : p.scale;
-        const uint32_t col = which == 0 ? kColDV : kColDK;
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + col + c0, rr);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + col + c0, rr);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = j * BK + e * 64 + c0 + c;  // sequence-relative key position
-            if (key < n) {
-              const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(rr[c]) * mul);
-              out[((size_t)h * p.T + s0 + key) * kD + d] = *reinterpret_cast<const uint16_t *>(&v);
-            }
+        for (int c = 0; c < 32; ++c) {
+          const int key = j * BK + e * 64 + c0 + c;  // sequence-relative key position
+          if (key < n) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(rr[c]) * mul);
+            out[((size_t)h * p.T + s0 + key) * kD + d] = *reinterpret_cast<const uint16_t *>(&v);
           }
         }
       }
@@ -511,7 +599,7 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
