@@ -137,12 +137,13 @@ BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[1
 
 // S = X Y^T for one 128-row X tile (two 16 KB panels) and one 64-row Y tile
 // (two 8 KB panels), K = d.
+// Descriptors differ in their low word only, and the K-step offsets are constants.
 BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
+  const uint32_t xl = desc_lo(x, 16), yl = desc_lo(y, 16);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk)
-    mma_bf16_ss(d_tmem, sdesc_sw128(x + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
-                sdesc_sw128(y + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), kIdescS,
-                kk > 0 ? 1u : 0u);
+    mma_ss_lo(d_tmem, xl + ((kk / 4) * 16384 + (kk % 4) * 32) / 16,
+              yl + ((kk / 4) * 8192 + (kk % 4) * 32) / 16, kDescHi, kIdescS, kk > 0 ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------- key-major index
@@ -289,12 +290,12 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
       auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 64 keys in steps of 16
         const int b = s & 1;
-        const uint32_t k = smKV + (s % NS) * 32768;
+        const uint32_t al = desc_lo(smDS + b * 16384, 16);
+        const uint32_t bl = desc_lo(smKV + (s % NS) * 32768, 8192);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(smDS + b * 16384 + kk * 32, 16, 1024),
-                      sdesc_sw128(k + kk * 2048, 8192, 1024), kIdescDQ,
-                      (s > 0 || kk > 0) ? 1u : 0u);
+          mma_ss_lo(tmem + kColDQ, al + kk * 2, bl + kk * 128, kDescHi, kIdescDQ,
+                    (s > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_KVEMPTY + s % NS));
         mma_commit(bar(B_DSFREE + b));
       };
@@ -495,13 +496,13 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
       bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
       auto kv_products = [&](int nt) {  // dV^T += dO^T P, dK^T += Q^T dS of tile nt
         const int b = nt & 1;
+        const uint32_t dol = desc_lo(smDO + b * 32768, 16384), pl = desc_lo(smP + b * 16384, 16384);
+        const uint32_t ql = desc_lo(smQ + b * 32768, 16384), dsl = desc_lo(smDS + b * 16384, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 128 query rows in steps of 16
+        for (int kk = 0; kk < 8; ++kk) {  // 128 query rows in steps of 16 (2048 bytes)
           const uint32_t acc = (nt > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smDO + b * 32768 + kk * 2048, 16384, 1024),
-                      sdesc_sw128(smP + b * 16384 + kk * 2048, 16384, 1024), kIdescKV, acc);
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smQ + b * 32768 + kk * 2048, 16384, 1024),
-                      sdesc_sw128(smDS + b * 16384 + kk * 2048, 16384, 1024), kIdescKV, acc);
+          mma_ss_lo(tmem + kColDV, dol + kk * 128, pl + kk * 128, kDescHi, kIdescKV, acc);
+          mma_ss_lo(tmem + kColDK, ql + kk * 128, dsl + kk * 128, kDescHi, kIdescKV, acc);
         }
         mma_commit(bar(B_QEMPTY + b));
         mma_commit(bar(B_PDSFREE + b));

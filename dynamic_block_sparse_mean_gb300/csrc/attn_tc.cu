@@ -153,29 +153,6 @@ BSA_DEV int2 kv_coord(const AttnParams &p, const Unit &w, int jb) {
   }
 }
 
-// High word of every shared-memory descriptor used here: stride byte offset
-// 1024 (8 rows of 128 bytes), descriptor version 1, 128-byte swizzle.
-constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-
-// Low word: start address >> 4 and leading byte offset >> 4.
-BSA_DEV uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
-  return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
-}
-
-// tcgen05.mma kind::f16 with both operands in shared memory, descriptors given as
-// (low word, shared high word).
-BSA_DEV void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
-                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
-      "mov.b64 ad, {%1, %5};\n\t"
-      "mov.b64 bd, {%2, %5};\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
-      : "memory");
-}
-
 // Same with A (P, bf16 pairs) read from tensor memory.
 BSA_DEV void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
                        uint32_t idesc, uint32_t accumulate) {
