@@ -9,7 +9,7 @@
 // Two passes so that every output element has one writer and no atomics touch the
 // gradients: the dQ pass walks the forward's worklist (row -> its key blocks); the
 // dK / dV pass walks the transposed index (key block -> the rows that selected
-// it), built here by a count, a scan and an atomic fill.  Both passes recompute S
+// it, ascending), built here by a count, a scan and a row bitmap per key block.  Both passes recompute S
 // and dP.  Masks are the forward's: the causal triangle inside the diagonal block
 // and query rows past the sequence end or past the KV-head group.
 //
@@ -148,32 +148,59 @@ BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
 
 // ---------------------------------------------------------------- key-major index
 
-// Count, per key block, the rows that selected it (entries outside [0, r] skipped).
-__global__ void kt_count_kernel(const int32_t *__restrict__ row_ptr,
-                                const int32_t *__restrict__ col_idx, int nrows, int Nq,
-                                int32_t *__restrict__ cnt) {
+// Mark, per key block, the rows that selected it: bit r of the key block's
+// ceil(N_q / 32) words.
+__global__ void kt_mark_kernel(const int32_t *__restrict__ row_ptr,
+                               const int32_t *__restrict__ col_idx, int nrows, int Nq, int W,
+                               uint32_t *__restrict__ bits) {
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
     const int r = row % Nq, base = row - r;
     for (int e = row_ptr[row]; e < row_ptr[row + 1]; ++e) {
       const int j = col_idx[e];
-      if (j >= 0 && j <= r) atomicAdd(cnt + base + j, 1);
+      if (j >= 0 && j <= r) atomicOr(bits + (size_t)(base + j) * W + r / 32, 1u << (r % 32));
     }
   }
 }
 
-__global__ void kt_fill_kernel(const int32_t *__restrict__ row_ptr,
-                               const int32_t *__restrict__ col_idx, int nrows, int Nq,
-                               const int32_t *__restrict__ kt_ptr, int32_t *__restrict__ cursor,
-                               int32_t *__restrict__ kt_rows) {
-  for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
-       row += gridDim.x * blockDim.x) {
-    const int r = row % Nq, base = row - r;
-    for (int e = row_ptr[row]; e < row_ptr[row + 1]; ++e) {
-      const int j = col_idx[e];
-      if (j < 0 || j > r) continue;
-      const int pos = atomicAdd(cursor + base + j, 1);
-      kt_rows[kt_ptr[base + j] + pos] = r;
+// Rows per key block: the population count of its bitmap (a row named twice in a
+// malformed worklist still counts once, matching what the emit writes).
+__global__ void kt_count_kernel(const uint32_t *__restrict__ bits, int nrows, int W,
+                                int32_t *__restrict__ cnt) {
+  for (int kb = blockIdx.x * blockDim.x + threadIdx.x; kb < nrows;
+       kb += gridDim.x * blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < W; ++w) c += __popc(bits[(size_t)kb * W + w]);
+    cnt[kb] = c;
+  }
+}
+
+// One warp per key block: its rows in ascending order at kt_rows[kt_ptr[kb] ..), so
+// the dK / dV sums run in the same order on every call.
+__global__ void kt_emit_kernel(const uint32_t *__restrict__ bits,
+                               const int32_t *__restrict__ kt_ptr, int32_t *__restrict__ kt_rows,
+                               int nrows, int W) {
+  const int lane = threadIdx.x % 32;
+  for (int kb = (blockIdx.x * blockDim.x + threadIdx.x) / 32; kb < nrows;
+       kb += gridDim.x * blockDim.x / 32) {
+    int pos = kt_ptr[kb];
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t m = w < W ? bits[(size_t)kb * W + w] : 0u;
+      const int c = __popc(m);
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int out = pos + incl - c;
+      while (m != 0u) {
+        const int b = __ffs(m) - 1;
+        kt_rows[out++] = w * 32 + b;
+        m &= m - 1u;
+      }
+      pos += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
 }
@@ -639,13 +666,14 @@ bool attention_bwd_tc_supported(const bsa_shape_t &s) {
   return s.dtype == BSA_BF16 && s.head_dim == kD && (s.block == 64 || s.block == 128);
 }
 
-// [count | cursor | kt_ptr (+1) | kt_work | kt_bucket | kt_rows (one per (row, block)
-// pair of any valid worklist: at most r + 1 per row)]
+// [count | kt_work | kt_ptr (+1) | kt_bucket | row bitmap (ceil(N_q / 32) words per key
+// block) | kt_rows (one per (row, block) pair of any valid worklist: at most r + 1 per row)]
 size_t attention_bwd_tc_index_bytes(const bsa_shape_t &s) {
   const size_t rows = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks;
+  const size_t W = ((size_t)s.max_blocks + 31) / 32;
   const size_t pairs = (size_t)s.num_seqs * s.num_kv_heads * s.max_blocks * (s.max_blocks + 1) / 2;
-  return 3 * up256(rows * 4) + up256((rows + 1) * 4) + up256((BSA_NUM_BUCKETS + 1) * 4) +
-         up256(pairs * 4);
+  return 2 * up256(rows * 4) + up256((rows + 1) * 4) + up256((BSA_NUM_BUCKETS + 1) * 4) +
+         up256(rows * W * 4) + up256(pairs * 4);
 }
 
 cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const void *K,
@@ -655,10 +683,9 @@ cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const v
                                     const int32_t *bucket_off, float scale, void *dQ, void *dK,
                                     void *dV, void *ws, int32_t *dev_status, cudaStream_t st) {
   const int nrows = s.num_seqs * s.num_kv_heads * s.max_blocks;
+  const int W = (s.max_blocks + 31) / 32;
   char *w = static_cast<char *>(ws);
   int32_t *cnt = reinterpret_cast<int32_t *>(w);
-  w += up256((size_t)nrows * 4);
-  int32_t *cursor = reinterpret_cast<int32_t *>(w);
   w += up256((size_t)nrows * 4);
   int32_t *kt_work = reinterpret_cast<int32_t *>(w);
   w += up256((size_t)nrows * 4);
@@ -666,22 +693,27 @@ cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const v
   w += up256(((size_t)nrows + 1) * 4);
   int32_t *kt_bucket = reinterpret_cast<int32_t *>(w);
   w += up256((BSA_NUM_BUCKETS + 1) * 4);
+  uint32_t *bits = reinterpret_cast<uint32_t *>(w);
+  w += up256((size_t)nrows * W * 4);
   int32_t *kt_rows = reinterpret_cast<int32_t *>(w);
 
-  // zero counters (count and cursor are adjacent) and the key gradients: a key
-  // block that no row selected keeps dK = dV = 0
-  cudaError_t e = cudaMemsetAsync(cnt, 0, 2 * up256((size_t)nrows * 4), st);
+  // zero the row bitmap and the key gradients: a key block that no row selected
+  // keeps dK = dV = 0
+  cudaError_t e = cudaMemsetAsync(bits, 0, (size_t)nrows * W * 4, st);
   if (e != cudaSuccess) return e;
   const size_t kv_bytes = (size_t)s.num_kv_heads * s.total_tokens * kD * 2;
   if ((e = cudaMemsetAsync(dK, 0, kv_bytes, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dV, 0, kv_bytes, st)) != cudaSuccess) return e;
   const int blocks = std::max(1, std::min(4 * num_sms(), (nrows + 255) / 256));
-  kt_count_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, cnt);
+  kt_mark_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, W, bits);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kt_count_kernel<<<blocks, 256, 0, st>>>(bits, nrows, W, cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_length_scan(cnt, kt_ptr, kt_work, kt_bucket, nrows, st)) != cudaSuccess)
     return e;
-  kt_fill_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, kt_ptr, cursor,
-                                         kt_rows);
+  const int eblocks = (int)std::max<size_t>(
+      1, std::min<size_t>((size_t)8 * num_sms(), ((size_t)nrows * 32 + 255) / 256));
+  kt_emit_kernel<<<eblocks, 256, 0, st>>>(bits, kt_ptr, kt_rows, nrows, W);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   BwdTcParams p;

@@ -304,9 +304,9 @@ bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,
  *   BF16 with head_dim 128 runs on the tensor cores (tcgen05, fp32 accumulators in
  *   TMEM): a query-major pass for dQ over the worklist and a key-major pass for dK
  *   and dV over its transpose (built in the workspace), each gradient element
- *   written once.  The order in which a key block's rows are summed follows an
- *   atomic fill, so dK / dV may differ between runs in the last bits.  Other
- *   shapes (fp32, head_dim 64) run an FP32 SIMT path.
+ *   written once, a key block's rows summed in ascending order (the result does
+ *   not change between runs).  Other shapes (fp32, head_dim 64) run an FP32 SIMT
+ *   path, whose dK / dV are summed with fp32 atomics.
  *   Q, dQ, O, dO : [H, T, d];  K, V, dK, dV : [H_kv, T, d];  element type shape->dtype.
  *   lse          : [H, T] fp32 from the forward.
  *   dev_status   : see conventions (a bounded wait that ran out).

@@ -58,3 +58,25 @@ def test_backward_matches_oracle(case):
         g = got.float().cpu().numpy().astype(np.float64)
         err = np.abs(g - ref).max() / np.abs(ref).max()
         assert err <= tol, (what, err)
+
+
+def test_tensor_core_backward_is_deterministic():
+    """The key-major pass sums a key block's rows in ascending order: two calls on
+    the same inputs give the same bits."""
+    x = synth.gen_prefill([900, 300], 8, 2, 128, 64, 23, "iid", "bf16")
+    q, k, v = upload(x)
+    sh = shape_of(x, 8, 2)
+    Jo, co, _, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, 64, 4,
+                                oracle.TOPK, 5, force_sink=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wl = bsa.build_worklist(torch.as_tensor(Jo.astype(np.int32), device="cuda"),
+                            torch.as_tensor(co.astype(np.int32), device="cuda"), sh, 5, status)
+    O, lse = bsa.attention_fwd(q, k, v, wl, sh, status)
+    do = dev_tensor(synth.f32_to_bf16_bits(np.random.default_rng(4).normal(size=x.q.shape)
+                                           .astype(np.float32)), "bf16")
+    a = [t.clone() for t in bsa.attention_bwd(q, k, v, O, do, lse, wl, sh, dev_status=status)]
+    b = bsa.attention_bwd(q, k, v, O, do, lse, wl, sh, dev_status=status)
+    torch.cuda.synchronize()
+    bsa.check_status(status)
+    for t0, t1 in zip(a, b):
+        assert torch.equal(t0, t1)
