@@ -52,7 +52,8 @@ bsa_status_t launched(cudaError_t e) { return e == cudaSuccess ? BSA_OK : BSA_ER
 bsa_status_t route_params_status(const bsa_route_params_t &p) {
   if (p.mode != BSA_ROUTE_TOPK && p.mode != BSA_ROUTE_THRESHOLD) return BSA_ERR_INVALID_ARG;
   if (p.k_max < 1 || p.k_max > BSA_MAX_K) return BSA_ERR_UNSUPPORTED;
-  if (p.mode == BSA_ROUTE_THRESHOLD && (p.k_min < 0 || !(p.tau_delta >= 0.f) || !isfinite(p.tau_delta)))
+  if (p.mode == BSA_ROUTE_THRESHOLD &&
+      (p.k_min < 0 || !(p.tau_delta >= 0.f) || !isfinite(p.tau_delta)))
     return BSA_ERR_INVALID_ARG;
   if (p.num_global < 0 || p.num_global > BSA_MAX_GLOBAL ||
       (p.num_global > 0 && p.global_blocks == nullptr))

@@ -9,9 +9,10 @@
 // Two passes so that every output element has one writer and no atomics touch the
 // gradients: the dQ pass walks the forward's worklist (row -> its key blocks); the
 // dK / dV pass walks the transposed index (key block -> the rows that selected
-// it, ascending), built here by a count, a scan and a row bitmap per key block.  Both passes recompute S
-// and dP.  Masks are the forward's: the causal triangle inside the diagonal block
-// and query rows past the sequence end or past the KV-head group.
+// it, ascending), built here from a row bitmap per key block, its population
+// counts and a scan.  Both passes recompute S and dP.  Masks are the forward's:
+// the causal triangle inside the diagonal block and query rows past the sequence
+// end or past the KV-head group.
 //
 // Operands sit in shared memory in the 128-byte-swizzled layout TMA writes: a
 // tile of R rows x 64 bf16 columns is R rows of 128 bytes, 16-byte chunk c of row
