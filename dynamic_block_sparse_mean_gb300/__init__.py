@@ -31,7 +31,7 @@ __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "Pref
            "attention_fwd", "attention_bwd", "causal_worklist", "coverage", "page_summaries",
            "page_summaries_append", "decode_paged", "check_status", "library_path",
            "PagedKVCache", "Chunk", "ChunkPlan", "chunk_append", "route_chunk",
-           "build_worklist_chunk", "attention_chunk"]
+           "build_worklist_chunk", "attention_chunk", "selftest_wait_timeout"]
 
 
 def library_path() -> str:
@@ -245,6 +245,13 @@ def causal_worklist(shape: PrefillShape, device, wl: Worklist | None = None, ws=
         ctypes.byref(s), _p(wl.row_ptr), _p(wl.col_idx), _p(wl.work), _p(wl.bucket_off), _p(ws),
         ws.numel(), _stream()))
     return wl
+
+
+def selftest_wait_timeout(dev_status):
+    """Run the bounded-wait self-test (bsa_selftest_wait_timeout): dev_status
+    receives BSA_ERR_TIMEOUT (19) and the context stays usable."""
+    check("bsa_selftest_wait_timeout",
+          _lib.lib().bsa_selftest_wait_timeout(_p(dev_status), _stream()))
 
 
 def coverage(lse_sparse, lse_dense, shape: PrefillShape, out=None):

@@ -77,6 +77,7 @@ PROTOTYPES = {
     "bsa_causal_worklist_capacity": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),
+    "bsa_selftest_wait_timeout": (I32, [V, V]),
     "bsa_chunk_append": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache), V, V, V, V]),
     "bsa_route_chunk_workspace_size": (SZ, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache),
                                             ctypes.POINTER(RouteParams)]),

@@ -122,6 +122,11 @@ const char *bsa_status_string(bsa_status_t s) {
   return "unknown status";
 }
 
+bsa_status_t bsa_selftest_wait_timeout(int32_t *dev_status, cudaStream_t stream) {
+  if (dev_status == nullptr) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_wait_timeout_selftest(dev_status, stream));
+}
+
 bsa_status_t bsa_block_summaries(const bsa_shape_t *shape, const void *K, float *C,
                                  cudaStream_t stream) {
   if (!shape_ok(shape) || K == nullptr || C == nullptr) return BSA_ERR_INVALID_ARG;

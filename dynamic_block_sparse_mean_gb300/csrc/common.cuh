@@ -94,8 +94,10 @@ BSA_DEV uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up when the
-// CTA-wide abort flag is raised or after kWaitCycles, recording a timeout.
-// Returns false when the caller must stop.
+// CTA-wide abort flag is raised or after kBudget cycles (kWaitCycles unless a
+// self-test asks for less), recording a timeout.  Returns false when the caller
+// must stop.
+template <long long kBudget = kWaitCycles>
 BSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_flag,
                        int32_t *status) {
 #pragma unroll 1
@@ -106,7 +108,7 @@ BSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_fl
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > kBudget) {
       set_status(status, BSA_ERR_TIMEOUT);
       *abort_flag = 1;
       return false;

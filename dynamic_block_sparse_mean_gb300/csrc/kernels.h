@@ -88,6 +88,8 @@ cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const v
                                     const int32_t *col_idx, const int32_t *work,
                                     const int32_t *bucket_off, float scale, void *dQ, void *dK,
                                     void *dV, void *ws, int32_t *dev_status, cudaStream_t st);
+// Bounded-wait self-test (selftest.cu).
+cudaError_t launch_wait_timeout_selftest(int32_t *dev_status, cudaStream_t st);
 // Backward of the sparse attention (attn_bwd.cu).
 size_t attention_bwd_workspace_bytes(const bsa_shape_t &s);
 cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void *K,

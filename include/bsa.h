@@ -432,6 +432,13 @@ bsa_status_t bsa_attention_chunk(const bsa_shape_t *shape, const bsa_kv_cache_t 
                                  float softmax_scale, void *O, float *lse, int32_t *dev_status,
                                  cudaStream_t stream);
 
+/* Self-test of the failure path: one small kernel waits, with the kernels' own
+ * bounded barrier wait and a budget of about 10 ms, on a barrier that nothing
+ * arrives at.  After the caller's synchronisation *dev_status holds
+ * BSA_ERR_TIMEOUT (if it was 0) and the context remains usable.  Touches no other
+ * state. */
+bsa_status_t bsa_selftest_wait_timeout(int32_t *dev_status, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *bsa_status_string(bsa_status_t status);
 
