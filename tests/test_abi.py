@@ -145,3 +145,32 @@ def test_chunk_calls_reject_bad_cache_descriptors(lib):
     a = [p16] * 5
     assert lib.bsa_attention_chunk(ctypes.byref(s), ctypes.byref(c), *a, ctypes.c_float(0.0), p16,
                                    null, null, null) == 1     # dev_status missing
+
+
+def test_backward_host_checks_and_workspace(lib):
+    null, p16 = None, ctypes.c_void_p(16)
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # bf16, head_dim 128: D [H, T] plus the key-major index (counts, list, offsets,
+    # buckets, a row bitmap of ceil(N_q / 32) words per key block, and the rows)
+    s = _shape(head_dim=128)                 # B 1, T 1024, H 2, H_kv 2, b 64, N_q 16
+    rows, W, pairs = 1 * 2 * 16, 1, 1 * 2 * 16 * 17 // 2
+    want = up(2 * 1024 * 4) + 2 * up(rows * 4) + up((rows + 1) * 4) + up(8 * 4) + up(rows * W * 4) \
+        + up(pairs * 4)
+    assert lib.bsa_attention_bwd_workspace_size(ctypes.byref(s)) == want
+    # fp32 or head_dim 64: D plus fp32 dK / dV accumulators
+    s64 = _shape()
+    kv = 2 * 1024 * 64 * 4
+    assert lib.bsa_attention_bwd_workspace_size(ctypes.byref(s64)) == up(2 * 1024 * 4) + 2 * up(kv)
+    args = [p16] * 10
+    assert lib.bsa_attention_bwd(ctypes.byref(s), *args, ctypes.c_float(0.0), p16, p16, p16,
+                                 null, p16, 1 << 30, null) == 1     # dev_status missing
+    assert lib.bsa_attention_bwd(ctypes.byref(s), *args, ctypes.c_float(0.0), p16, p16, p16,
+                                 p16, p16, 16, null) == 3           # workspace too small
+    assert lib.bsa_attention_bwd(ctypes.byref(s), *args, ctypes.c_float(0.0), p16, p16, p16,
+                                 p16, ctypes.c_void_p(16), 1 << 30, null) == 1   # ws not 256-aligned
+    assert lib.bsa_attention_bwd(ctypes.byref(_shape(head_dim=96)), *args, ctypes.c_float(0.0),
+                                 p16, p16, p16, p16, ctypes.c_void_p(256), 1 << 30, null) == 2
+
+
+def test_selftest_entry_rejects_missing_status(lib):
+    assert lib.bsa_selftest_wait_timeout(None, None) == 1
