@@ -7,7 +7,10 @@ prompt workload (n=32768, H=32 / H_kv=8, d=128, b=64, 32 blocks per row).
 The JSON line's value is the selected-tile TFLOP/s of the whole step; the
 router ms, stage times, the tensor-core roofline of the attention kernel, an
 end-to-end number from host buffers, the paged-decode KV GB/s on the 64-request
-decode workload, and the float64 oracle timed on the host cores ride along.
+decode workload, and the float64 oracle timed on the host cores ride along, as
+do three legs run outside the timed loop: router quality (coverage, density-1
+time, planted recall), the backward pass, and the same prompt as a chunked
+prefill over a paged KV cache.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
