@@ -527,3 +527,27 @@ def test_chunked_prefill_equals_single_pass():
             got = slice(ccu[i], ccu[i + 1])
             assert np.allclose(Oc[:, got], Oo[:, sl], rtol=0, atol=1e-12)
             assert np.allclose(lc[:, got], lo[:, sl], rtol=0, atol=1e-12)
+
+
+def test_chunked_prefill_union_threshold_equals_single_pass():
+    """The same chunk-by-chunk identity under threshold routing with a local window
+    and a global list (union routing): the chunk's rows use their logical block for
+    the window, the global ids and the threshold's candidate set."""
+    b, H, Hk, d = 32, 2, 1, 16
+    G = H // Hk
+    x = synth.gen_prefill([600], H, Hk, d, b, 41, "iid", "fp32")
+    Q, K, V = (getattr(x, n).astype(np.float64) for n in "qkv")
+    cu = x.cu_seqlens
+    kw = dict(k_min=2, tau_delta=1.5, force_sink=False, window=3, global_blocks=(1, 7))
+    Jo, co, _, _ = oracle.route(Q, K, cu, b, G, oracle.THRESHOLD, 8, **kw)
+    Oo, lo = oracle.attention(Q, K, V, cu, b, G, Jo, co)
+    kc, vc, bt = _paged_from_prompt(K, V, cu, b, 9)
+    for pre, n in ((0, 224), (224, 320), (544, 56)):
+        qc = Q[:, pre:pre + n]
+        Jc, cc, Oc, lc = oracle.chunked_prefill(qc, kc, vc, bt, [pre], [0, n], b, G,
+                                                oracle.THRESHOLD, 8, **kw)
+        nq, r0 = (n + b - 1) // b, pre // b
+        assert np.array_equal(cc[0, :, :nq], co[0, :, r0:r0 + nq])
+        assert np.array_equal(Jc[0, :, :nq], Jo[0, :, r0:r0 + nq])
+        assert np.allclose(Oc[:, :n], Oo[:, pre:pre + n], rtol=0, atol=1e-12)
+        assert np.allclose(lc[:, :n], lo[:, pre:pre + n], rtol=0, atol=1e-12)
