@@ -276,7 +276,11 @@ bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const vo
  *   q . page_summ[phys(p), h]; the best top_k (score desc, index asc) plus the
  *   last page L-1 are kept, ascending, in sel; the softmax (scale, default
  *   1/sqrt(d)) runs over the valid tokens of the kept pages.
- *   q        : [R, H, d] bf16.          k_cache, v_cache : [P, H_kv, page, d] bf16.
+ *   q        : [R, H, d] bf16.          k_cache, v_cache : [P, H_kv, page, d] bf16;
+ *              slots of a request's last page past its length must hold finite
+ *              values (zeros, as bsa_chunk_append leaves them): they are masked
+ *              out of the softmax but still meet P = 0 in the P.V product, where a
+ *              NaN or Inf would reach the output.
  *   page_summ: [P, H_kv, d] fp32.       block_table, context_lens as above.
  *   o        : [R, H, d] bf16.          lse : [R, H] fp32 (nullable).
  *   sel      : [R, H_kv, top_k + 1] int32 logical pages, -1 padded.
@@ -374,6 +378,8 @@ bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
  *   - J, counts, row_ptr and work are indexed by (i, h, q) like a prefill of the
  *     chunk; J holds logical block ids 0 .. r (routing, forced blocks and union
  *     parameters exactly as bsa_route with r the logical block).
+ *   - Page slots past a sequence's context must hold finite values; the append
+ *     zeroes them in the pages it writes (see bsa_decode_paged on why).
  * ------------------------------------------------------------------------- */
 typedef struct {
   void *k_cache;               /* [P, H_kv, 64, d] bf16                                */
