@@ -551,3 +551,25 @@ def test_chunked_prefill_union_threshold_equals_single_pass():
         assert np.array_equal(Jc[0, :, :nq], Jo[0, :, r0:r0 + nq])
         assert np.allclose(Oc[:, :n], Oo[:, pre:pre + n], rtol=0, atol=1e-12)
         assert np.allclose(lc[:, :n], lo[:, pre:pre + n], rtol=0, atol=1e-12)
+
+
+def test_decode_group_score_is_the_max_over_query_heads():
+    # Two query heads share one KV head (G = 2); d = 2, pages of 2 tokens, context 6.
+    # Page means c_0 = (0.9, 0), c_1 = (0.5, 0.5); page 2 is the last page.
+    # q_0 = (1, 0), q_1 = (-1, 2): scores q_h . c_p are
+    #   page 0: 0.9 and -0.9   (max 0.9, sum 0.0)
+    #   page 1: 0.5 and  0.5   (max 0.5, sum 1.0)
+    # so pooling by max keeps page 0, pooling by sum or mean would keep page 1.
+    q = np.array([[[1.0, 0.0], [-1.0, 2.0]]])                 # [R=1, H=2, d=2]
+    keys = np.array([[0.9, 0.0], [0.9, 0.0],
+                     [0.5, 0.5], [0.5, 0.5],
+                     [0.0, 0.0], [0.0, 0.0]])
+    kc = keys.reshape(3, 1, 2, 2)
+    vc = np.arange(12, dtype=np.float64).reshape(3, 1, 2, 2)
+    bt = np.array([[0, 1, 2]], dtype=np.int32)
+    _, _, sel, cnt, sc = oracle.decode(q, kc, vc, bt, np.array([6]), 2, top_k=1,
+                                       return_scores=True)
+    per_head = np.array([[0.9, 0.5], [-0.9, 0.5]])            # by hand, as above
+    assert np.allclose(sc[(0, 0)], per_head.max(axis=0))
+    assert list(sel[0, 0, :cnt[0, 0]]) == [0, 2]               # page 0 and the last page
+    assert per_head.sum(axis=0).argmax() == 1                  # a sum would have kept page 1
