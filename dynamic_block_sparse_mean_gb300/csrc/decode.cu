@@ -9,6 +9,12 @@
 //   attn    tensor cores: each unit of two selected pages gives a partial
 //           softmax (m, l, u) per query head (eqs.(3)-(5) within the unit)
 //   merge   combines the unit partials of a (request, KV head) into o and lse
+// Request lengths are checked on the device before any indexed access: a length
+// of 0 is an idle slot of a padded batch (no pages kept, o = 0, lse = -inf, no
+// error); a negative length or one past max_pages * 64 is BSA_ERR_CACHE with the
+// same empty result.  A block-table entry outside [0, num_phys_pages) is
+// BSA_ERR_CACHE too: its page scores -inf, and if it is still kept (fewer pages
+// than top_k) the attention reads zeros in its place.
 #include <algorithm>
 
 #include "common.cuh"
@@ -58,19 +64,32 @@ BSA_DEV void rs_step(float (&v)[64], int lane) {
   }
 }
 
+// A request length the decode accepts: 1 .. max_pages * page (0 is an idle slot).
+BSA_DEV bool len_ok(int len, int max_pages) { return len >= 1 && len <= max_pages * kPage; }
+
 template <int G>
 __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
     const uint16_t *__restrict__ q, const float *__restrict__ ps, const int32_t *__restrict__ bt,
-    const int32_t *__restrict__ lens, float *__restrict__ scores, int Hk, int max_pages) {
+    const int32_t *__restrict__ lens, float *__restrict__ scores, int32_t *status, int Hk,
+    int max_pages, int num_phys) {
   extern __shared__ __align__(16) float qs[];  // [H][kQStride]
   __shared__ int phys_s[64];
   const int rho = blockIdx.y;
   const int H = G * Hk;
-  const int L = (lens[rho] + kPage - 1) / kPage;
+  const int len = lens[rho];
+  if (!len_ok(len, max_pages)) return;  // reported by the select kernel
+  const int L = (len + kPage - 1) / kPage;
   const int p_begin = blockIdx.x * 64;
   if (p_begin >= L - 1) return;
   const int npg = min(L - 1, p_begin + 64) - p_begin;
-  if (threadIdx.x < npg) phys_s[threadIdx.x] = __ldg(bt + (size_t)rho * max_pages + p_begin + threadIdx.x);
+  if (threadIdx.x < npg) {
+    int ph = __ldg(bt + (size_t)rho * max_pages + p_begin + threadIdx.x);
+    if (ph < 0 || ph >= num_phys) {  // a stale or foreign page id: never read through it
+      set_status(status, BSA_ERR_CACHE);
+      ph = -1;
+    }
+    phys_s[threadIdx.x] = ph;
+  }
   for (int e = threadIdx.x; e < H * kD; e += blockDim.x)
     qs[(e / kD) * kQStride + e % kD] = bf16_to_f32(q[(size_t)rho * H * kD + e]);
   __syncthreads();
@@ -82,7 +101,9 @@ __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
 #pragma unroll
     for (int k = 0; k < 8; ++k) {  // a missing page of the last group repeats the first
       const int pg = p0 + k < npg ? p0 + k : p0;
-      c[k] = __ldg(reinterpret_cast<const float4 *>(ps + ((size_t)phys_s[pg] * Hk + h) * kD) + lane);
+      const int ph = phys_s[pg];
+      c[k] = ph >= 0 ? __ldg(reinterpret_cast<const float4 *>(ps + ((size_t)ph * Hk + h) * kD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float v[64];
 #pragma unroll
@@ -98,7 +119,8 @@ __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
     best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
     const int row = lane >> 2;
     if ((lane & 3) == 0 && p0 + row < npg)
-      scores[((size_t)rho * Hk + h) * max_pages + p_begin + p0 + row] = best;
+      scores[((size_t)rho * Hk + h) * max_pages + p_begin + p0 + row] =
+          phys_s[p0 + row] >= 0 ? best : -INFINITY;
   }
   grid_dep_launch();
 }
@@ -140,18 +162,26 @@ BSA_DEV int2 block_scan(int v, int *buf) {
 // grid (H_kv, R), one CTA per (request, KV head).
 __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
     const float *__restrict__ scores, const int32_t *__restrict__ lens, int32_t *__restrict__ sel,
-    int32_t *__restrict__ sel_counts, int Hk, int max_pages, int top_k) {
+    int32_t *__restrict__ sel_counts, int32_t *status, int Hk, int max_pages, int top_k) {
   extern __shared__ uint32_t keys[];  // max_pages
   __shared__ int hist[256];
   __shared__ int scan_buf[32];
   __shared__ int s_bin, s_above;
   const int rho = blockIdx.y, h = blockIdx.x;
-  const int L = (lens[rho] + 63) / 64;
+  int32_t *out = sel + ((size_t)rho * Hk + h) * (top_k + 1);
+  grid_dep_wait();  // scores come from the previous launch
+  const int len = lens[rho];
+  if (!len_ok(len, max_pages)) {  // idle (0) or invalid: no pages kept
+    if (len != 0 && h == 0 && threadIdx.x == 0) set_status(status, BSA_ERR_CACHE);
+    for (int e = threadIdx.x; e <= top_k; e += blockDim.x) out[e] = -1;
+    if (threadIdx.x == 0) sel_counts[(size_t)rho * Hk + h] = 0;
+    grid_dep_launch();
+    return;
+  }
+  const int L = (len + 63) / 64;
   const int N = L - 1;  // scored pages
   const float *sc = scores + ((size_t)rho * Hk + h) * max_pages;
-  int32_t *out = sel + ((size_t)rho * Hk + h) * (top_k + 1);
   const int k = min(top_k, N);
-  grid_dep_wait();  // scores come from the previous launch
   for (int e = threadIdx.x; e < N; e += blockDim.x) keys[e] = order_key(sc[e]);
   __syncthreads();
 
@@ -299,8 +329,19 @@ struct DecParams {
   float *part_ml, *part_o;
   int32_t *status;
   float scale_log2;
-  int H, Hk, G, max_pages, top_k, nchunk, units, oob_page;
+  int H, Hk, G, max_pages, top_k, nchunk, units, oob_page, num_phys;
 };
+
+// Tensor-map page coordinate (phys * H_kv + h) of logical page lp, or the
+// zero-filled out-of-range coordinate for an id outside the cache.
+BSA_DEV int dec_page_coord(const DecParams &p, int rho, int h, int lp) {
+  const int ph = __ldg(p.bt + (size_t)rho * p.max_pages + lp);
+  if (ph < 0 || ph >= p.num_phys) {
+    set_status(p.status, BSA_ERR_CACHE);
+    return p.oob_page;
+  }
+  return ph * p.Hk + h;
+}
 
 BSA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -382,17 +423,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (u < p.units) {
         const int pair = u / p.nchunk, c = u - pair * p.nchunk;
         const int cnt = __ldg(p.sel_counts + pair);
-        if (2 * c < cnt) {
+        const int rho = pair / p.Hk, h = pair - rho * p.Hk;
+        const int n = __ldg(p.lens + rho);
+        if (2 * c < cnt && len_ok(n, p.max_pages)) {
           live = true;
-          const int rho = pair / p.Hk, h = pair - rho * p.Hk;
-          const int n = __ldg(p.lens + rho);
           const int32_t *sp = p.sel + (size_t)pair * per_pair + 2 * c;
           const int lpA = __ldg(sp);
-          zA = __ldg(p.bt + (size_t)rho * p.max_pages + lpA) * p.Hk + h;
+          zA = dec_page_coord(p, rho, h, lpA);
           vA = min(kPage, n - lpA * kPage);
           if (2 * c + 1 < cnt) {
             const int lpB = __ldg(sp + 1);
-            zB = __ldg(p.bt + (size_t)rho * p.max_pages + lpB) * p.Hk + h;
+            zB = dec_page_coord(p, rho, h, lpB);
             vB = min(kPage, n - lpB * kPage);
           } else {
             zB = p.oob_page;  // zero-filled by the copy, keys masked
@@ -614,6 +655,12 @@ __global__ void __launch_bounds__(kMaxG * kD) dec_merge_kernel(
   const int pair = rho * Hk + h;
   grid_dep_wait();  // the partials come from the previous launch
   const int nu = (sel_counts[pair] + 1) / 2;
+  if (nu == 0) {  // no page kept (idle or invalid request): empty softmax
+    const int gg = threadIdx.x / kD, cc = threadIdx.x % kD, hq = h * G + gg;
+    o[((size_t)rho * H + hq) * kD + cc] = 0;
+    if (lse != nullptr && cc == 0) lse[(size_t)rho * H + hq] = -INFINITY;
+    return;
+  }
   const size_t u0 = (size_t)pair * nchunk;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp < G) {
@@ -704,7 +751,8 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
                              cudaFuncAttributeMaxDynamicSharedMemorySize, qs_bytes);          \
     if (e != cudaSuccess) return e;                                                           \
     dec_score_kernel<GG><<<sgrid, kScoreThreads, qs_bytes, st>>>(                             \
-        qb, page_summ, block_table, context_lens, scores, s.num_kv_heads, s.max_pages_per_req); \
+        qb, page_summ, block_table, context_lens, scores, dev_status, s.num_kv_heads,           \
+        s.max_pages_per_req, s.num_phys_pages);                                               \
   } while (0)
   switch (G) {
     case 1: BSA_DEC_SCORE(1); break;
@@ -723,7 +771,7 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
     if (e != cudaSuccess) return e;
   }
   e = launch_dependent(dec_select_kernel, dim3(s.num_kv_heads, s.num_reqs), dim3(kSelThreads), sm,
-                       st, scores, context_lens, sel, sel_counts, s.num_kv_heads,
+                       st, scores, context_lens, sel, sel_counts, dev_status, s.num_kv_heads,
                        s.max_pages_per_req, s.top_k);
   if (e != cudaSuccess) return e;
 
@@ -744,6 +792,7 @@ cudaError_t launch_decode(const bsa_decode_shape_t &s, const void *q, const void
   p.nchunk = nchunk;
   p.units = (int)units;
   p.oob_page = (int)zpages;
+  p.num_phys = s.num_phys_pages;
   auto *kern = G == 1 ? dec_tc_kernel<1> : G == 2 ? dec_tc_kernel<2> : G == 4 ? dec_tc_kernel<4>
                                                                               : dec_tc_kernel<8>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);

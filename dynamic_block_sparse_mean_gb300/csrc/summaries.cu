@@ -81,10 +81,11 @@ __global__ void __launch_bounds__(kThreads) block_summaries_kernel(
 }
 
 // grid (max_pages_per_req, R, H_kv): one CTA per (logical page p, request, KV head).
+// A page id outside [0, P) is skipped (nothing is read or written through it).
 __global__ void __launch_bounds__(kThreads) page_summaries_kernel(
     const uint16_t *__restrict__ kc, const int32_t *__restrict__ bt,
     const int32_t *__restrict__ lens, float *__restrict__ ps, int max_pages, int Hk, int page,
-    int d) {
+    int d, int P) {
   extern __shared__ float red[];
   const int p = blockIdx.x, rho = blockIdx.y, h = blockIdx.z;
   const int n = lens[rho];
@@ -92,21 +93,25 @@ __global__ void __launch_bounds__(kThreads) page_summaries_kernel(
   if (lo >= n) return;
   const int nrows = min(page, n - lo);
   const int phys = bt[(size_t)rho * max_pages + p];
+  if (phys < 0 || phys >= P) return;
   const uint16_t *base = kc + (((size_t)phys * Hk + h) * page) * d;
   block_mean<uint16_t>(base, nrows, d, d, ps + ((size_t)phys * Hk + h) * d, red);
 }
 
-// grid (R, H_kv), d threads: eq.(11) for the key each request just appended.
+// grid (R, H_kv), d threads: eq.(11) for the key each request just appended.  A
+// length past the block table, or a page id outside [0, P), skips the request.
 __global__ void page_summaries_append_kernel(const uint16_t *__restrict__ kc,
                                              const int32_t *__restrict__ bt,
                                              const int32_t *__restrict__ lens,
                                              float *__restrict__ psum, float *__restrict__ ps,
-                                             int max_pages, int Hk, int page, int d) {
+                                             int max_pages, int Hk, int page, int d, int P) {
   const int rho = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   const int n = lens[rho];  // keys after the append; the new one sits at n - 1
-  if (n < 1 || c >= d) return;
+  if (n < 1 || n > max_pages * page || c >= d) return;
   const int p = (n - 1) / page, slot = (n - 1) % page;
-  const size_t row = (size_t)bt[(size_t)rho * max_pages + p] * Hk + h;
+  const int phys = bt[(size_t)rho * max_pages + p];
+  if (phys < 0 || phys >= P) return;
+  const size_t row = (size_t)phys * Hk + h;
   const float k = bf16_to_f32(kc[(row * page + slot) * d + c]);
   const float sum = slot == 0 ? k : psum[row * d + c] + k;  // s <- s + k_t (a new page starts at k)
   psum[row * d + c] = sum;
@@ -188,7 +193,7 @@ cudaError_t launch_page_summaries_append(const bsa_decode_shape_t &s, const void
                                          float *page_summ, cudaStream_t st) {
   page_summaries_append_kernel<<<dim3(s.num_reqs, s.num_kv_heads), s.head_dim, 0, st>>>(
       static_cast<const uint16_t *>(k_cache), block_table, context_lens, page_sum, page_summ,
-      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim);
+      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim, s.num_phys_pages);
   return cudaGetLastError();
 }
 
@@ -216,7 +221,7 @@ cudaError_t launch_page_summaries(const bsa_decode_shape_t &s, const void *k_cac
   const size_t sm = (size_t)(kThreads / (s.head_dim / 8)) * s.head_dim * sizeof(float);
   page_summaries_kernel<<<grid, kThreads, sm, st>>>(
       static_cast<const uint16_t *>(k_cache), block_table, context_lens, page_summ,
-      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim);
+      s.max_pages_per_req, s.num_kv_heads, s.page_size, s.head_dim, s.num_phys_pages);
   return cudaGetLastError();
 }
 

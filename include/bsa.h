@@ -201,7 +201,10 @@ bsa_status_t bsa_build_worklist(const bsa_shape_t *shape, int32_t k_max, const i
  *    with BSA_ERR_UNSUPPORTED before anything is enqueued.
  *  - The first call on a device looks up that array's device address, with
  *    the caller's current device; make this first call before any stream
- *    capture.
+ *    capture.  The address is kept per device together with the CUDA context
+ *    it belongs to: a call from another context of that device (after a
+ *    cudaDeviceReset, or with a context of the caller's own made current)
+ *    looks it up again, so such a call too must come before any capture.
  *  - Every call uses the same array.  Calls ordered on one stream are safe;
  *    calls whose kernels may overlap on the GPU (different streams, or host
  *    threads issuing to one device without ordering) race on it and may all
@@ -242,8 +245,10 @@ bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const vo
  *   mean of the valid keys of that page.  Pages no request references are
  *   left untouched.
  *   k_cache     : [P, H_kv, page_size, d] bf16.
- *   block_table : [R, max_pages_per_req] int32 physical page ids.
- *   context_lens: [R] int32, 1 .. max_pages_per_req * page_size.
+ *   block_table : [R, max_pages_per_req] int32 physical page ids; an id outside
+ *                 [0, P) is skipped (nothing is read or written through it).
+ *   context_lens: [R] int32, 1 .. max_pages_per_req * page_size (pages past the
+ *                 block table are not summarised; 0 skips a request).
  *   page_summ   : [P, H_kv, d] fp32.
  * ------------------------------------------------------------------------- */
 bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_cache,
@@ -261,7 +266,9 @@ bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_c
  *               valid for its keys before the append, e.g. built by appending
  *               from an empty page);
  *   page_summ : [P, H_kv, d] fp32 means, as bsa_page_summaries writes them.
- *   context_lens : [R] int32, counts after the append (>= 1; 0 skips a request).
+ *   context_lens : [R] int32, counts after the append (>= 1; 0 skips a request,
+ *               and so does a count past max_pages_per_req * page_size or a page id
+ *               outside [0, P)).
  * ------------------------------------------------------------------------- */
 bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const void *k_cache,
                                        const int32_t *block_table, const int32_t *context_lens,
@@ -286,6 +293,15 @@ bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const vo
  *   sel      : [R, H_kv, top_k + 1] int32 logical pages, -1 padded.
  *   sel_counts : [R, H_kv] int32.
  *   ws       : at least bsa_decode_workspace_size() bytes, 256-byte aligned.
+ *   Lengths and page ids are checked on the device before they index anything:
+ *   - context_lens[rho] == 0 is an idle slot (a padded batch): sel row all -1,
+ *     count 0, o = 0, lse = -inf, no error.
+ *   - a length < 0 or > max_pages_per_req * page_size gives the same empty result
+ *     and sets BSA_ERR_CACHE in dev_status (nullable: then not reported).
+ *   - a block_table entry outside [0, num_phys_pages) sets BSA_ERR_CACHE; that
+ *     page scores -inf, and where it is still kept (a request with at most top_k
+ *     scored pages) the attention reads zeros in its place.  Other requests are
+ *     unaffected.
  * ------------------------------------------------------------------------- */
 size_t bsa_decode_workspace_size(const bsa_decode_shape_t *shape);
 bsa_status_t bsa_decode_paged(const bsa_decode_shape_t *shape, const void *q,

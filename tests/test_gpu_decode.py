@@ -82,3 +82,69 @@ def test_streaming_page_summaries_follow_eq11():
                 want = oracle.streaming_summary(keys[h])[-1]
                 assert np.abs(sg[phys, h] - want).max() < 1e-5
                 assert np.abs(sg[phys, h] - bg[phys, h]).max() < 1e-5
+
+
+BSA_ERR_CACHE = 20
+
+
+def _run_plan(x, top_k, cl=None, bt=None):
+    q, kc, vc, bt0, cl0 = _upload(x)
+    bt = bt0 if bt is None else torch.as_tensor(bt, device="cuda")
+    cl = cl0 if cl is None else torch.as_tensor(np.asarray(cl, dtype=np.int32), device="cuda")
+    ps = bsa.page_summaries(kc, bt, cl)
+    R, H, d = q.shape
+    P, Hk, page, _ = kc.shape
+    plan = bsa.DecodePlan(R, H, Hk, d, page, bt.shape[1], P, top_k)
+    plan.sel.fill_(777)                      # sentinel: every row must be rewritten
+    plan.sel_counts.fill_(777)
+    plan.run(q, kc, vc, ps, bt, cl)
+    torch.cuda.synchronize()
+    return (plan.out.float().cpu().numpy(), plan.lse.cpu().numpy(), plan.sel.cpu().numpy(),
+            plan.sel_counts.cpu().numpy(), int(plan.status.item()))
+
+
+def _assert_empty(o, lse, sel, cnt, rho):
+    assert (cnt[rho] == 0).all() and (sel[rho] == -1).all()
+    assert (o[rho] == 0).all() and np.isneginf(lse[rho]).all()
+
+
+def test_decode_idle_and_invalid_lengths():
+    """Length 0 is an idle slot (empty result, no error); a length past the block
+    table is BSA_ERR_CACHE with the same empty result; neighbours are exact."""
+    max_pages = 30
+    lens = [700, 0, 1500, 200]
+    x = synth.gen_decode(lens, 8, 2, 128, 64, seed=61, max_pages=max_pages)
+    o, lse, sel, cnt, st = _run_plan(x, 8)
+    assert st == 0
+    _assert_empty(o, lse, sel, cnt, 1)
+    check_decode(x, 8, o, lse, sel, cnt, [0, 2, 3], 4)
+
+    bad = [700, 0, 1500, max_pages * 64 + 1]     # request 3 overruns its block-table row
+    o, lse, sel, cnt, st = _run_plan(x, 8, cl=bad)
+    assert st == BSA_ERR_CACHE
+    _assert_empty(o, lse, sel, cnt, 1)
+    _assert_empty(o, lse, sel, cnt, 3)
+    check_decode(x, 8, o, lse, sel, cnt, [0, 2], 4)
+
+    neg = [700, -5, 1500, 200]
+    o, lse, sel, cnt, st = _run_plan(x, 8, cl=neg)
+    assert st == BSA_ERR_CACHE
+    _assert_empty(o, lse, sel, cnt, 1)
+    check_decode(x, 8, o, lse, sel, cnt, [0, 2, 3], 4)
+
+
+def test_decode_page_id_outside_cache():
+    """A block-table entry outside [0, P) is reported and never read through: as a
+    scored page it scores -inf (not kept); as a kept page it reads zeros."""
+    x = synth.gen_decode([900, 2000, 300], 8, 2, 128, 64, seed=62)
+    P = x.k_cache.shape[0]
+    bt = x.block_table.copy()
+    bt[1, 3] = P + 5            # request 1: a scored page among 31 (top 8 kept)
+    bt[2, 1] = -7               # request 2: 5 pages, all kept (4 scored <= top_k)
+    o, lse, sel, cnt, st = _run_plan(x, 8, bt=bt)
+    assert st == BSA_ERR_CACHE
+    check_decode(x, 8, o, lse, sel, cnt, [0], 4)
+    for h in range(2):
+        assert 3 not in sel[1, h, :cnt[1, h]].tolist()
+        assert sel[2, h, :cnt[2, h]].tolist() == [0, 1, 2, 3, 4]
+    assert np.isfinite(o[1:]).all() and np.isfinite(lse[1:]).all()
