@@ -5,6 +5,8 @@
 //   2. scan kernel   row_ptr by prefix sum, and the work list: a stable counting
 //                    sort of rows by capacity bucket, largest first (one CTA)
 //   3. fill kernel   copies the block ids into col_idx (grid-wide)
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -237,22 +239,45 @@ __device__ __align__(256) int32_t g_noalloc_rows[BSA_WORKLIST_NOALLOC_MAX_ROWS];
 
 }  // namespace
 
-// Device address of g_noalloc_rows on the current device, looked up once per
-// device (with that device current) and cached.
+// The driver's cuCtxGetCurrent, reached through the runtime (no libcuda link).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+  });
+  return fn;
+}
+
+// Device address of g_noalloc_rows on the current device, looked up with that
+// device current and cached per device together with the CUDA context it was
+// looked up in.  A call from another context of the device (the caller reset
+// the device, or made its own context current) looks the address up again.
 cudaError_t worklist_noalloc_scratch(int32_t **out) {
   constexpr int kMaxDevices = 64;
   static int32_t *cache[kMaxDevices] = {nullptr};
+  static CUcontext cache_ctx[kMaxDevices] = {nullptr};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CUcontext ctx = nullptr;
+  auto get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == nullptr) {
+  if (ctx == nullptr || cache[dev] == nullptr || cache_ctx[dev] != ctx) {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_rows);
+    e = cudaGetSymbolAddress(&p, g_noalloc_rows);  // makes the device's context current
     if (e != cudaSuccess) return e;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorUnknown;
     cache[dev] = static_cast<int32_t *>(p);
+    cache_ctx[dev] = ctx;
   }
   *out = cache[dev];
   return cudaSuccess;

@@ -102,3 +102,50 @@ def _lib_max_rows():
     hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "include", "bsa.h")).read()
     return eval(re.search(r"#define BSA_WORKLIST_NOALLOC_MAX_ROWS \((.*?)\)", hdr).group(1))
+
+
+def _sparse_index_at_cap(S, Hk, Nq, seed):
+    """J / counts for S sequences x Hk KV heads x Nq blocks: each row holds up to
+    three history blocks below its diagonal at random gaps, plus the diagonal;
+    5 % of rows are left empty (they fall back to the diagonal)."""
+    rng = np.random.default_rng(seed)
+    r = np.broadcast_to(np.arange(Nq), (S, Hk, Nq))
+    gaps = np.cumsum(1 + rng.integers(0, 40, size=(S, Hk, Nq, 3)), axis=-1)   # d1 < d2 < d3
+    hist = r[..., None] - gaps[..., ::-1]                                      # ascending
+    ids = np.concatenate([np.where(hist >= 0, hist, -1), r[..., None]], axis=-1)
+    key = np.where(ids >= 0, ids, np.iinfo(np.int32).max)                     # -1s to the end
+    ids = np.take_along_axis(ids, np.argsort(key, axis=-1, kind="stable"), axis=-1)
+    cnt = (ids >= 0).sum(-1)
+    empty = rng.random((S, Hk, Nq)) < 0.05
+    ids[empty] = -1
+    cnt[empty] = 0
+    return ids.astype(np.int32), cnt.astype(np.int32)
+
+
+def test_noalloc_worklist_at_its_row_limit():
+    """A shape with exactly BSA_WORKLIST_NOALLOC_MAX_ROWS rows is accepted and gives
+    the workspace version's worklist."""
+    S, Hk, b, k_max = 4, 8, 64, 4
+    Nq = _lib_max_rows() // (S * Hk)
+    assert S * Hk * Nq == _lib_max_rows()
+    J, cnt = _sparse_index_at_cap(S, Hk, Nq, seed=3)
+    cu = np.arange(S + 1, dtype=np.int64) * Nq * b
+    sh = bsa.PrefillShape.make(cu, Hk, Hk, 64, b)
+    assert sh.num_rows == _lib_max_rows()
+    s = sh.c()
+    dJ, dc = torch.as_tensor(J, device="cuda"), torch.as_tensor(cnt, device="cuda")
+    lib = _lib.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    ref = _buffers(sh.num_rows, k_max)
+    ws = torch.empty(max(256, lib.bsa_worklist_workspace_size(ctypes.byref(s), k_max)),
+                     dtype=torch.uint8, device="cuda")
+    assert lib.bsa_build_worklist(ctypes.byref(s), k_max, p(dJ), p(dc), *(p(t) for t in ref),
+                                  p(ws), ws.numel(), stream) == 0
+    got = _buffers(sh.num_rows, k_max)
+    assert lib.bsa_build_worklist_noalloc(ctypes.byref(s), k_max, p(dJ), p(dc),
+                                          *(p(t) for t in got), stream) == 0
+    torch.cuda.synchronize()
+    _assert_same(ref, got)
+    rp = ref[0].cpu().numpy()
+    assert rp[-1] == int(np.maximum(cnt, 1).sum())     # empty rows became {r}
