@@ -52,7 +52,10 @@ torch.nn.functional.scaled_dot_product_attention when every causal block is
 selected; tile-order invariance; a duplicate block changes the multiset result;
 empty row equals {r}; GQA permutation; brute force on tiny inputs; the error
 bound of [P2] §4; the online-softmax recurrences against the direct softmax;
-eq.(11) streaming means; the worked budget numbers of [P2] §2.2 (golden file).
+eq.(11) streaming means; the worked budget numbers of [P2] §2.2 (golden file);
+token recall against the dense top-t teacher worked by hand (ties, GQA, an
+empty row), equal to 1 at density 1 and to the explicit mask's key count when
+the teacher covers every visible key.
 """
 from __future__ import annotations
 
@@ -480,6 +483,40 @@ def coverage(Q, K, cu_seqlens, b: int, G: int, J, counts, rows=None, scale=None)
                 inside = np.isin(np.arange(t + 1) // b, np.asarray(sel))
                 C[hq, s0 + t] = float(a[inside].sum())
     return C
+
+
+def dense_scores(q, Kseq, t: int):
+    """Unscaled dense scores q . k_s of one query at sequence position t over its
+    visible keys s = 0 .. t (the softmax scale does not change their order)."""
+    return np.asarray(Kseq[:t + 1], dtype=np.float64) @ np.asarray(q, dtype=np.float64)
+
+
+def token_recall(Q, K, cu_seqlens, b: int, G: int, J, counts, t_top: int, queries):
+    """Token recall@t against the dense teacher ([P2] §1.1, the paragraph on
+    recall@k: G_i = the dense attention's top-t keys of query i, N(i) = its
+    candidate keys, token recall = |G_i ∩ N(i)| / |G_i|; the physical tile
+    budget is reported beside it).
+
+    queries: (query head hq, packed token index) pairs.  For query i at sequence
+    position t, G_i holds the min(t_top, t + 1) visible keys (s <= t, same
+    sequence) of largest dense score, ranked by (score desc, index asc) (R-6);
+    N(i) holds the visible keys whose block is in the J row (i, hq // G, t // b),
+    an empty row keeping its diagonal (R-7).  Returns {(hq, token): (|G_i ∩ N(i)|,
+    |G_i|)}."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = {}
+    for hq, tok in queries:
+        i = int(np.searchsorted(cu, tok, side="right") - 1)
+        s0 = int(cu[i])
+        t = int(tok) - s0
+        h, r = hq // G, t // b
+        cnt = int(counts[i, h, r])
+        sel = set(int(x) for x in J[i, h, r, :cnt]) or {r}
+        g = dense_scores(Q[hq, tok], K[h, s0:s0 + t + 1], t)
+        top = rank_order(g, np.arange(t + 1))[:t_top]
+        hits = sum(1 for s in top if int(s) // b in sel)
+        out[(int(hq), int(tok))] = (hits, len(top))
+    return out
 
 
 def dense_causal_pairs(n: int) -> int:

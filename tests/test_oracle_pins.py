@@ -273,6 +273,71 @@ def test_coverage_matches_library_logsumexp_and_limits():
     assert (Cb[ok] >= C[ok] - 1e-12).all()
 
 
+def _recall_hand_case():
+    """n = 8, b = 2 (4 blocks), d = 1, H = 4 query heads over H_kv = 2 (G = 2), all
+    queries 1.0, so a query's dense scores are the keys themselves."""
+    K = np.zeros((2, 8, 1))
+    K[0, :, 0] = [0.5, 3.0, 2.0, -1.0, 4.0, 0.1, 2.5, 1.0]
+    K[1, :, 0] = [1.0, 1.0, 1.0, 1.0, 0.0, 0.0, 0.0, 0.0]      # ties at the top
+    Q = np.ones((4, 8, 1))
+    J = np.full((1, 2, 4, 4), -1)
+    cnt = np.zeros((1, 2, 4), dtype=np.int64)
+    for h in range(2):
+        for r in range(4):
+            J[0, h, r, 0], cnt[0, h, r] = r, 1                  # diagonal only
+    J[0, 0, 3, :2], cnt[0, 0, 3] = [1, 3], 2
+    J[0, 1, 3, :2], cnt[0, 1, 3] = [0, 3], 2
+    cnt[0, 0, 2] = 0                                            # empty row -> {2}
+    return Q, K, J, cnt
+
+
+def test_token_recall_hand_worked_cases():
+    # Top-3 teacher (P2 §1.1 recall paragraph), worked by hand:
+    #  KV head 0, token 7: scores 0..7 = K0 -> top-3 {4, 1, 6}; N = blocks {1, 3} =
+    #   keys {2, 3, 6, 7} -> 1 hit.  token 6: visible 0..6 (itself included) -> top-3
+    #   {4, 1, 6}, 1 hit.  token 5: empty row -> block {2} = keys {4, 5}; top-3
+    #   {4, 1, 2} -> 1 hit.  token 1: only 2 visible keys, |G| = 2, both in block 0.
+    #  KV head 1 (all visible scores tie at 1.0 up to key 3): token 7 -> top-3 by
+    #   lower index {0, 1, 2}; N = blocks {0, 3} = {0, 1, 6, 7} -> 2 hits.  token 3:
+    #   N = block {1} = {2, 3}; top-3 {0, 1, 2} -> 1 hit.
+    Q, K, J, cnt = _recall_hand_case()
+    want = {7: (1, 3), 6: (1, 3), 5: (1, 3), 1: (2, 2)}
+    want1 = {7: (2, 3), 3: (1, 3)}
+    for hq in range(4):     # query heads 0, 1 share KV head 0; 2, 3 share KV head 1
+        table = want if hq < 2 else want1
+        got = oracle.token_recall(Q, K, [0, 8], 2, 2, J, cnt, 3, [(hq, t) for t in table])
+        assert {t: got[(hq, t)] for t in table} == table
+
+
+def test_token_recall_limits_and_monotonicity():
+    x, Q, K, V = _inputs([300, 200], 4, 2, 32, 64, seed=33)
+    G, b, t_top = 2, 64, 16
+    rng = np.random.default_rng(5)
+    queries = [(int(rng.integers(4)), int(rng.integers(500))) for _ in range(60)]
+    # every causal block selected: the teacher is always inside the candidate set
+    Ja, ca = oracle.causal_all_blocks(x.cu_seqlens, b, 2)
+    for (hq, tok), (hits, gs) in oracle.token_recall(Q, K, x.cu_seqlens, b, G, Ja, ca, t_top,
+                                                     queries).items():
+        assert hits == gs == min(t_top, tok - (0 if tok < 300 else 300) + 1)
+    # a teacher larger than the visible keys is the whole visible set: hits = the
+    # query's allowed keys under the explicit mask of the row
+    Jo, co, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 2)
+    big = oracle.token_recall(Q, K, x.cu_seqlens, b, G, Jo, co, 10 ** 6, queries)
+    info = oracle.seq_info(x.cu_seqlens, b)
+    for (hq, tok), (hits, gs) in big.items():
+        i = 0 if tok < 300 else 1
+        s0, n, nb = info[i]
+        t = tok - s0
+        r = t // b
+        mult = oracle.block_multiplicity(Jo[i, hq // G, r, :co[i, hq // G, r]], nb, r)
+        assert gs == t + 1 and hits == int(oracle.key_mask(t, t + 1, mult, b).sum())
+    # more blocks never lose a teacher key
+    small = oracle.token_recall(Q, K, x.cu_seqlens, b, G, Jo, co, t_top, queries)
+    Jb, cb, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 4)
+    large = oracle.token_recall(Q, K, x.cu_seqlens, b, G, Jb, cb, t_top, queries)
+    assert all(large[q][0] >= small[q][0] for q in small)
+
+
 def test_backward_matches_central_differences():
     # d/dx sum(O * dO) by central differences of the forward oracle, for random
     # entries of Q, K and V (independent of autograd).
