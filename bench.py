@@ -2,17 +2,21 @@
 """Benchmark of the block-sparse attention hot path on GB300.
 
 One step = one pass of the prefill path over one batch: block summaries,
-router (scores + selection), worklist, sparse attention — on the 32k-token
-prompt workload (n=32768, H=32 / H_kv=8, d=128, b=64, 32 blocks per row).
-The JSON line's value is the selected-tile TFLOP/s of the whole step; the
-router ms, stage times, the tensor-core roofline of the attention kernel, an
-end-to-end number from host buffers, the paged-decode KV GB/s on the 64-request
-decode workload, and the float64 oracle timed on the host cores ride along, as
-do three legs run outside the timed loop: router quality (coverage, density-1
-time, planted recall), the backward pass, and the same prompt as a chunked
-prefill over a paged KV cache.
+router (scores + selection), worklist, sparse attention.  The headline line is
+the 128k-token prompt (n=131072, H=64 / H_kv=8, d=128, b=128, top-16 + sink +
+diagonal), the largest single-GPU workload; its value is the selected-tile
+TFLOP/s of the whole step.  The same line carries, per prefill workload (tiny,
+32k prompt, variable-length batch, 128k prompt), the step time, router ms,
+stage times, the roofline of the attention kernel (tensor), of the router
+(HBM and tensor) and of the summaries kernel (HBM), and the speedup over the
+same kernel at density 1; the paged-decode KV GB/s on the 64-request decode
+workload; an end-to-end number from host buffers; the float64 oracle timed on
+the host cores; and legs run outside the timed loop: router quality
+(coverage, token recall against the dense top-t teacher, planted recall), the
+backward pass, and the 32k prompt as a chunked prefill over a paged KV cache.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload long|prompt|varlen|tiny] [--configs tiny,prompt,varlen|none]
 """
 from __future__ import annotations
 
@@ -20,7 +24,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -39,10 +42,10 @@ sys.path.insert(0, ROOT)
 METRIC = "block-sparse attn TFLOP/s on selected tiles + router ms; decode KV GB/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_ATTN = {name: os.path.join(ROOT, "profiles", f"attn_tc_{tag}.md")
-                for name, tag in (("prompt", "prompt32k"), ("varlen", "varlen256k"),
-                                  ("long", "long128k"), ("tiny", "tiny"))}
-ATTN_SOURCE = os.path.join(ROOT, "dynamic_block_sparse_mean_gb300", "csrc", "attn_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "dynamic_block_sparse_mean_gb300", "csrc")
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD_KEYS = ("tiny", "prompt", "varlen", "long")
 
 
 def parse_args(argv=None):
@@ -51,7 +54,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="prompt", choices=["tiny", "prompt", "varlen", "long"])
+    ap.add_argument("--workload", default="long", choices=list(WORKLOAD_KEYS),
+                    help="the headline workload (default: the 128k prompt, the largest)")
+    ap.add_argument("--configs", default="tiny,prompt,varlen",
+                    help="other prefill workloads timed into the same line ('none': skip)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -161,18 +167,21 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(path: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM read + write bytes per launch of `kernel` on `workload` from the
+    committed ncu record (profiles/dram_traffic.json), if the kernel's source file
     is unchanged since the counters were taken (else None)."""
-    if not os.path.exists(path):
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    txt = open(path).read()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_sha or not m_tr:
-        return None
-    sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
-    return float(m_tr.group(1)) if sha == m_sha.group(1) else None
+    for rec in json.load(open(TRAFFIC_FILE)).get("records", []):
+        if rec.get("kernel") != kernel or rec.get("workload") != workload:
+            continue
+        src = os.path.join(CSRC, rec["source"])
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return float(rec["dram_bytes_per_launch"]) if sha == rec.get("source_sha256") else None
+    return None
 
 
 # ---------------------------------------------------------------- workloads
@@ -197,31 +206,49 @@ def bench_prefill(w, steps, warmup, device, world, sampler):
     plan = bsa.PrefillPlan(x.cu_seqlens, w.num_heads, w.num_kv_heads, w.head_dim, w.block,
                            bsa.RouteParams(w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink),
                            device=device)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    # Inputs smaller than twice the L2 would be served from it on repeated steps:
+    # then every step is preceded by a write of a buffer larger than the L2.
+    flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+             if in_bytes < 2 * L2_BYTES else None)
     for _ in range(max(3, warmup)):
         plan.run(q, k, v)
     torch.cuda.synchronize(device)
     bsa.check_status(plan.status)
 
-    # The timed loop: whole steps back to back, events only around the loop (an event
-    # between two launches would also cut the programmatic dependent launch that
-    # lets each kernel's set-up overlap its predecessor).
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world, device)
     torch.cuda.synchronize(device)
     sampler.start()
-    t0.record()
-    for s in range(steps):
-        plan.run(q, k, v)
-    t1.record()
-    torch.cuda.synchronize(device)
+    if flush is None:
+        # The timed loop: whole steps back to back, events only around the loop (an
+        # event between two launches would also cut the programmatic dependent launch
+        # that lets each kernel's set-up overlap its predecessor).
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for s in range(steps):
+            plan.run(q, k, v)
+        t1.record()
+        torch.cuda.synchronize(device)
+        total_ms = t0.elapsed_time(t1)
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for s in range(steps):
+            flush.zero_()
+            ev[s][0].record()
+            plan.run(q, k, v)
+            ev[s][1].record()
+        torch.cuda.synchronize(device)
+        total_ms = sum(a.elapsed_time(b_) for a, b_ in ev)
     clocks = sampler.stop()
     barrier(world, device)
     bsa.check_status(plan.status)
-    total_ms = t0.elapsed_time(t1)
     # Stage breakdown: a second loop with events between the ABI calls.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     for s in range(steps):
         e = ev[s]
+        if flush is not None:
+            flush.zero_()
         e[0].record()
         plan.summaries(k)
         e[1].record()
@@ -244,7 +271,12 @@ def bench_prefill(w, steps, warmup, device, world, sampler):
     eff = accounting.effective_pairs(J, counts, x.cu_seqlens, w.block, G) * 4.0 * w.head_dim
     tiles = counts[counts > 0]
     launches = sum(bsa.PrefillPlan.LAUNCHES.values()) * steps
-    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, steps=steps, stages=st,
+    l2 = ("inputs larger than L2 (Q+K+V %.0f MB > 129 MB); no flush" % (in_bytes / 1e6)
+          if flush is None else
+          "L2 flushed before every step (write of %.0f MB); Q+K+V %.1f MB" %
+          (flush.numel() * 4 / 1e6, in_bytes / 1e6))
+    del flush
+    res = dict(x=x, plan=plan, q=q, k=k, v=v, total_ms=total_ms, steps=steps, stages=st, l2=l2,
                flops=flops, eff_flops=eff, clocks=clocks, launches=launches, T=T,
                tiles={"min": int(tiles.min()), "mean": float(tiles.mean()), "max": int(tiles.max()),
                       "total": int(counts.sum())},
@@ -302,7 +334,47 @@ def router_quality(res, w, device):
         out["planted_recall"] = hit / len(x.planted)
         out["planted_pairs"] = len(x.planted)
     del Od, ld, C, dense
+    out["recall_at_k"] = token_recall_leg(res, w, device)
     return out
+
+
+def token_recall_leg(res, w, device, t_top=64, max_tiles=20000, sample=2048):
+    """Token recall of the routed rows against the dense top-t teacher (the recall@k
+    paragraph of 2.1 §1.1), with the physical budget beside it: every query of the
+    batch when it has at most max_tiles 64-query tiles, else a seeded sample."""
+    import dynamic_block_sparse_mean_gb300 as bsa
+    plan, q, k, x = res["plan"], res["q"], res["k"], res["x"]
+    sh = plan.shape
+    per = bsa.recall_tiles_per_seq(sh)
+    cu = np.asarray(x.cu_seqlens, dtype=np.int64)
+    lens = np.diff(cu)
+    valid = [(i * w.num_heads + hq) * per + c for i in range(len(lens))
+             for hq in range(w.num_heads) for c in range((int(lens[i]) + 63) // 64)]
+    tiles = None
+    if len(valid) > max_tiles:
+        pick = np.sort(np.random.default_rng(77).choice(len(valid), size=sample, replace=False))
+        tiles = torch.as_tensor(np.asarray(valid, dtype=np.int32)[pick], device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    hits = bsa.token_recall(q, k, plan.J, plan.counts, sh, t_top, tiles=tiles, dev_status=st)
+    t1.record()
+    torch.cuda.synchronize(device)
+    bsa.check_status(st)
+    pos = np.concatenate([np.arange(n) for n in lens])
+    gsize = np.minimum(t_top, pos + 1)[None, :]
+    h = hits.cpu().numpy()
+    got = h >= 0
+    rec = (h / gsize)[got]
+    qs = np.quantile(rec, [0.001, 0.01, 0.05, 0.5])
+    return {"t": t_top, "mean": float(rec.mean()), "min": float(rec.min()), "p0.1": float(qs[0]),
+            "p1": float(qs[1]), "p5": float(qs[2]), "p50": float(qs[3]),
+            "queries": int(got.sum()),
+            "sample": "all queries" if tiles is None else
+                      f"{sample} random 64-query tiles of {len(valid)} (seed 77)",
+            "physical_tiles_per_row_mean": res["tiles"]["mean"],
+            "physical_keys_per_query_max": res["tiles"]["mean"] * w.block,
+            "kernel_ms": t0.elapsed_time(t1)}
 
 
 def bench_backward(res, w, device, reps=3):
@@ -413,35 +485,36 @@ def bench_chunked(res, w, device, chunk_tokens=8192, reps=3):
             "launches_per_prompt": nsteps * sum(bsa.ChunkPlan.LAUNCHES.values())}
 
 
-def bench_e2e(res, steps, device):
-    """Same metric through PrefillPlan.run with host (pinned) buffers: every step
-    copies Q, K, V host -> device and reads O back device -> host."""
-    x, plan = res["x"], res["plan"]
+def bench_e2e(res, w, steps, device):
+    """Same metric through the public host-buffer API (bsa.HostPrefill): every step
+    uploads Q, K, V from pinned host memory and downloads O into pinned host
+    memory; the copies of neighbouring steps overlap the current step's kernels
+    (two device slots, one stream per copy direction)."""
+    import dynamic_block_sparse_mean_gb300 as bsa
+    x = res["x"]
     hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
                   for a in (x.q, x.k, x.v))
-    dq, dk, dv = (torch.empty(t.shape, dtype=torch.bfloat16, device=device) for t in (hq, hk, hv))
-    ho = torch.empty(plan.out.shape, dtype=torch.bfloat16).pin_memory()
-
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        out, _ = plan.run(dq, dk, dv)
-        ho.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize(device)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        step()
-    t1.record()
-    torch.cuda.synchronize(device)
-    ms = t0.elapsed_time(t1) / steps
+    ho = [torch.empty(hq.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    pipe = bsa.HostPrefill(x.cu_seqlens, w.num_heads, w.num_kv_heads, w.head_dim, w.block,
+                           bsa.RouteParams(w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink),
+                           device=device)
+    for s in range(3):
+        pipe.submit(hq, hk, hv, ho[s % 2])
+    pipe.synchronize()
+    for st in pipe.status:
+        bsa.check_status(st)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        pipe.submit(hq, hk, hv, ho[s % 2])
+    pipe.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    for st in pipe.status:
+        bsa.check_status(st)
+    same = bool(torch.equal(ho[(steps - 1) % 2], res["plan"].out.cpu()))
     bi = sum(t.numel() * 2 for t in (hq, hk, hv))
-    bo = ho.numel() * 2
-    return ms, bi, bo
+    bo = ho[0].numel() * 2
+    del pipe, ho, hq, hk, hv
+    return ms, bi, bo, same
 
 
 def bench_decode(steps, warmup, device, num_reqs=None):
@@ -574,6 +647,95 @@ def decode_entry(args, device, peaks, src):
                          "frac": gbs / hbm, "peak_source": f"{src} copy bandwidth"}}
 
 
+def stage_rooflines(res, w, peaks, src):
+    """Roofline objects of the attention kernel (tensor), the router call (HBM and
+    tensor) and the summaries kernel (HBM) from the stage times of one workload."""
+    from dynamic_block_sparse_mean_gb300 import accounting
+    st = res["stages"]
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    x = res["x"]
+    nblocks = int(sum((int(x.cu_seqlens[i + 1] - x.cu_seqlens[i]) + w.block - 1) // w.block
+                      for i in range(len(x.cu_seqlens) - 1)))
+    Nq = res["plan"].shape.max_blocks
+    attn_kernel = f"attn_tc_kernel<{w.head_dim},{w.block}>"
+    attn_tf = res["flops"] / (st["attention"] * 1e-3) / 1e12
+    attention = {"bound": "tensor", "kernel": attn_kernel, "achieved": attn_tf, "peak": bf16,
+                 "unit": "TFLOP/s", "frac": attn_tf / bf16,
+                 "peak_source": f"{src} bf16 burst",
+                 "traffic": recorded_traffic(attn_kernel, w.name),
+                 "algorithmic_flops_per_launch": res["flops"],
+                 "compulsory_bytes_per_launch": res["attn_bytes"]}
+    rb = accounting.router_bytes(w.num_heads, w.num_kv_heads, res["T"], w.head_dim,
+                                 w.num_seqs, Nq, w.k_max)
+    r_gbs = rb / (st["route"] * 1e-3) / 1e9
+    r_tf = res["router_flops"] / (st["route"] * 1e-3) / 1e12
+    router = {"ms": st["route"],
+              "hbm": {"bound": "hbm", "kernel": "bsa_route (split + scores + select)",
+                      "achieved": r_gbs, "peak": hbm, "unit": "GB/s", "frac": r_gbs / hbm,
+                      "peak_source": f"{src} copy bandwidth", "bytes_per_call": rb},
+              "tensor": {"bound": "tensor", "kernel": "bsa_route (split + scores + select)",
+                         "achieved": r_tf, "peak": bf16, "unit": "TFLOP/s", "frac": r_tf / bf16,
+                         "peak_source": f"{src} bf16 burst",
+                         "flops_per_call": res["router_flops"],
+                         "note": "1x count: 2 d per (query row, history block)"}}
+    sb = accounting.summaries_bytes(w.num_kv_heads, res["T"], w.head_dim, nblocks)
+    s_gbs = sb / (st["summaries"] * 1e-3) / 1e9
+    summaries = {"bound": "hbm", "kernel": "block_summaries_kernel", "achieved": s_gbs,
+                 "peak": hbm, "unit": "GB/s", "frac": s_gbs / hbm,
+                 "peak_source": f"{src} copy bandwidth", "bytes_per_launch": sb}
+    return attention, router, summaries
+
+
+def prefill_entry(key, args, device, world, rank, local, peaks, src, headline):
+    """Time one prefill workload and run its legs; returns (summary dict, res)."""
+    w = prefill_workload(key)
+    steps = args.steps if headline or key != "tiny" else max(args.steps, 50)
+    sampler = ClockSampler(local)
+    res = bench_prefill(w, steps, args.warmup, device, world, sampler)
+    ms_step = res["total_ms"] / steps
+    max_ms, tot_flops = reduce_max_sum(world, ms_step, res["flops"], device)
+    attention, router, summaries = stage_rooflines(res, w, peaks, src)
+    st = res["stages"]
+    out = {"workload": w.name, "value": tot_flops / (max_ms * 1e-3) / 1e12, "unit": UNIT,
+           "ms_per_step": max_ms, "steps": steps, "total_tokens": res["T"],
+           "l2": res["l2"], "router_ms": st["summaries"] + st["route"], "stages_ms": st,
+           "attention_tflops": attention["achieved"],
+           "effective_pair_tflops": res["eff_flops"] / (st["attention"] * 1e-3) / 1e12,
+           "tiles_per_row": res["tiles"], "roofline": attention, "router": router,
+           "summaries": summaries, "clocks": res["clocks"],
+           "gpu_launches": res["launches"]}
+    if not args.no_quality:
+        q = router_quality(res, w, device)
+        out["speedup_vs_dense"] = q.pop("speedup_vs_dense")
+        out["router_quality"] = q
+    if not args.no_backward and w.head_dim == 128 and key in ("prompt", "long"):
+        out["backward"] = bench_backward(res, w, device)
+    if not args.no_chunked and key == "prompt":
+        out["chunked_prefill"] = bench_chunked(res, w, device)
+    if headline and not args.no_e2e:
+        e_ms, bi, bo, same = bench_e2e(res, w, max(3, min(args.steps, 20)), device)
+        out["e2e"] = {"value": res["flops"] * world / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+                      "ms_per_step": e_ms, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                      "api": "HostPrefill.submit (copies overlapped with compute)",
+                      "output_equals_device_path": same}
+    if headline and rank == 0 and world == 1 and not args.no_cpu:
+        v, n, dt = cpu_oracle_throughput(res["x"], w, budget_s=12.0)
+        out["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": NCORES, "kind": "oracle",
+            "sample": f"{n} random rows of {w.name} in {dt:.1f} s (oracle summaries of the "
+                      f"touched heads, router scores, selection, masked full-row attention); "
+                      f"FLOPs counted as selected physical tiles"}
+    return out, res
+
+
+def free_res(res):
+    for key in ("q", "k", "v", "plan", "x"):
+        res.pop(key, None)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
 def run_native(args):
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -585,8 +747,8 @@ def run_native(args):
     if rank == 0 or world == 1:
         __graft_entry__.build()
     barrier(world, device)
+    peaks, src = measured_peaks()
     if args.decode_only:  # diagnostic: the decode leg alone, one line
-        peaks, src = measured_peaks()
         dec = decode_entry(args, device, peaks, src)
         if rank == 0:
             print(json.dumps({"metric": "decode KV GB/s", "value": dec["value"], "unit": "GB/s",
@@ -594,71 +756,43 @@ def run_native(args):
                               "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
                               "higher_is_better": True, "decode": dec}), flush=True)
         return 0
+    head, res = prefill_entry(args.workload, args, device, world, rank, local, peaks, src, True)
     w = prefill_workload(args.workload)
-    sampler = ClockSampler(local)
-    res = bench_prefill(w, args.steps, args.warmup, device, world, sampler)
-    ms_step = res["total_ms"] / args.steps
-    max_ms, tot_flops = reduce_max_sum(world, ms_step, res["flops"], device)
-    value = tot_flops / (max_ms * 1e-3) / 1e12
-    peaks, src = measured_peaks()
-    st = res["stages"]
-    attn_tf = res["flops"] / (st["attention"] * 1e-3) / 1e12
-    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = recorded_traffic(PROFILE_ATTN[args.workload], ATTN_SOURCE)
-    roofline = {"bound": "tensor", "kernel": f"attn_tc_kernel<{w.head_dim},{w.block}>",
-                "achieved": attn_tf,
-                "peak": peak_tf, "unit": "TFLOP/s", "frac": attn_tf / peak_tf,
-                "peak_source": f"{src} bf16 burst", "traffic": traffic,
-                "algorithmic_flops_per_launch": res["flops"],
-                "compulsory_bytes_per_launch": res["attn_bytes"]}
-    quality = router_quality(res, w, device) if not args.no_quality else None
-    backward = bench_backward(res, w, device) if not args.no_backward else None
-    chunked = bench_chunked(res, w, device) if not args.no_chunked else None
-    e2e = None
-    if not args.no_e2e:
-        e_ms, bi, bo = bench_e2e(res, max(3, min(args.steps, 20)), device)
-        e2e = {"value": res["flops"] * world / (e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "ms_per_step": e_ms, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
-    dec = None
-    if not args.no_decode:
-        del res["q"], res["k"], res["v"]
-        dec = decode_entry(args, device, peaks, src)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        v, n, dt = cpu_oracle_throughput(res["x"], w, budget_s=12.0)
-        cpu = {"value": v, "unit": UNIT, "cores": NCORES, "kind": "oracle",
-               "sample": f"{n} random rows of {w.name} in {dt:.1f} s (oracle summaries of the "
-                         f"touched heads, router scores, selection, masked full-row attention); "
-                         f"FLOPs counted as selected physical tiles"}
+    free_res(res)
+    configs = {w.name: head}
+    others = [] if args.configs == "none" else [c for c in args.configs.split(",") if c]
+    for key in others:
+        if key == args.workload or key not in WORKLOAD_KEYS:
+            continue
+        sub, r = prefill_entry(key, args, device, world, rank, local, peaks, src, False)
+        free_res(r)
+        configs[sub["workload"]] = sub
+    dec = None if args.no_decode else decode_entry(args, device, peaks, src)
     if rank != 0:
         return 0
-    x = res["x"]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "num_seqs": w.num_seqs, "total_tokens": res["T"],
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "total_tokens": head["total_tokens"],
                    "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block": w.block, "k_max": w.k_max,
-                   "route": "topk" if w.mode == 0 else "threshold",
-                   "l2": "inputs larger than L2 (Q+K+V %.0f MB > 129 MB); no flush" %
-                         ((x.q.nbytes + x.k.nbytes + x.v.nbytes) / 1e6),
+                   "route": "topk" if w.mode == 0 else "threshold", "l2": head["l2"],
                    "parallelism": f"replicas x{world}"},
-        "router_ms": st["summaries"] + st["route"],
-        "stages_ms": st,
-        "attention_tflops": attn_tf,
-        "effective_pair_tflops": res["eff_flops"] / (st["attention"] * 1e-3) / 1e12,
-        "router_tflops": res["router_flops"] / (st["route"] * 1e-3) / 1e12,
-        "tiles_per_row": res["tiles"],
-        "roofline": roofline,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
+        "router_ms": head["router_ms"],
+        "stages_ms": head["stages_ms"],
+        "attention_tflops": head["attention_tflops"],
+        "roofline": head["roofline"],
+        "router": head["router"],
+        "summaries": head["summaries"],
+        "speedup_vs_dense": head.get("speedup_vs_dense"),
+        "cpu_baseline": head.get("cpu_baseline"),
+        "e2e": head.get("e2e"),
         "decode": dec,
-        "router_quality": quality,
-        "backward": backward,
-        "chunked_prefill": chunked,
-        "gpu_launches": res["launches"],
-        "clocks": res["clocks"],
+        "configs": configs,
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
     print(json.dumps(line), flush=True)
     return 0

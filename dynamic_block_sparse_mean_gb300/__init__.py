@@ -30,8 +30,9 @@ __all__ = ["ROUTE_TOPK", "ROUTE_THRESHOLD", "RouteParams", "PrefillShape", "Pref
            "DecodePlan", "BsaError", "block_summaries", "route", "build_worklist",
            "attention_fwd", "attention_bwd", "causal_worklist", "coverage", "page_summaries",
            "page_summaries_append", "decode_paged", "check_status", "library_path",
-           "PagedKVCache", "Chunk", "ChunkPlan", "chunk_append", "route_chunk",
-           "build_worklist_chunk", "attention_chunk", "selftest_wait_timeout"]
+           "HostPrefill", "PagedKVCache", "Chunk", "ChunkPlan", "chunk_append", "route_chunk",
+           "build_worklist_chunk", "attention_chunk", "selftest_wait_timeout", "token_recall",
+           "recall_tiles_per_seq"]
 
 
 def library_path() -> str:
@@ -264,6 +265,30 @@ def coverage(lse_sparse, lse_dense, shape: PrefillShape, out=None):
     return out
 
 
+def recall_tiles_per_seq(shape: PrefillShape) -> int:
+    """64-token query tiles per sequence of the recall tile numbering."""
+    s = shape.c()
+    return int(_lib.lib().bsa_recall_tiles_per_seq(ctypes.byref(s)))
+
+
+def token_recall(q, k, J, counts, shape: PrefillShape, t_top: int, tiles=None, hits=None,
+                 dev_status=None):
+    """|G_i ∩ N(i)| per query for the dense top-t teacher (bsa_token_recall): hits
+    [H, T] int32, written for the queries of `tiles` (a device int32 tensor of tile
+    ids (i * H + hq) * recall_tiles_per_seq + c, or None for every tile)."""
+    if hits is None:
+        hits = torch.full((shape.num_heads, shape.total_tokens), -1, dtype=torch.int32,
+                          device=q.device)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    s = shape.c()
+    check("bsa_token_recall", _lib.lib().bsa_token_recall(
+        ctypes.byref(s), int(t_top), _p(q), _p(k), _p(J), _p(counts), int(J.shape[-1]),
+        _p(tiles), 0 if tiles is None else int(tiles.numel()), _p(hits), _p(dev_status),
+        _stream()))
+    return hits
+
+
 class PrefillPlan:
     """All buffers of one prefill shape, allocated once; run() enqueues the four calls
     (summaries, route, worklist, attention) on the current stream."""
@@ -334,6 +359,84 @@ class PrefillPlan:
             self._dense_wl = causal_worklist(self.shape, q.device)
         Od, ld = attention_fwd(q, k, v, self._dense_wl, self.shape, self.status, scale)
         return coverage(self.lse, ld, self.shape), Od, ld
+
+
+class HostPrefill:
+    """Prefill of batches that live in host memory, with the copies overlapped.
+
+    Two device slots (inputs and a PrefillPlan each) alternate between batches:
+    while batch s computes, the upload of batch s + 1 runs on one copy stream and
+    the download of batch s - 1's output on another.  Inside a batch the inputs
+    are uploaded in the order the path needs them (K for the summaries, then Q
+    for the router, then V for the attention), so the first kernels start before
+    the whole batch has arrived.  submit() only enqueues; the output host buffer
+    is complete once synchronize() (or the returned event) has passed.  Host
+    buffers should be pinned for the copies to run asynchronously.
+    """
+
+    def __init__(self, cu_seqlens_host, num_heads: int, num_kv_heads: int, head_dim: int,
+                 block: int, route: RouteParams, dtype=torch.bfloat16, device="cuda"):
+        self.device = torch.device(device)
+        self.plans = [PrefillPlan(cu_seqlens_host, num_heads, num_kv_heads, head_dim, block, route,
+                                  dtype, device) for _ in range(2)]
+        T = self.plans[0].shape.total_tokens
+        self.q = [torch.empty(num_heads, T, head_dim, dtype=dtype, device=device) for _ in range(2)]
+        self.k = [torch.empty(num_kv_heads, T, head_dim, dtype=dtype, device=device)
+                  for _ in range(2)]
+        self.v = [torch.empty(num_kv_heads, T, head_dim, dtype=dtype, device=device)
+                  for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=self.device)
+        self.d2h = torch.cuda.Stream(device=self.device)
+        self.compute = torch.cuda.current_stream(self.device)
+        self._inputs_free = [None, None]   # compute of the slot's last batch done
+        self._output_free = [None, None]   # download of the slot's last output done
+        self._n = 0
+
+    @property
+    def status(self):
+        return self.plans[0].status, self.plans[1].status
+
+    def submit(self, q_host, k_host, v_host, out_host) -> torch.cuda.Event:
+        """Enqueue one batch: upload q / k / v (host [H, T, d] / [H_kv, T, d]), run
+        the path, download O into out_host.  Returns the event of the download."""
+        s = self._n % 2
+        self._n += 1
+        plan = self.plans[s]
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        k_in, q_in, v_in = ev(), ev(), ev()
+        with torch.cuda.stream(self.h2d):
+            if self._inputs_free[s] is not None:
+                self.h2d.wait_event(self._inputs_free[s])
+            self.k[s].copy_(k_host, non_blocking=True)
+            k_in.record(self.h2d)
+            self.q[s].copy_(q_host, non_blocking=True)
+            q_in.record(self.h2d)
+            self.v[s].copy_(v_host, non_blocking=True)
+            v_in.record(self.h2d)
+        with torch.cuda.stream(self.compute):
+            self.compute.wait_event(k_in)
+            plan.summaries(self.k[s])
+            self.compute.wait_event(q_in)
+            plan.select(self.q[s])
+            plan.worklist()
+            self.compute.wait_event(v_in)
+            if self._output_free[s] is not None:
+                self.compute.wait_event(self._output_free[s])
+            plan.attend(self.q[s], self.k[s], self.v[s])
+            done = ev()
+            done.record(self.compute)
+            self._inputs_free[s] = done
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(done)
+            out_host.copy_(plan.out, non_blocking=True)
+            out_done = ev()
+            out_done.record(self.d2h)
+            self._output_free[s] = out_done
+        return out_done
+
+    def synchronize(self):
+        for st in (self.h2d, self.compute, self.d2h):
+            st.synchronize()
 
 
 # ---------------------------------------------------------------- chunked prefill

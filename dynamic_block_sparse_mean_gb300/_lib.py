@@ -77,6 +77,8 @@ PROTOTYPES = {
     "bsa_causal_worklist_capacity": (SZ, [ctypes.POINTER(Shape)]),
     "bsa_build_causal_worklist": (I32, [ctypes.POINTER(Shape), V, V, V, V, V, SZ, V]),
     "bsa_coverage": (I32, [ctypes.POINTER(Shape), V, V, V, V]),
+    "bsa_recall_tiles_per_seq": (I32, [ctypes.POINTER(Shape)]),
+    "bsa_token_recall": (I32, [ctypes.POINTER(Shape), I32, V, V, V, V, I32, V, I32, V, V, V]),
     "bsa_selftest_wait_timeout": (I32, [V, V]),
     "bsa_chunk_append": (I32, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache), V, V, V, V]),
     "bsa_route_chunk_workspace_size": (SZ, [ctypes.POINTER(Shape), ctypes.POINTER(KVCache),

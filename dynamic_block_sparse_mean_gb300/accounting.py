@@ -83,3 +83,11 @@ def decode_bytes(context_lens, sel, sel_counts, num_heads: int, Hk: int, d: int,
     bt = float((L * 4).sum())
     return {"summaries": summ, "kv": kv_bytes, "q_o_lse": qo, "block_table": bt,
             "total": summ + kv_bytes + qo + bt}
+
+
+def router_bytes(H: int, Hk: int, T: int, d: int, num_seqs: int, max_blocks: int,
+                 k_max: int, elem: int = 2) -> float:
+    """Compulsory HBM bytes of the router call (scores + selection): Q read once,
+    the fp32 summaries read once, J and the counts written once."""
+    rows = float(num_seqs) * Hk * max_blocks
+    return (float(elem) * H * T * d + 4.0 * rows * d + 4.0 * rows * k_max + 4.0 * rows)

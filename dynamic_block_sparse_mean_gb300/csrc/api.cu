@@ -253,6 +253,28 @@ bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
   return launched(bsa::launch_coverage(*shape, lse_sparse, lse_dense, C, stream));
 }
 
+int32_t bsa_recall_tiles_per_seq(const bsa_shape_t *shape) {
+  if (!shape_ok(shape)) return 0;
+  return bsa::recall_tiles_per_seq(*shape);
+}
+
+bsa_status_t bsa_token_recall(const bsa_shape_t *shape, int32_t t_top, const void *Q,
+                              const void *K, const int32_t *J, const int32_t *counts,
+                              int32_t k_max, const int32_t *tiles, int32_t num_tiles,
+                              int32_t *hits, int32_t *dev_status, cudaStream_t stream) {
+  if (!shape_ok(shape) || Q == nullptr || K == nullptr || J == nullptr || counts == nullptr ||
+      hits == nullptr || dev_status == nullptr || t_top < 1 || num_tiles < 0 ||
+      (tiles == nullptr && num_tiles != 0))
+    return BSA_ERR_INVALID_ARG;
+  if (!shape_supported(shape) || k_max < 1 || k_max > BSA_MAX_K || shape->max_blocks > 65536 ||
+      (long long)shape->num_seqs * shape->num_heads * bsa::recall_tiles_per_seq(*shape) >
+          INT32_MAX)
+    return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K)) return BSA_ERR_INVALID_ARG;
+  return launched(bsa::launch_token_recall(*shape, t_top, Q, K, J, counts, k_max, tiles,
+                                           num_tiles, hits, dev_status, stream));
+}
+
 bsa_status_t bsa_chunk_append(const bsa_shape_t *shape, const bsa_kv_cache_t *cache,
                               const void *K, const void *V, int32_t *dev_status,
                               cudaStream_t stream) {

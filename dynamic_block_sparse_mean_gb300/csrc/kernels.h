@@ -108,6 +108,13 @@ cudaError_t launch_coverage(const bsa_shape_t &s, const float *lse_sparse, const
 // Device address of the fixed scratch array used by bsa_build_worklist_noalloc.
 cudaError_t worklist_noalloc_scratch(int32_t **out);
 
+// Token recall against the dense top-t teacher (recall.cu).
+int recall_tiles_per_seq(const bsa_shape_t &s);
+cudaError_t launch_token_recall(const bsa_shape_t &s, int32_t t_top, const void *Q,
+                                const void *K, const int32_t *J, const int32_t *counts,
+                                int32_t k_max, const int32_t *tiles, int32_t num_tiles,
+                                int32_t *hits, int32_t *dev_status, cudaStream_t st);
+
 // a5, tensor-core BF16 path (attn_tc.cu) and SIMT FP32 path (attn_simt.cu)
 cudaError_t launch_attention_tc(const bsa_shape_t &s, const void *Q, const void *K,
                                 const void *V, const int32_t *row_ptr, const int32_t *col_idx,

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 6
+#define BSA_VERSION 7
 
 typedef enum {
   BSA_OK = 0,
@@ -368,6 +368,34 @@ bsa_status_t bsa_build_causal_worklist(const bsa_shape_t *shape, int32_t *row_pt
  * ------------------------------------------------------------------------- */
 bsa_status_t bsa_coverage(const bsa_shape_t *shape, const float *lse_sparse,
                           const float *lse_dense, float *C, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Token recall against the dense top-t teacher — [P2] §1.1, the paragraph on
+ *   recall@k: with G_i the dense attention's top-t keys of query i and N(i) its
+ *   candidate keys, token recall = |G_i ∩ N(i)| / |G_i|, to be reported beside
+ *   the physical tile budget.  For query token t (sequence position) of query head
+ *   hq: G_i = the min(t_top, t + 1) visible keys s <= t of the same sequence with
+ *   the largest unscaled score Q[hq].K[hq / G, s], ranked by (score descending,
+ *   index ascending), scores in fp32 from the stored elements; N(i) = the visible
+ *   keys whose block is in the J row (i, hq / G, t / block), an empty row keeping
+ *   its diagonal.  A measurement of the router (fp32 SIMT, several passes over
+ *   each query's keys), not part of the hot path.
+ *   Queries are taken in tiles of 64 consecutive sequence positions of one query
+ *   head: tile id (i * H + hq) * bsa_recall_tiles_per_seq(shape) + c covers
+ *   positions 64 c .. 64 c + 63 of sequence i.
+ *   tiles     : device [num_tiles] tile ids, or NULL for every tile of the batch
+ *               (num_tiles then 0); an id outside the batch sets
+ *               BSA_ERR_INDEX_RANGE; tiles past a sequence's end are skipped.
+ *   J, counts : as bsa_route writes them (k_max = row capacity).
+ *   hits      : [H, T] int32; |G_i ∩ N(i)| written for the queries of the listed
+ *               tiles, other entries untouched.  |G_i| = min(t_top, t + 1).
+ *   Needs max_blocks <= 65536.
+ * ------------------------------------------------------------------------- */
+int32_t bsa_recall_tiles_per_seq(const bsa_shape_t *shape);
+bsa_status_t bsa_token_recall(const bsa_shape_t *shape, int32_t t_top, const void *Q,
+                              const void *K, const int32_t *J, const int32_t *counts,
+                              int32_t k_max, const int32_t *tiles, int32_t num_tiles,
+                              int32_t *hits, int32_t *dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Chunked prefill over a paged KV cache — [P2] §3.1 (block summaries are cache

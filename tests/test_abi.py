@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.bsa_version() == 6
+    hdr = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    assert lib.bsa_version() == int(re.search(r"#define BSA_VERSION (\d+)", hdr).group(1))
     for code in _lib.STATUS_NAMES:
         assert lib.bsa_status_string(code)
 
@@ -103,6 +104,14 @@ def test_host_side_argument_errors(lib):
                                 ctypes.c_void_p(16), null, ctypes.c_void_p(16), ctypes.c_void_p(16),
                                 null, null, 0, null) == 2
     assert lib.bsa_decode_workspace_size(ctypes.byref(ds)) > 0
+    # token recall: t_top >= 1, a tile count only with a tile list, k_max in range
+    p16 = ctypes.c_void_p(16)
+    rec = lambda t, km, tiles, nt: lib.bsa_token_recall(  # noqa: E731
+        ctypes.byref(s), t, p16, p16, p16, p16, km, tiles, nt, p16, p16, null)
+    assert rec(0, 4, null, 0) == 1
+    assert rec(64, 4, null, 3) == 1
+    assert rec(64, 300, null, 0) == 2
+    assert lib.bsa_recall_tiles_per_seq(ctypes.byref(s)) == 16
 
 
 def test_chunk_calls_reject_bad_cache_descriptors(lib):
