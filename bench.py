@@ -58,6 +58,9 @@ def parse_args(argv=None):
                     help="the headline workload (default: the 128k prompt, the largest)")
     ap.add_argument("--configs", default="tiny,prompt,varlen",
                     help="other prefill workloads timed into the same line ('none': skip)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="cut a fixed-length prefill workload to its first N tokens (small "
+                         "cases for profiler captures; the name gets a _firstN suffix)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -187,10 +190,15 @@ def recorded_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------- workloads
 
 
-def prefill_workload(name: str):
+def prefill_workload(name: str, tokens: int | None = None):
+    import dataclasses
+
     from dynamic_block_sparse_mean_gb300 import workloads as W
     table = {"tiny": W.TINY, "prompt": W.PROMPT_32K, "varlen": W.VARLEN_256K, "long": W.LONG_128K}
-    return table[name]
+    w = table[name]
+    if tokens is not None and w.seqlen is not None and tokens < w.seqlen:
+        w = dataclasses.replace(w, seqlen=tokens, name=f"{w.name}_first{tokens}")
+    return w
 
 
 def to_dev_bf16(a: np.ndarray, device):
@@ -609,7 +617,7 @@ def run_reference(args):
     if world > 1 and rank != 0:
         return 0
     from dynamic_block_sparse_mean_gb300 import synth
-    w = prefill_workload(args.workload)
+    w = prefill_workload(args.workload, args.tokens)
     x = synth.make_prefill(w)
     per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
     for s in range(args.warmup):
@@ -689,7 +697,7 @@ def stage_rooflines(res, w, peaks, src):
 
 def prefill_entry(key, args, device, world, rank, local, peaks, src, headline):
     """Time one prefill workload and run its legs; returns (summary dict, res)."""
-    w = prefill_workload(key)
+    w = prefill_workload(key, args.tokens)
     steps = args.steps if headline or key != "tiny" else max(args.steps, 50)
     sampler = ClockSampler(local)
     res = bench_prefill(w, steps, args.warmup, device, world, sampler)
@@ -757,7 +765,7 @@ def run_native(args):
                               "higher_is_better": True, "decode": dec}), flush=True)
         return 0
     head, res = prefill_entry(args.workload, args, device, world, rank, local, peaks, src, True)
-    w = prefill_workload(args.workload)
+    w = prefill_workload(args.workload, args.tokens)
     free_res(res)
     configs = {w.name: head}
     others = [] if args.configs == "none" else [c for c in args.configs.split(",") if c]

@@ -68,6 +68,7 @@ class RouteParams:
     force_sink: bool = False
     window: int = 1
     global_blocks: tuple = ()
+    screen: int = 0   # bf16 score screening: 0 automatic, 1 always, -1 never
     _gdev: object = field(default=None, repr=False, compare=False)
 
     def _globals_on(self, device):
@@ -83,7 +84,7 @@ class RouteParams:
         return _lib.RouteParams(self.mode, self.k_max, self.k_min, self.tau_delta,
                                 1 if self.force_sink else 0, self.window,
                                 0 if g is None else g.numel(),
-                                None if g is None else g.data_ptr())
+                                None if g is None else g.data_ptr(), int(self.screen))
 
 
 @dataclass

@@ -38,7 +38,7 @@ class RouteParams(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("k_max", ctypes.c_int32), ("k_min", ctypes.c_int32),
                 ("tau_delta", ctypes.c_float), ("force_sink", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("num_global", ctypes.c_int32),
-                ("global_blocks", ctypes.c_void_p)]
+                ("global_blocks", ctypes.c_void_p), ("screen", ctypes.c_int32)]
 
 
 class DecodeShape(ctypes.Structure):

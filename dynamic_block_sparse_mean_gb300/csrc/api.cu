@@ -79,7 +79,7 @@ bsa_status_t chunk_status(const bsa_shape_t *s, const bsa_kv_cache_t *c) {
     return BSA_ERR_INVALID_ARG;
   if ((long long)c->num_phys_pages * s->num_kv_heads * 64 > INT32_MAX ||
       (long long)s->num_seqs * s->num_kv_heads * c->max_context_blocks > (1LL << 30) ||
-      (long long)c->max_context_blocks * 5 + 1040 > 227 * 1024)
+      !bsa::route_select_fits(c->max_context_blocks, s->head_dim))
     return BSA_ERR_UNSUPPORTED;
   if (!aligned16(c->k_cache) || !aligned16(c->v_cache) || !aligned16(c->page_summ) ||
       (c->page_sum != nullptr && !aligned16(c->page_sum)))
@@ -148,7 +148,8 @@ bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *param
   if (!shape_ok(shape) || params == nullptr || Q == nullptr || C == nullptr || J == nullptr ||
       counts == nullptr)
     return BSA_ERR_INVALID_ARG;
-  if (!shape_supported(shape)) return BSA_ERR_UNSUPPORTED;
+  if (!shape_supported(shape) || !bsa::route_select_fits(shape->max_blocks, shape->head_dim))
+    return BSA_ERR_UNSUPPORTED;
   const bsa_status_t ps = route_params_status(*params);
   if (ps != BSA_OK) return ps;
   if (!aligned16(Q) || !aligned16(C)) return BSA_ERR_INVALID_ARG;

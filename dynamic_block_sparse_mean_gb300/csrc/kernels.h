@@ -38,13 +38,23 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 bool make_tmap_3d_bf16(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t b0, uint32_t b1, uint32_t b2);
 
-// a2 on the tensor cores (route_tc.cu): exact fp32 scores from bf16 Q and the
-// three-way bf16 split of the fp32 summaries; writes S[row][j] for j < r.
+// a2 on the tensor cores (route_tc.cu): fp32 scores from bf16 Q and the three-way
+// bf16 split of the fp32 summaries; writes S[row][j] for j < r.  screen: two of the
+// three parts (q . (c_hi + c_mid)), and the norms that bound the rest.
 // cache != nullptr: a chunked prefill, summaries gathered from the paged cache.
 size_t route_tc_workspace_bytes(const bsa_shape_t &s, const bsa_kv_cache_t *cache);
 cudaError_t launch_route_scores_tc(const bsa_shape_t &s, const void *Q, const float *C,
-                                   const bsa_kv_cache_t *cache, float *S, void *ws,
-                                   int32_t *dev_status, cudaStream_t st);
+                                   const bsa_kv_cache_t *cache, float *S, bool screen, void *ws,
+                                   int32_t *qlen, int32_t *dev_status, cudaStream_t st);
+// Where the screen's inputs live in the route workspace: the split planes
+// [3, c3_rows, d] bf16, |c| and |c - c_hi - c_mid| per summary row, and the largest
+// query norm of each router row.
+struct RouteScreen {
+  const uint16_t *C3;
+  const float *cn, *rn, *Qn;
+  size_t c3_rows;
+};
+RouteScreen route_tc_screen(const bsa_shape_t &s, const bsa_kv_cache_t *cache, void *ws);
 
 // a1 and the decode page summaries (summaries.cu)
 cudaError_t launch_block_summaries(const bsa_shape_t &s, const void *K, float *C,
@@ -63,6 +73,8 @@ cudaError_t launch_chunk_append(const bsa_shape_t &s, const bsa_kv_cache_t &cach
 // cache != nullptr: a chunked prefill (C unused, summaries from the cache).
 size_t route_workspace_bytes(const bsa_shape_t &s, const bsa_route_params_t &p,
                              const bsa_kv_cache_t *cache = nullptr);
+// Whether a score row of Nk entries fits the selection kernel's shared memory.
+bool route_select_fits(int Nk, int d);
 cudaError_t launch_route(const bsa_shape_t &s, const bsa_route_params_t &p, const void *Q,
                          const float *C, const bsa_kv_cache_t *cache, int32_t *J,
                          int32_t *counts, float *scores, int32_t *dev_status, void *ws,

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define BSA_VERSION 7
+#define BSA_VERSION 8
 
 typedef enum {
   BSA_OK = 0,
@@ -106,6 +106,15 @@ typedef struct {
   const int32_t *global_blocks; /* device [num_global] sequence-relative block ids
                                    (>= 0; ids past a row are ignored by that row);
                                    NULL when num_global == 0; read during the call */
+  int32_t screen;     /* BF16 scores without a score matrix (no effect on the result,
+                         only on the work): the tensor cores compute q . (c_hi + c_mid)
+                         of the three-part bf16 split of each fp32 summary, every score
+                         carries a rigorous error bound, and only the candidates whose
+                         bound meets the selection boundary are rescored exactly.
+                         0 = automatic: on when a row pools G * block >= 512 query
+                         rows, where the saved third of the score products outweighs
+                         the per-row bound work; 1 = always; -1 = never (three parts).
+                         A call that passes `scores` always computes them exactly. */
 } bsa_route_params_t;
 
 /* Paged decode shape ([P2] §2.2 decode; §3.1 paged KV cache and block table). */

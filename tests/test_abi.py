@@ -45,6 +45,16 @@ def test_version_and_status_strings(lib):
         assert lib.bsa_status_string(code)
 
 
+def _route_split_bytes(rows, d, qrows):
+    """The BF16 router's workspace besides the score matrix: the three-way bf16 split
+    of the summaries, their two norms, one query-norm bound per router row, and the
+    rescoring queue (its length, the queued rows, per row a count and 64 candidate
+    ids), each rounded up to 256 bytes."""
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    return (up(rows * d * 3 * 2) + 2 * up(rows * 4) + up(qrows * 4) +
+            up(4) + 2 * up(qrows * 4) + up(qrows * 64 * 4))
+
+
 def _shape(**kw):
     base = dict(num_seqs=1, total_tokens=1024, max_seqlen=1024, num_heads=2, num_kv_heads=2,
                 head_dim=64, block=64, max_blocks=16, dtype=0, cu_seqlens=0x1000)
@@ -84,8 +94,8 @@ def test_host_side_argument_errors(lib):
                              null) == 1
     ok_p = _lib.RouteParams(0, 4, 0, 0.0, 1, 2, 1, gl)                # 2 + 1 + sink = 4
     assert lib.bsa_route(ctypes.byref(s), ctypes.byref(ok_p), *args, null, null, null, 0, null) == 3
-    split = (1 * 2 * 16 * 64 * 3 * 2 + 255) // 256 * 256      # bf16 three-way split of C
-    assert lib.bsa_route_workspace_size(ctypes.byref(s), ctypes.byref(p)) == split + 1 * 2 * 16 * 16 * 4
+    assert lib.bsa_route_workspace_size(ctypes.byref(s), ctypes.byref(p)) == \
+        _route_split_bytes(32, 64, 32) + 1 * 2 * 16 * 16 * 4
     wl = [ctypes.c_void_p(16)] * 7
     assert lib.bsa_build_worklist(ctypes.byref(s), 4, *wl, null, 0, null) == 3
     assert lib.bsa_build_worklist(ctypes.byref(s), 0, *wl, null, 0, null) == 2
@@ -140,8 +150,7 @@ def test_chunk_calls_reject_bad_cache_descriptors(lib):
     p = _lib.RouteParams(0, 4, 0, 0.0, 0, 1, 0, None)
     c = cache()
     need = lib.bsa_route_chunk_workspace_size(ctypes.byref(s), ctypes.byref(c), ctypes.byref(p))
-    split = (1 * 2 * 16 * 64 * 3 * 2 + 255) // 256 * 256
-    assert need == split + 1 * 2 * 16 * 16 * 4
+    assert need == _route_split_bytes(32, 64, 32) + 1 * 2 * 16 * 16 * 4
     args = [p16] * 4
     assert lib.bsa_route_chunk(ctypes.byref(s), ctypes.byref(c), ctypes.byref(p), *args, p16,
                                null, 0, null) == 3

@@ -31,6 +31,11 @@ CASES = [
     ("gqa2_d64_threshold_union", [[0, 256, 1280, 2000], [0, 0, 640, 901]], 4, 2, 64,
      dict(mode=oracle.THRESHOLD, k_max=10, k_min=2, tau_delta=2.0, window=2,
           global_blocks=(1, 4))),
+    # the same chunking with the router's score screen forced on (bounded screened
+    # scores, exact rescoring of the candidates at the boundary)
+    ("gqa4_d128_topk_sink_screened", [[0, 512, 1024, 1500], [0, 128, 128, 700], [0, 64, 64, 64],
+                                      [0, 100, 100, 100]], 8, 2, 128,
+     dict(mode=oracle.TOPK, k_max=6, force_sink=True, screen=1)),
 ]
 IDS = [c[0] for c in CASES]
 
@@ -197,11 +202,11 @@ def test_chunk_attention_on_oracle_chunk_index():
     assert mx <= BF16_MAX_ABS and mean <= BF16_MEAN_ABS and lmx <= BF16_LSE_ABS, (mx, mean, lmx)
 
 
-def test_chunked_equals_single_pass_bit_for_bit():
+@pytest.mark.parametrize("case", [CASES[0], CASES[2]], ids=[CASES[0][0], CASES[2][0]])
+def test_chunked_equals_single_pass_bit_for_bit(case):
     """The summaries of appended pages, the router's scores and the attention
     tiles are the single-pass ones in the same order, so the chunked J and O equal
     the single-pass PrefillPlan's exactly."""
-    case = CASES[0]
     x, cache, params, steps = _run_chunks(case)
     H, Hk, d = case[2], case[3], case[4]
     q, k, v = upload(x)

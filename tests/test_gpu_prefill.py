@@ -67,6 +67,57 @@ def test_router_matches_oracle_tie_aware(case):
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_router_screen_matches_oracle_tie_aware(case):
+    # Without a score matrix the BF16 router screens with q . (c_hi + c_mid) and
+    # rescores only the candidates its error bound cannot place.
+    x, q, k, v, sh, params = _run_case(case, seed=8)
+    params.screen = 1
+    H, Hk = case[2], case[3]
+    C = bsa.block_summaries(k, sh)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    J, cnt = bsa.route(q, C, sh, params, dev_status=st)
+    torch.cuda.synchronize()
+    bsa.check_status(st)
+    Jo, co, go, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), x.cu_seqlens, x.block,
+                                 H // Hk, params.mode, params.k_max, params.k_min, params.tau_delta,
+                                 params.force_sink)
+    rows = oracle.all_rows(x.cu_seqlens, x.block, Hk)
+    check_route_rows(J.cpu().numpy(), cnt.cpu().numpy(), Jo, co, go, rows, params.mode,
+                     params.force_sink, params.tau_delta)
+
+
+@pytest.mark.parametrize("mode", [oracle.TOPK, oracle.THRESHOLD])
+def test_router_screen_with_every_candidate_tied(mode):
+    # Keys repeat with period b, so every complete block holds the same keys: all
+    # summaries and all candidate scores tie exactly, no bound can place any
+    # candidate, and every one is rescored (several rounds per row); ties go to the
+    # lower block index on both sides, so J must equal the oracle's exactly.
+    lengths, H, Hk, d, b = [1500, 700], 4, 2, 128, 64
+    x = synth.gen_prefill(lengths, H, Hk, d, b, 11, "iid", "bf16")
+    cu = x.cu_seqlens
+    for i, n in enumerate(lengths):
+        s0 = int(cu[i])
+        for t in range(b, n):
+            x.k[:, s0 + t] = x.k[:, s0 + t % b]
+    q, k, v = upload(x)
+    sh = shape_of(x, H, Hk)
+    params = (bsa.RouteParams(oracle.TOPK, 6, 0, 0.0, True, screen=1) if mode == oracle.TOPK else
+              bsa.RouteParams(oracle.THRESHOLD, 8, 2, 2.0, False, screen=1))
+    C = bsa.block_summaries(k, sh)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    J, cnt = bsa.route(q, C, sh, params, dev_status=st)
+    torch.cuda.synchronize()
+    bsa.check_status(st)
+    Jo, co, go, _ = oracle.route(oracle_view(x, "q"), oracle_view(x, "k"), cu, b, H // Hk,
+                                 params.mode, params.k_max, params.k_min, params.tau_delta,
+                                 params.force_sink)
+    assert np.array_equal(cnt.cpu().numpy(), co)
+    Jg = J.cpu().numpy()
+    for (i, h, r) in oracle.all_rows(cu, b, Hk):
+        assert list(Jg[i, h, r, :co[i, h, r]]) == list(Jo[i, h, r, :co[i, h, r]]), (i, h, r)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_worklist_csr_and_buckets(case):
     x, q, k, v, sh, params = _run_case(case)
     H, Hk = case[2], case[3]
