@@ -12,21 +12,29 @@
 // twice and its copy masked).  Every MMA therefore has N = 128, the shape at
 // which tcgen05 runs at its full rate (N = 64 runs at two thirds).
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax / epilogue for M-tile 0 (thread = one query row = one TMEM lane)
 //   warps 4-7  softmax / epilogue for M-tile 1
 //   warp 8     TMA producer: Q tiles, then the K and V rows of each key step
-//   warp 9     MMA issuer (one thread)
+//   warps 9-10 MMA issuers, one thread each: warp 9 + t issues M-tile t's products
 // TMEM (512 columns): O_0, O_1 (d columns each), S_0, S_1 (128 columns each).  The
 // softmax overwrites the first 64 columns of S_t with P (bf16 pairs) and the PV
 // product reads P straight from tensor memory.
 //
-// Issue order of the MMA thread for step s, per M-tile t:
+// Issue order of M-tile t's MMA thread for step s (one batch):
 //     PV_t(s)   [after P_t(s)]      O_t += P_t(s) V(s)
 //     QK_t(s+1) [after K(s+1)]      S_t  = Q_t K(s+1)^T
 // tcgen05.mma operations of one thread execute in issue order, so QK_t(s+1)
-// overwrites S_t only after PV_t(s) has read P_t(s).  While the softmax of one
-// M-tile runs, the tensor cores work on the other M-tile.
+// overwrites S_t only after PV_t(s) has read P_t(s).  Each M-tile has its own
+// issuing thread, and the two alternate batch by batch (a ping-pong of two
+// barriers), so the tensor pipe sees PV_0 QK_0 | PV_1 QK_1 | PV_0 ... and the two
+// tiles' softmaxes stay half a step apart.  A barrier check stalls its own
+// thread's MMA issue for about a hundred cycles, even on a completed phase
+// (measured on GB300: four checks per 32 MMAs of one thread slow the pipe from 64
+// to 80 cycles per MMA; two threads with the same checks keep it at 64), so each
+// issuer's checks now overlap the other tile's batch.  A K / V stage and the Q
+// tiles are released by one commit of each issuer; an issuer without a tile in a
+// unit walks its steps all the same.
 //
 // The running max used for the exponentials is refreshed only when the row max
 // grows by more than 8 (log2 units); O and l are then rescaled in TMEM.  u / l is
@@ -39,9 +47,9 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // M-tile 0's issuer; M-tile 1's is kMmaWarp + 1; owns TMEM
 constexpr int kTmemCols = 512;
 constexpr int kStep = 128;  // keys per step
 constexpr int kPrefetch = 2;  // steps of K / V prefetched into L2 ahead of their stage load
@@ -70,8 +78,9 @@ struct Cfg {
   static constexpr int B_OFINAL = B_OFREE + 2;    // all PV of a unit done (once per unit)
   static constexpr int B_OSTAGED = B_OFINAL + 2;  // a staged output half is complete (4 warps)
   static constexpr int B_OSFREE = B_OSTAGED + 2;  // the staging buffer was read by its store
-  static constexpr int B_FINAL = B_OSFREE + 2;
-  static constexpr int kNumBars = B_FINAL + 1;
+  static constexpr int B_FINAL = B_OSFREE + 2;    // one per issuer
+  static constexpr int B_TURN = B_FINAL + 2;      // issuer t's batch is issued (one per issuer)
+  static constexpr int kNumBars = B_TURN + 2;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffCtl + 16;
   // 1 KB for base alignment; at least 120 KB so that exactly one CTA (which owns
@@ -321,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
-    mbar_init(bar(C::B_QEMPTY), 1);
+    mbar_init(bar(C::B_QEMPTY), 2);  // released by both issuers
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 2);
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
@@ -339,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_OSFREE + t), 1);
     }
     mbar_init(bar(C::B_FINAL), 1);
+    mbar_init(bar(C::B_FINAL + 1), 1);
+    mbar_init(bar(C::B_TURN), 1);
+    mbar_init(bar(C::B_TURN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -441,19 +453,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ MMA issuers
+    const int t = warp - kMmaWarp;  // the M-tile this thread issues for
     if (lane == 0) {
       int stp = 0, ucount = 0;
-      int k[2] = {0, 0};     // steps per M-tile (S / P / O-done phases)
-      int ut[2] = {0, 0};    // units per M-tile (O-free / O-final phases)
+      int ks = 0;   // steps of this tile (S / P phases)
+      int ut = 0;   // units of this tile (O-free / O-final phases)
       bool ok = true;
       // Descriptors differ only in their low word; K-step offsets within a panel
       // are compile-time constants, so each MMA costs one add.
       const uint32_t qlo0 = desc_lo(smQ, 16), klo0 = desc_lo(smK, 16);
       const uint32_t vlo0 = desc_lo(smV, C::kPanel);
       const uint32_t dhi = kDescHi;
-      auto issue_qk = [&](int t, int st) {
+      auto issue_qk = [&](int st) {
         const uint32_t alo = qlo0 + (uint32_t)(t * C::kQTile) / 16u;
         const uint32_t blo = klo0 + (uint32_t)(st * C::kStage) / 16u;
         const uint32_t d = tmem + C::colS(t);
@@ -465,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int st, bool acc) {
+      auto issue_pv = [&](int st, bool acc) {
         const uint32_t blo = vlo0 + (uint32_t)(st * C::kStage) / 16u;
         const uint32_t a = tmem + C::colS(t), d = tmem + C::colO(t);
 #pragma unroll
@@ -473,25 +486,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_lo(d, a + kk * 8, blo + kk * (2048u / 16u), dhi, C::kIdescPV,
                     (acc || kk > 0) ? 1u : 0u);
       };
+      // Batches alternate between the issuers: issuer 0's batch b follows issuer 1's
+      // batch b - 1, issuer 1's batch b follows issuer 0's batch b.
+      int nb = 0;
+      auto my_turn = [&]() {
+        if (t == 0 && nb == 0) return true;
+        const int other = 1 - t, k = t == 0 ? nb - 1 : nb;
+        return mbar_wait(bar(C::B_TURN + other), k & 1, abort_flag, p.status);
+      };
+      auto turn_done = [&]() {
+        mbar_arrive(bar(C::B_TURN + t));
+        ++nb;
+      };
       Unit nx;
       if (blockIdx.x < total_units) nx = decode_unit<CHUNK>(p, blockIdx.x);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
         const Unit x = nx;
         if (u + (int)gridDim.x < total_units) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
         const int nsteps = (x.nkv + BPS - 1) / BPS;
+        const bool active = t < x.nt;
+        // Every barrier a batch needs is checked before the issuer takes its turn,
+        // while the other tile's batch runs; the turn check is then the only wait
+        // between the two threads' batches.
         if (!(ok = mbar_wait(bar(C::B_QFULL), ucount & 1, abort_flag, p.status))) break;
-        tc_fence_after();
         {  // QK of step 0
           const int st = stp % C::NS;
           if (!(ok = mbar_wait(bar(C::B_KFULL + st), (stp / C::NS) & 1, abort_flag, p.status)))
             break;
+          if (!(ok = my_turn())) break;
           tc_fence_after();
-          for (int t = 0; t < x.nt; ++t) {
-            issue_qk(t, st);
+          if (active) {
+            issue_qk(st);
             mma_commit(bar(C::B_SFULL + t));
           }
           mma_commit(bar(C::B_KEMPTY + st));
           if (nsteps == 1) mma_commit(bar(C::B_QEMPTY));
+          turn_done();
         }
         for (int s = 0; ok && s < nsteps; ++s) {
           const int g = stp + s, st = g % C::NS;
@@ -499,44 +529,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = s + 1 < nsteps;
           if (!(ok = mbar_wait(bar(C::B_VFULL + st), (g / C::NS) & 1, abort_flag, p.status)))
             break;
-          tc_fence_after();
-          for (int t = 0; t < x.nt; ++t) {
-            if (!(ok = mbar_wait(bar(C::B_PFULL + t), (k[t] + s) & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-            if (s == 0) {
-              if (!(ok = mbar_wait(bar(C::B_OFREE + t), (ut[t] & 1) ^ 1, abort_flag, p.status)))
-                break;
-              tc_fence_after();
-            }
-            issue_pv(t, st, s > 0);
-            if (!more) mma_commit(bar(C::B_OFINAL + t));
-            if (more) {
-              if (t == 0) {
-                if (!(ok = mbar_wait(bar(C::B_KFULL + st1), (g1 / C::NS) & 1, abort_flag,
-                                     p.status)))
-                  break;
-                tc_fence_after();
-              }
-              issue_qk(t, st1);
-              mma_commit(bar(C::B_SFULL + t));
-            }
+          if (active) {
+            if (!(ok = mbar_wait(bar(C::B_PFULL + t), (ks + s) & 1, abort_flag, p.status))) break;
+            if (s == 0 &&
+                !(ok = mbar_wait(bar(C::B_OFREE + t), (ut & 1) ^ 1, abort_flag, p.status)))
+              break;
           }
-          if (!ok) break;
+          if (more &&
+              !(ok = mbar_wait(bar(C::B_KFULL + st1), (g1 / C::NS) & 1, abort_flag, p.status)))
+            break;
+          if (!(ok = my_turn())) break;
+          tc_fence_after();
+          if (active) {
+            issue_pv(st, s > 0);
+            if (!more) mma_commit(bar(C::B_OFINAL + t));
+          }
           mma_commit(bar(C::B_VEMPTY + st));
           if (more) {
+            if (active) {
+              issue_qk(st1);
+              mma_commit(bar(C::B_SFULL + t));
+            }
             mma_commit(bar(C::B_KEMPTY + st1));
             if (s + 2 == nsteps) mma_commit(bar(C::B_QEMPTY));
           }
+          turn_done();
         }
-        for (int t = 0; t < x.nt; ++t) {
-          k[t] += nsteps;
-          ++ut[t];
+        if (active) {
+          ks += nsteps;
+          ++ut;
         }
         stp += nsteps;
       }
-      // Every MMA issued so far completes before TMEM is released.
-      mma_commit(bar(C::B_FINAL));
-      mbar_wait_drain(bar(C::B_FINAL), 0);
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit(bar(C::B_FINAL + t));
+      mbar_wait_drain(bar(C::B_FINAL + t), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
