@@ -79,60 +79,97 @@ BSA_DEV QRow qrow(const BwdTcParams &p, int t, int rho, int h, int r, int s0, in
   return q;
 }
 
-// P and dS of 32 keys of one query row (keys key0 .. key0 + 31 of the block),
-// packed as bf16 pairs; keys past the query on the diagonal, and invalid rows, are 0.
-BSA_DEV void softmax_grad32(const uint32_t (&s)[32], const uint32_t (&dp)[32], bool valid,
-                            bool diag, int key0, int tok, float scale_log2, float lse2, float Drow,
-                            uint32_t (&pk)[16], uint32_t (&dk)[16]) {
-#pragma unroll
-  for (int c = 0; c < 32; c += 2) {
-    float pr[2], ds[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const bool ok = valid && (!diag || key0 + c + e <= tok);
-      pr[e] = ok ? fast_exp2(__uint_as_float(s[c + e]) * scale_log2 - lse2) : 0.f;
-      ds[e] = pr[e] * (__uint_as_float(dp[c + e]) - Drow);
-    }
-    pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
-    dk[c / 2] = pack_bf16x2(ds[0], ds[1]);
-  }
+// 16 TMEM columns of this thread's lane, not waited (see tmem_ld32_async).
+BSA_DEV void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
-// Four 16-byte chunks (half h of a 128-byte row) into the swizzled tile.
-BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[16]);
-BSA_DEV void softmax_grad32(const uint32_t (&s)[32], const uint32_t (&dp)[32], bool valid,
-                            bool diag, int key0, int tok, float scale_log2, float lse2, float Drow,
-                            uint32_t (&pk)[16], uint32_t (&dk)[16]);
+// Wait for this thread's TMEM loads into the two 16-register buffers.
+BSA_DEV void tmem_wait_ld16x2(uint32_t (&r)[16], uint32_t (&q)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(q[0]), "+r"(q[1]),
+                 "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7]),
+                 "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]), "+r"(q[13]),
+                 "+r"(q[14]), "+r"(q[15])
+               :
+               : "memory");
+}
+
+// Packed pairs of fp32 (low word = first element) and the sm_100+ pair arithmetic.
+BSA_DEV uint64_t f2_pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+BSA_DEV uint64_t f2_pack(uint32_t lo, uint32_t hi) { return (uint64_t)lo | ((uint64_t)hi << 32); }
+BSA_DEV float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+BSA_DEV float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+BSA_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+BSA_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+BSA_DEV uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // P and dS of the 64 keys of one TMEM S / dP tile row into shared memory (P only
-// when smP != 0).  The second half's loads are in flight while the first half
-// is computed.
+// when smP != 0), 16 columns at a time: the next 16 columns' loads are in flight
+// while the current ones are computed, and only 64 registers hold loaded values
+// (holding all 128 at once left the compiler no room to overlap the exp / multiply
+// chains of different columns, which made this routine four times slower).
+// Keys past the query on the diagonal (key0 + column > tok), and invalid rows,
+// get P = dS = 0.
 BSA_DEV void tile_grad64(uint32_t tS, uint32_t tDP, uint32_t smP, uint32_t smDS, int rho,
                          bool valid, bool diag, int key0, int tok, float scale_log2, float lse2,
                          float Drow) {
-  uint32_t s0[32], d0[32], s1[32], d1[32], pk[16], dk[16];
-  tmem_ld32_async(tS, s0);
-  tmem_ld32_async(tDP, d0);
-  tmem_wait_ld(s0);
-  tmem_wait_ld(d0);
-  tmem_ld32_async(tS + 32, s1);
-  tmem_ld32_async(tDP + 32, d1);
-  softmax_grad32(s0, d0, valid, diag, key0, tok, scale_log2, lse2, Drow, pk, dk);
-  if (smP != 0u) st_row_half(smP, rho, 0, pk);
-  st_row_half(smDS, rho, 0, dk);
-  tmem_wait_ld(s1);
-  tmem_wait_ld(d1);
-  softmax_grad32(s1, d1, valid, diag, key0 + 32, tok, scale_log2, lse2, Drow, pk, dk);
-  if (smP != 0u) st_row_half(smP, rho, 1, pk);
-  st_row_half(smDS, rho, 1, dk);
-}
-
-BSA_DEV void st_row_half(uint32_t base, int rho, int half, const uint32_t (&v)[16]) {
+  uint32_t sb[2][16], db[2][16];
+  const int lim = !valid ? 0 : (diag ? min(64, max(0, tok - key0 + 1)) : 64);  // first masked column
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
+  const uint64_t nd2 = f2_pack(-Drow, -Drow);
+  tmem_ld16_async(tS, sb[0]);
+  tmem_ld16_async(tDP, db[0]);
+  tmem_wait_ld16x2(sb[0], db[0]);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int c = half * 4 + q;
-    st_shared_v4(base + rho * 128 + ((c ^ (rho & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                 v[4 * q + 3]);
+  for (int c = 0; c < 4; ++c) {
+    if (c < 3) {
+      tmem_ld16_async(tS + 16 * (c + 1), sb[(c + 1) & 1]);
+      tmem_ld16_async(tDP + 16 * (c + 1), db[(c + 1) & 1]);
+    }
+    const uint32_t(&sv)[16] = sb[c & 1];
+    const uint32_t(&dv)[16] = db[c & 1];
+    uint32_t pk[8], dk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int col = 16 * c + 2 * e;
+      const uint64_t z = f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sc2, nl2);
+      const float p0 = col < lim ? fast_exp2(f2_lo(z)) : 0.f;
+      const float p1 = col + 1 < lim ? fast_exp2(f2_hi(z)) : 0.f;
+      const uint64_t ds = f2_mul(f2_pack(p0, p1), f2_add(f2_pack(dv[2 * e], dv[2 * e + 1]), nd2));
+      pk[e] = pack_bf16x2(p0, p1);
+      dk[e] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // 16-byte chunk 2c + h of the 128-byte row
+      const uint32_t off = rho * 128 + (((2 * c + h) ^ (rho & 7)) << 4);
+      if (smP != 0u) st_shared_v4(smP + off, pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+      st_shared_v4(smDS + off, dk[4 * h], dk[4 * h + 1], dk[4 * h + 2], dk[4 * h + 3]);
+    }
+    if (c < 3) tmem_wait_ld16x2(sb[(c + 1) & 1], db[(c + 1) & 1]);
   }
 }
 
@@ -209,24 +246,32 @@ __global__ void kt_emit_kernel(const uint32_t *__restrict__ bits,
 // ---------------------------------------------------------------- dQ pass
 
 // One CTA per (work row, M-tile), one per SM: Q and dO of the tile stay in shared
-// memory; the 64-key tiles of the row's blocks stream through a three-stage K / V
-// ring.  S and dP of step s land in one of two TMEM buffers while the softmax
-// warps turn step s-1 into dS (two shared-memory buffers), which then feeds
-// dQ += dS K (fp32 in TMEM).  320 threads: two softmax warpgroups (warps 0-3 take
-// the even steps, 4-7 the odd ones; one query row per thread), warp 8 TMA, warp 9
-// MMA.
+// memory; the 64-key tiles of the row's blocks stream through a five-stage K ring
+// and a three-stage V ring (V of step s is free once dP(s) is done, K only after
+// dQ(s), two batches later; both rings keep two batches of loads ahead of the
+// MMAs, which hides the L2 / DRAM latency of a 16 KB tile).  Steps alternate between two halves of the CTA: warpgroup e (warps 4e ..
+// 4e + 3, one query row per thread) and MMA thread e (warp 9 + e) take the steps
+// s = e (mod 2), with S / dP buffer e in TMEM, dS buffer e in shared memory and
+// their own dQ accumulator dQ_e += dS K (fp32 in TMEM); the epilogue adds dQ_0 +
+// dQ_1 in that order, so the result is the same on every call.  The two MMA
+// threads alternate batches (S / dP of step s and dQ of step s - 2) through a
+// two-barrier ping-pong and check every barrier a batch needs before their turn:
+// a barrier check stalls its own thread's MMA issue (about a hundred cycles), so
+// each thread's checks run while the other's batch executes.  352 threads.
 namespace dq {
-constexpr int kThreads = 320;
-constexpr int NS = 3;
-constexpr int kOffQ = 0, kOffDO = 32768, kOffKV = 65536;  // stage: K (16 KB) then V (16 KB)
-constexpr int kOffDS = kOffKV + NS * 32768;
+constexpr int kThreads = 352;
+constexpr int NK = 5, NV = 3;  // K and V ring stages (16 KB each)
+constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NK * 16384;
+constexpr int kOffDS = kOffV + NV * 16384;
 constexpr int kOffBar = kOffDS + 2 * 16384;
-constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = B_KVFULL + NS, B_SFULL = B_KVEMPTY + NS;
+constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK;
+constexpr int B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV;
 constexpr int B_SFREE = B_SFULL + 2, B_DSFULL = B_SFREE + 2, B_DSFREE = B_DSFULL + 2;
-constexpr int B_DQFULL = B_DSFREE + 2;
-constexpr int kOffCtl = kOffBar + (B_DQFULL + 1) * 8;
+constexpr int B_DQFULL = B_DSFREE + 2;  // one per MMA thread
+constexpr int B_TURN = B_DQFULL + 2;    // MMA thread e's batch is issued
+constexpr int kOffCtl = kOffBar + (B_TURN + 2) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;  // dQ_e at 256 + 128 e
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace dq
 
@@ -249,9 +294,13 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    for (int st = 0; st < NS; ++st) {
-      mbar_init(bar(B_KVFULL + st), 1);
-      mbar_init(bar(B_KVEMPTY + st), 1);
+    for (int st = 0; st < NK; ++st) {
+      mbar_init(bar(B_KFULL + st), 1);
+      mbar_init(bar(B_KEMPTY + st), 1);
+    }
+    for (int st = 0; st < NV; ++st) {
+      mbar_init(bar(B_VFULL + st), 1);
+      mbar_init(bar(B_VEMPTY + st), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_SFULL + b), 1);
@@ -259,7 +308,10 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       mbar_init(bar(B_DSFULL + b), 4);
       mbar_init(bar(B_DSFREE + b), 1);
     }
-    mbar_init(bar(B_DQFULL), 1);
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(bar(B_DQFULL + e), 1);
+      mbar_init(bar(B_TURN + e), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -277,15 +329,16 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int r = row % p.Nq, h = (row / p.Nq) % p.Hk, i = row / (p.Nq * p.Hk);
   const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
   const int kv0 = __ldg(p.row_ptr + row), nsteps = (__ldg(p.row_ptr + row + 1) - kv0) * KT;
-  const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smKV = sbase + kOffKV,
-                 smDS = sbase + kOffDS;
+  const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
+                 smV = sbase + kOffV, smDS = sbase + kOffDS;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int issued[NS];
-      for (int st = 0; st < NS; ++st) issued[st] = -1;
+      int issued_k[NK], issued_v[NV];
+      for (int st = 0; st < NK; ++st) issued_k[st] = -1;
+      for (int st = 0; st < NV; ++st) issued_v[st] = -1;
       const int hq0 = h * p.G + (t * 128) / BK;
       mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
       for (int pn = 0; pn < 2; ++pn) {
@@ -293,67 +346,80 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
         tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
       }
       for (int s = 0; s < nsteps; ++s) {
-        const int st = s % NS;
-        if (s >= NS &&
-            !(ok = mbar_wait(bar(B_KVEMPTY + st), ((s - NS) / NS) & 1, abort_flag, p.status)))
-          break;
         const int y = s0 + __ldg(p.col_idx + kv0 + s / KT) * BK + (s % KT) * 64;
-        mbar_arrive_expect_tx(bar(B_KVFULL + st), 4 * 8192);
-        issued[st] = (s / NS) & 1;
-        const uint32_t k = smKV + st * 32768, v = k + 16384;
-        for (int pn = 0; pn < 2; ++pn) {
-          tma_load_3d(k + pn * 8192, &tmK, bar(B_KVFULL + st), pn * 64, y, h);
-          tma_load_3d(v + pn * 8192, &tmV, bar(B_KVFULL + st), pn * 64, y, h);
-        }
+        const int sk = s % NK, sv = s % NV;
+        if (s >= NK &&
+            !(ok = mbar_wait(bar(B_KEMPTY + sk), ((s - NK) / NK) & 1, abort_flag, p.status)))
+          break;
+        mbar_arrive_expect_tx(bar(B_KFULL + sk), 2 * 8192);
+        issued_k[sk] = (s / NK) & 1;
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_3d(smK + sk * 16384 + pn * 8192, &tmK, bar(B_KFULL + sk), pn * 64, y, h);
+        if (s >= NV &&
+            !(ok = mbar_wait(bar(B_VEMPTY + sv), ((s - NV) / NV) & 1, abort_flag, p.status)))
+          break;
+        mbar_arrive_expect_tx(bar(B_VFULL + sv), 2 * 8192);
+        issued_v[sv] = (s / NV) & 1;
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_3d(smV + sv * 16384 + pn * 8192, &tmV, bar(B_VFULL + sv), pn * 64, y, h);
       }
       // every copy issued lands before the CTA leaves
       mbar_wait_drain(bar(B_QFULL), 0);
-      for (int st = 0; st < NS; ++st)
-        if (issued[st] >= 0) mbar_wait_drain(bar(B_KVFULL + st), issued[st]);
+      for (int st = 0; st < NK; ++st)
+        if (issued_k[st] >= 0) mbar_wait_drain(bar(B_KFULL + st), issued_k[st]);
+      for (int st = 0; st < NV; ++st)
+        if (issued_v[st] >= 0) mbar_wait_drain(bar(B_VFULL + st), issued_v[st]);
       (void)ok;
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA threads
+    const int e = warp - 9;  // this thread's steps: s = e (mod 2)
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
-      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 64 keys in steps of 16
-        const int b = s & 1;
-        const uint32_t al = desc_lo(smDS + b * 16384, 16);
-        const uint32_t bl = desc_lo(smKV + (s % NS) * 32768, 8192);
+      auto dq_product = [&](int s) {  // dQ_e += dS(s) K(s): 64 keys in steps of 16
+        const uint32_t al = desc_lo(smDS + e * 16384, 16);
+        const uint32_t bl = desc_lo(smK + (s % NK) * 16384, 8192);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss_lo(tmem + kColDQ, al + kk * 2, bl + kk * 128, kDescHi, kIdescDQ,
-                    (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_KVEMPTY + s % NS));
-        mma_commit(bar(B_DSFREE + b));
+          mma_ss_lo(tmem + kColDQ + 128 * e, al + kk * 2, bl + kk * 128, kDescHi, kIdescDQ,
+                    (s >= 2 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_KEMPTY + s % NK));
+        mma_commit(bar(B_DSFREE + e));
       };
-      for (int s = 0; ok && s < nsteps; ++s) {
-        const int st = s % NS, b = s & 1;
-        if (!(ok = mbar_wait(bar(B_KVFULL + st), (s / NS) & 1, abort_flag, p.status))) break;
-        if (s >= 2 &&
-            !(ok = mbar_wait(bar(B_SFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
+      // Both threads run ceil(nsteps / 2) + 1 batches (thread 1 may have empty ones):
+      // batch k is S / dP of step 2k + e and dQ of step 2k + e - 2, each if present.
+      const int nbatch = (nsteps + 1) / 2 + 1;
+      for (int k = 0; ok && k < nbatch; ++k) {
+        const int s = 2 * k + e, sp = s - 2;
+        const bool has_s = s < nsteps, has_prev = sp >= 0 && sp < nsteps;
+        if (has_s) {
+          if (!(ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status)) ||
+              !(ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status)))
+            break;
+          if (s >= 2 &&
+              !(ok = mbar_wait(bar(B_SFREE + e), ((s - 2) >> 1) & 1, abort_flag, p.status)))
+            break;
+        }
+        if (has_prev &&
+            !(ok = mbar_wait(bar(B_DSFULL + e), (sp >> 1) & 1, abort_flag, p.status)))
+          break;
+        // thread 0's batch k follows thread 1's batch k - 1, thread 1's batch k thread 0's
+        if (!(e == 0 && k == 0) &&
+            !(ok = mbar_wait(bar(B_TURN + (1 - e)), (e == 0 ? k - 1 : k) & 1, abort_flag,
+                             p.status)))
           break;
         tc_fence_after();
-        const uint32_t k = smKV + st * 32768, v = k + 16384;
-        mma_xyT(tmem + kColS + 64 * b, smQ, k);
-        mma_xyT(tmem + kColDP + 64 * b, smDO, v);
-        mma_commit(bar(B_SFULL + b));
-        if (s >= 1) {
-          if (!(ok = mbar_wait(bar(B_DSFULL + (b ^ 1)), ((s - 1) >> 1) & 1, abort_flag,
-                               p.status)))
-            break;
-          tc_fence_after();
-          dq_product(s - 1);
+        if (has_s) {
+          mma_xyT(tmem + kColS + 64 * e, smQ, smK + (s % NK) * 16384);
+          mma_xyT(tmem + kColDP + 64 * e, smDO, smV + (s % NV) * 16384);
+          mma_commit(bar(B_SFULL + e));
+          mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
         }
+        if (has_prev) dq_product(sp);
+        mbar_arrive(bar(B_TURN + e));
       }
-      if (ok && nsteps > 0 &&
-          (ok = mbar_wait(bar(B_DSFULL + ((nsteps - 1) & 1)), ((nsteps - 1) >> 1) & 1, abort_flag,
-                          p.status))) {
-        tc_fence_after();
-        dq_product(nsteps - 1);
-      }
-      mma_commit(bar(B_DQFULL));
-      mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
+      mma_commit(bar(B_DQFULL + e));
+      mbar_wait_drain(bar(B_DQFULL + e), 0);  // MMAs done before TMEM is freed
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -384,14 +450,21 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
         mbar_arrive(bar(B_DSFULL + b));
       }
     }
-    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
-    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
+    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ =
+    // dQ_0 + dQ_1 (dQ_1 holds the odd steps; there are none when nsteps == 1)
+    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status) &&
+        mbar_wait(bar(B_DQFULL + 1), 0, abort_flag, p.status)) {
       tc_fence_after();
       uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
+        uint32_t rr[32], r1[32];
         tmem_ld32(tmem + lane_base + kColDQ + 64 * g + c0, rr);
+        tmem_ld32(tmem + lane_base + kColDQ + 128 + 64 * g + c0, r1);
+        if (nsteps >= 2)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            rr[c] = __float_as_uint(__uint_as_float(rr[c]) + __uint_as_float(r1[c]));
         uint32_t o[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
