@@ -501,8 +501,8 @@ constexpr int kOffK = 0, kOffV = 16384, kOffQ = 32768, kOffDO = kOffQ + 2 * 3276
 constexpr int kOffP = kOffDO + 2 * 32768, kOffDS = kOffP + 2 * 16384;
 constexpr int kOffBar = kOffDS + 2 * 16384;
 constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_SFREE = 7;
-constexpr int B_PDSFULL = 9, B_PDSFREE = 11, B_DONE = 13;
-constexpr int kOffCtl = kOffBar + 14 * 8;
+constexpr int B_PDSFULL = 9, B_PDSFREE = 11, B_DONE = 13, B_DOFULL = 14, B_DOEMPTY = 16;
+constexpr int kOffCtl = kOffBar + 18 * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kTmemCols = 512;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -530,6 +530,8 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_QFULL + b), 1);
       mbar_init(bar(B_QEMPTY + b), 1);
+      mbar_init(bar(B_DOFULL + b), 1);
+      mbar_init(bar(B_DOEMPTY + b), 1);
       mbar_init(bar(B_SFULL + b), 1);
       mbar_init(bar(B_SFREE + b), 4);
       mbar_init(bar(B_PDSFULL + b), 4);
@@ -562,50 +564,78 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int issued[2] = {-1, -1};
+      int issued_q[2] = {-1, -1}, issued_do[2] = {-1, -1};
       mbar_arrive_expect_tx(bar(B_KVFULL), 4 * 8192);
       for (int pn = 0; pn < 2; ++pn) {
         tma_load_3d(smK + pn * 8192, &tmK, bar(B_KVFULL), pn * 64, key_row, h);
         tma_load_3d(smV + pn * 8192, &tmV, bar(B_KVFULL), pn * 64, key_row, h);
       }
+      auto tile_coord = [&](int nt, int &y, int &hq) {
+        y = s0 + row_of(nt) * BK;
+        hq = h * p.G + ((nt % p.mtiles) * 128) / BK;
+      };
+      // Q / dO of the tiles two and three ahead go to L2 now, so that the ring's
+      // copies (issued only when a stage frees) find them there
+      auto prefetch = [&](int nt) {
+        if (nt >= ntiles) return;
+        int y, hq;
+        tile_coord(nt, y, hq);
+        for (int pn = 0; pn < 2; ++pn) {
+          tma_prefetch_l2_3d(&tmQ, pn * 64, y, hq);
+          tma_prefetch_l2_3d(&tmDO, pn * 64, y, hq);
+        }
+      };
+      prefetch(0);
+      prefetch(1);
       for (int nt = 0; nt < ntiles; ++nt) {
         const int st = nt & 1;
+        int y, hq;
+        tile_coord(nt, y, hq);
+        prefetch(nt + 2);
         if (nt >= 2 && !(ok = mbar_wait(bar(B_QEMPTY + st), ((nt - 2) >> 1) & 1, abort_flag,
                                         p.status)))
           break;
-        const int r = row_of(nt), t = nt % p.mtiles;
-        const int hq0 = h * p.G + (t * 128) / BK;
-        mbar_arrive_expect_tx(bar(B_QFULL + st), 4 * 16384);
-        issued[st] = (nt >> 1) & 1;
-        for (int pn = 0; pn < 2; ++pn) {
-          tma_load_3d(smQ + st * 32768 + pn * 16384, &tmQ, bar(B_QFULL + st), pn * 64,
-                      s0 + r * BK, hq0);
-          tma_load_3d(smDO + st * 32768 + pn * 16384, &tmDO, bar(B_QFULL + st), pn * 64,
-                      s0 + r * BK, hq0);
-        }
+        mbar_arrive_expect_tx(bar(B_QFULL + st), 2 * 16384);
+        issued_q[st] = (nt >> 1) & 1;
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_3d(smQ + st * 32768 + pn * 16384, &tmQ, bar(B_QFULL + st), pn * 64, y, hq);
+        if (nt >= 2 && !(ok = mbar_wait(bar(B_DOEMPTY + st), ((nt - 2) >> 1) & 1, abort_flag,
+                                        p.status)))
+          break;
+        mbar_arrive_expect_tx(bar(B_DOFULL + st), 2 * 16384);
+        issued_do[st] = (nt >> 1) & 1;
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_3d(smDO + st * 32768 + pn * 16384, &tmDO, bar(B_DOFULL + st), pn * 64, y, hq);
       }
       // every copy issued lands before the CTA leaves (on the normal path the MMA
       // warp has consumed them all; after an abort this waits out the flights)
       mbar_wait_drain(bar(B_KVFULL), 0);
-      for (int st = 0; st < 2; ++st)
-        if (issued[st] >= 0) mbar_wait_drain(bar(B_QFULL + st), issued[st]);
+      for (int st = 0; st < 2; ++st) {
+        if (issued_q[st] >= 0) mbar_wait_drain(bar(B_QFULL + st), issued_q[st]);
+        if (issued_do[st] >= 0) mbar_wait_drain(bar(B_DOFULL + st), issued_do[st]);
+      }
       (void)ok;
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
-      auto kv_products = [&](int nt) {  // dV^T += dO^T P, dK^T += Q^T dS of tile nt
+      // dK^T += Q^T dS, then dV^T += dO^T P of tile nt: Q's stage is released
+      // first, so its next copy starts while the dV products run
+      auto kv_products = [&](int nt) {
         const int b = nt & 1;
         const uint32_t dol = desc_lo(smDO + b * 32768, 16384), pl = desc_lo(smP + b * 16384, 16384);
         const uint32_t ql = desc_lo(smQ + b * 32768, 16384), dsl = desc_lo(smDS + b * 16384, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 128 query rows in steps of 16 (2048 bytes)
-          const uint32_t acc = (nt > 0 || kk > 0) ? 1u : 0u;
-          mma_ss_lo(tmem + kColDV, dol + kk * 128, pl + kk * 128, kDescHi, kIdescKV, acc);
-          mma_ss_lo(tmem + kColDK, ql + kk * 128, dsl + kk * 128, kDescHi, kIdescKV, acc);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // 128 query rows in steps of 16 (2048 bytes)
+          mma_ss_lo(tmem + kColDK, ql + kk * 128, dsl + kk * 128, kDescHi, kIdescKV,
+                    (nt > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_QEMPTY + b));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_lo(tmem + kColDV, dol + kk * 128, pl + kk * 128, kDescHi, kIdescKV,
+                    (nt > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_DOEMPTY + b));
         mma_commit(bar(B_PDSFREE + b));
       };
       for (int nt = 0; ok && nt < ntiles; ++nt) {
@@ -616,6 +646,8 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
           break;
         tc_fence_after();
         mma_xyT(tmem + kColS + 64 * b, smQ + b * 32768, smK);
+        if (!(ok = mbar_wait(bar(B_DOFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
         mma_xyT(tmem + kColDP + 64 * b, smDO + b * 32768, smV);
         mma_commit(bar(B_SFULL + b));
         if (nt >= 1) {
