@@ -9,7 +9,10 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libbsa.so")
+# BSA_BOUNDS_CHECK=1 selects the bounds-checked build (libbsa_bounds.so, built by
+# build(bounds_check=True)): same ABI, every table index range-checked on the device.
+BOUNDS_CHECK = os.environ.get("BSA_BOUNDS_CHECK", "0") == "1"
+LIB_PATH = os.path.join(PKG, "libbsa_bounds.so" if BOUNDS_CHECK else "libbsa.so")
 
 BSA_OK = 0
 STATUS_NAMES = {
@@ -62,6 +65,7 @@ I32 = ctypes.c_int32
 F32 = ctypes.c_float
 PROTOTYPES = {
     "bsa_version": (I32, []),
+    "bsa_bounds_checked": (I32, []),
     "bsa_status_string": (ctypes.c_char_p, [I32]),
     "bsa_block_summaries": (I32, [ctypes.POINTER(Shape), V, V, V]),
     "bsa_route_workspace_size": (SZ, [ctypes.POINTER(Shape), ctypes.POINTER(RouteParams)]),

@@ -107,6 +107,8 @@ extern "C" {
 
 int32_t bsa_version(void) { return BSA_VERSION; }
 
+int32_t bsa_bounds_checked(void) { return BSA_BOUNDS_CHECK ? 1 : 0; }
+
 const char *bsa_status_string(bsa_status_t s) {
   switch (s) {
     case BSA_OK: return "ok";
@@ -363,7 +365,7 @@ bsa_status_t bsa_attention_fwd(const bsa_shape_t *shape, const void *Q, const vo
     return launched(bsa::launch_attention_tc(*shape, Q, K, V, row_ptr, col_idx, work, bucket_off,
                                              scale, O, lse, dev_status, stream));
   return launched(bsa::launch_attention_simt_f32(*shape, Q, K, V, row_ptr, col_idx, work,
-                                                 bucket_off, scale, O, lse, stream));
+                                                 bucket_off, scale, O, lse, dev_status, stream));
 }
 
 bsa_status_t bsa_page_summaries(const bsa_decode_shape_t *shape, const void *k_cache,

@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_kernel(
     const int32_t *__restrict__ cu, const int32_t *__restrict__ row_ptr,
     const int32_t *__restrict__ col_idx, const int32_t *__restrict__ work,
     const int32_t *__restrict__ bucket_off, float scale, T *__restrict__ dQ,
-    float *__restrict__ dK32, float *__restrict__ dV32, int T_tok, int Nq, int Hk, int G) {
+    float *__restrict__ dK32, float *__restrict__ dV32, int T_tok, int Nq, int Hk, int G,
+    int32_t *__restrict__ status) {
   constexpr int DP = D + 1;                  // padded shared rows (conflict-free columns)
   constexpr int KP = kKC + 1;
   constexpr int EQ = B * D / kBwdThreads;    // dQ elements per thread
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_kernel(
 
   const int kb0 = row_ptr[row], nkv = row_ptr[row + 1] - kb0;
   for (int jj = 0; jj < nkv; ++jj) {
-    const int kb = col_idx[kb0 + jj];
+    const int kb = checked_index(col_idx[kb0 + jj], 0, r, status);
     for (int c0 = 0; c0 < B; c0 += kKC) {
       __syncthreads();
       for (int e = tid; e < kKC * D; e += kBwdThreads) {
@@ -224,7 +225,7 @@ cudaError_t launch_bwd(const bsa_shape_t &s, const void *Q, const void *K, const
                        const void *dO, const float *lse, const float *Dv,
                        const int32_t *row_ptr, const int32_t *col_idx, const int32_t *work,
                        const int32_t *bucket_off, float scale, void *dQ, float *dK32,
-                       float *dV32, cudaStream_t st) {
+                       float *dV32, int32_t *status, cudaStream_t st) {
   const size_t sm =
       (size_t)(2 * B * (D + 1) + 2 * kKC * (D + 1) + 2 * B * (kKC + 1) + 2 * B) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<T, D, B>,
@@ -235,7 +236,8 @@ cudaError_t launch_bwd(const bsa_shape_t &s, const void *Q, const void *K, const
   attn_bwd_kernel<T, D, B><<<(unsigned)units, kBwdThreads, sm, st>>>(
       static_cast<const T *>(Q), static_cast<const T *>(K), static_cast<const T *>(V),
       static_cast<const T *>(dO), lse, Dv, s.cu_seqlens, row_ptr, col_idx, work, bucket_off,
-      scale, static_cast<T *>(dQ), dK32, dV32, s.total_tokens, s.max_blocks, s.num_kv_heads, G);
+      scale, static_cast<T *>(dQ), dK32, dV32, s.total_tokens, s.max_blocks, s.num_kv_heads, G,
+      status);
   return cudaGetLastError();
 }
 
@@ -244,7 +246,7 @@ cudaError_t launch_bwd_typed(const bsa_shape_t &s, const void *Q, const void *K,
                              const void *O, const void *dO, const float *lse,
                              const int32_t *row_ptr, const int32_t *col_idx, const int32_t *work,
                              const int32_t *bucket_off, float scale, void *dQ, void *dK, void *dV,
-                             void *ws, cudaStream_t st) {
+                             void *ws, int32_t *status, cudaStream_t st) {
   const size_t hrows = (size_t)s.num_heads * s.total_tokens;
   const size_t kv = (size_t)s.num_kv_heads * s.total_tokens * s.head_dim;
   char *w = static_cast<char *>(ws);
@@ -263,16 +265,16 @@ cudaError_t launch_bwd_typed(const bsa_shape_t &s, const void *Q, const void *K,
   if (e != cudaSuccess) return e;
   if (s.head_dim == 64 && s.block == 64)
     e = launch_bwd<T, 64, 64>(s, Q, K, V, dO, lse, Dv, row_ptr, col_idx, work, bucket_off, scale,
-                              dQ, dK32, dV32, st);
+                              dQ, dK32, dV32, status, st);
   else if (s.head_dim == 64 && s.block == 128)
     e = launch_bwd<T, 64, 128>(s, Q, K, V, dO, lse, Dv, row_ptr, col_idx, work, bucket_off, scale,
-                               dQ, dK32, dV32, st);
+                               dQ, dK32, dV32, status, st);
   else if (s.head_dim == 128 && s.block == 64)
     e = launch_bwd<T, 128, 64>(s, Q, K, V, dO, lse, Dv, row_ptr, col_idx, work, bucket_off, scale,
-                               dQ, dK32, dV32, st);
+                               dQ, dK32, dV32, status, st);
   else
     e = launch_bwd<T, 128, 128>(s, Q, K, V, dO, lse, Dv, row_ptr, col_idx, work, bucket_off,
-                                scale, dQ, dK32, dV32, st);
+                                scale, dQ, dK32, dV32, status, st);
   if (e != cudaSuccess) return e;
   bwd_convert_kernel<T><<<zgrid, 256, 0, st>>>(dK32, static_cast<T *>(dK), kv);
   bwd_convert_kernel<T><<<zgrid, 256, 0, st>>>(dV32, static_cast<T *>(dV), kv);
@@ -312,9 +314,9 @@ cudaError_t launch_attention_bwd(const bsa_shape_t &s, const void *Q, const void
   }
   if (s.dtype == BSA_BF16)
     return launch_bwd_typed<uint16_t>(s, Q, K, V, O, dO, lse, row_ptr, col_idx, work, bucket_off,
-                                      scale, dQ, dK, dV, ws, st);
+                                      scale, dQ, dK, dV, ws, dev_status, st);
   return launch_bwd_typed<float>(s, Q, K, V, O, dO, lse, row_ptr, col_idx, work, bucket_off,
-                                 scale, dQ, dK, dV, ws, st);
+                                 scale, dQ, dK, dV, ws, dev_status, st);
 }
 
 }  // namespace bsa

@@ -190,13 +190,16 @@ BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
 // ceil(N_q / 32) words.
 __global__ void kt_mark_kernel(const int32_t *__restrict__ row_ptr,
                                const int32_t *__restrict__ col_idx, int nrows, int Nq, int W,
-                               uint32_t *__restrict__ bits) {
+                               uint32_t *__restrict__ bits, int32_t *__restrict__ status) {
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < nrows;
        row += gridDim.x * blockDim.x) {
     const int r = row % Nq, base = row - r;
     for (int e = row_ptr[row]; e < row_ptr[row + 1]; ++e) {
       const int j = col_idx[e];
-      if (j >= 0 && j <= r) atomicOr(bits + (size_t)(base + j) * W + r / 32, 1u << (r % 32));
+      if (j >= 0 && j <= r)
+        atomicOr(bits + (size_t)(base + j) * W + r / 32, 1u << (r % 32));
+      else if (BSA_BOUNDS_CHECK)
+        set_status(status, BSA_ERR_INDEX_RANGE);  // skipped in every build
     }
   }
 }
@@ -346,7 +349,8 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
         tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
       }
       for (int s = 0; s < nsteps; ++s) {
-        const int y = s0 + __ldg(p.col_idx + kv0 + s / KT) * BK + (s % KT) * 64;
+        const int y =
+            s0 + checked_index(__ldg(p.col_idx + kv0 + s / KT), 0, r, p.status) * BK + (s % KT) * 64;
         const int sk = s % NK, sv = s % NV;
         if (s >= NK &&
             !(ok = mbar_wait(bar(B_KEMPTY + sk), ((s - NK) / NK) & 1, abort_flag, p.status)))
@@ -811,7 +815,8 @@ cudaError_t launch_attention_bwd_tc(const bsa_shape_t &s, const void *Q, const v
   if ((e = cudaMemsetAsync(dK, 0, kv_bytes, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dV, 0, kv_bytes, st)) != cudaSuccess) return e;
   const int blocks = std::max(1, std::min(4 * num_sms(), (nrows + 255) / 256));
-  kt_mark_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, W, bits);
+  kt_mark_kernel<<<blocks, 256, 0, st>>>(row_ptr, col_idx, nrows, s.max_blocks, W, bits,
+                                         dev_status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   kt_count_kernel<<<blocks, 256, 0, st>>>(bits, nrows, W, cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(
     const int32_t *__restrict__ cu, const int32_t *__restrict__ row_ptr,
     const int32_t *__restrict__ col_idx, const int32_t *__restrict__ work,
     const int32_t *__restrict__ bucket_off, float scale, float *__restrict__ O,
-    float *__restrict__ lse, int T_tok, int Nq, int Hk, int G) {
+    float *__restrict__ lse, int T_tok, int Nq, int Hk, int G, int32_t *__restrict__ status) {
   constexpr int RPW = B / kWarps;  // query rows per warp
   constexpr int DL = D / 32;       // output columns per lane
   extern __shared__ float smem[];
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(
   }
   const int kb0 = row_ptr[row], nkv = row_ptr[row + 1] - kb0;
   for (int jj = 0; jj < nkv; ++jj) {
-    const int kb = col_idx[kb0 + jj];
+    const int kb = checked_index(col_idx[kb0 + jj], 0, r, status);
     for (int c0 = 0; c0 < B; c0 += kChunk) {
       __syncthreads();
       for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
@@ -106,7 +106,7 @@ template <int D, int B>
 cudaError_t launch_simt(const bsa_shape_t &s, const void *Q, const void *K, const void *V,
                         const int32_t *row_ptr, const int32_t *col_idx, const int32_t *work,
                         const int32_t *bucket_off, float scale, void *O, float *lse,
-                        cudaStream_t st) {
+                        int32_t *status, cudaStream_t st) {
   const size_t sm = (size_t)(B * D + kChunk * (D + 1) + kChunk * D) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<D, B>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -116,7 +116,7 @@ cudaError_t launch_simt(const bsa_shape_t &s, const void *Q, const void *K, cons
   attn_simt_kernel<D, B><<<(unsigned)units, kWarps * 32, sm, st>>>(
       static_cast<const float *>(Q), static_cast<const float *>(K), static_cast<const float *>(V),
       s.cu_seqlens, row_ptr, col_idx, work, bucket_off, scale, static_cast<float *>(O), lse,
-      s.total_tokens, s.max_blocks, s.num_kv_heads, G);
+      s.total_tokens, s.max_blocks, s.num_kv_heads, G, status);
   return cudaGetLastError();
 }
 
@@ -126,14 +126,18 @@ cudaError_t launch_attention_simt_f32(const bsa_shape_t &s, const void *Q, const
                                       const void *V, const int32_t *row_ptr,
                                       const int32_t *col_idx, const int32_t *work,
                                       const int32_t *bucket_off, float scale, void *O,
-                                      float *lse, cudaStream_t st) {
+                                      float *lse, int32_t *status, cudaStream_t st) {
   if (s.head_dim == 64 && s.block == 64)
-    return launch_simt<64, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, st);
+    return launch_simt<64, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, status,
+                               st);
   if (s.head_dim == 64 && s.block == 128)
-    return launch_simt<64, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, st);
+    return launch_simt<64, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, status,
+                                st);
   if (s.head_dim == 128 && s.block == 64)
-    return launch_simt<128, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, st);
-  return launch_simt<128, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, st);
+    return launch_simt<128, 64>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse, status,
+                                st);
+  return launch_simt<128, 128>(s, Q, K, V, row_ptr, col_idx, work, bucket_off, scale, O, lse,
+                               status, st);
 }
 
 }  // namespace bsa

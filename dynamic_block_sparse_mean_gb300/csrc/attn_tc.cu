@@ -108,6 +108,7 @@ struct AttnParams {
   const int32_t *qoff;
   const int32_t *bt;
   int maxp;
+  int num_phys;   // physical pages of the cache (CHUNK kernels only)
   int T, H, Hk, G, Nq, mtiles, npairs;
   float scale_log2;
 };
@@ -152,10 +153,11 @@ BSA_DEV Unit decode_unit(const AttnParams &p, int u) {
 // clamped to the table; a physical id outside the cache reads zeros).
 template <bool CHUNK, int BK>
 BSA_DEV int2 kv_coord(const AttnParams &p, const Unit &w, int jb) {
-  const int j = __ldg(p.col_idx + w.kv0 + jb);
+  const int j = checked_index(__ldg(p.col_idx + w.kv0 + jb), 0, w.r, p.status);
   if constexpr (CHUNK) {
     const int pg = min(max(j, 0), p.maxp - 1);
-    const int phys = __ldg(p.bt + (size_t)w.i * p.maxp + pg);
+    const int phys =
+        checked_index(__ldg(p.bt + (size_t)w.i * p.maxp + pg), 0, p.num_phys - 1, p.status);
     return make_int2((phys * p.Hk + w.h) * 64, 0);
   } else {
     return make_int2(w.s0 + j * BK, w.h);
@@ -778,6 +780,7 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   p.qoff = CHUNK ? cache->prefix_lens : nullptr;
   p.bt = CHUNK ? cache->block_table : nullptr;
   p.maxp = CHUNK ? cache->max_pages_per_req : 0;
+  p.num_phys = CHUNK ? cache->num_phys_pages : 0;
   p.T = s.total_tokens;
   p.H = s.num_heads;
   p.Hk = s.num_kv_heads;

@@ -22,6 +22,30 @@ BSA_DEV void set_status(int32_t *status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Bounds-checked builds (-DBSA_BOUNDS_CHECK=1, libbsa_bounds.so): an index read from
+// a caller-visible table (worklist col_idx, decode selection, block table) that is
+// about to address memory is checked against [lo, hi]; one outside records
+// BSA_ERR_INDEX_RANGE and is clamped into the range, so the kernel keeps its
+// control flow and never addresses memory outside its buffers.  The default build
+// trusts these tables (they come from the library's own validated kernels) and
+// compiles the check away.
+#ifndef BSA_BOUNDS_CHECK
+#define BSA_BOUNDS_CHECK 0
+#endif
+BSA_DEV int checked_index(int v, int lo, int hi, int32_t *status) {
+#if BSA_BOUNDS_CHECK
+  if (v < lo || v > hi) {
+    set_status(status, BSA_ERR_INDEX_RANGE);
+    return v < lo ? lo : hi;
+  }
+#else
+  (void)lo;
+  (void)hi;
+  (void)status;
+#endif
+  return v;
+}
+
 // A chunk of n > 0 tokens that follows `prefix` cached tokens is usable when the
 // prefix is whole blocks of b and the context fits in Nk blocks (computed without
 // forming prefix + n, which a bad prefix could overflow).  A sequence adding no

@@ -428,11 +428,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (2 * c < cnt && len_ok(n, p.max_pages)) {
           live = true;
           const int32_t *sp = p.sel + (size_t)pair * per_pair + 2 * c;
-          const int lpA = __ldg(sp);
+          const int lpA = checked_index(__ldg(sp), 0, p.max_pages - 1, p.status);
           zA = dec_page_coord(p, rho, h, lpA);
           vA = min(kPage, n - lpA * kPage);
           if (2 * c + 1 < cnt) {
-            const int lpB = __ldg(sp + 1);
+            const int lpB = checked_index(__ldg(sp + 1), 0, p.max_pages - 1, p.status);
             zB = dec_page_coord(p, rho, h, lpB);
             vB = min(kPage, n - lpB * kPage);
           } else {

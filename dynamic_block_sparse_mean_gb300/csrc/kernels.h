@@ -141,7 +141,7 @@ cudaError_t launch_attention_simt_f32(const bsa_shape_t &s, const void *Q, const
                                       const void *V, const int32_t *row_ptr,
                                       const int32_t *col_idx, const int32_t *work,
                                       const int32_t *bucket_off, float scale, void *O,
-                                      float *lse, cudaStream_t st);
+                                      float *lse, int32_t *status, cudaStream_t st);
 
 // a6 (decode.cu)
 size_t decode_workspace_bytes(const bsa_decode_shape_t &s);

@@ -504,6 +504,19 @@ const char *bsa_status_string(bsa_status_t status);
 /* BSA_VERSION of the built library. */
 int32_t bsa_version(void);
 
+/* 1 in the bounds-checked build (libbsa_bounds.so, compiled with
+ * -DBSA_BOUNDS_CHECK=1), 0 in the default build.  The bounds-checked build
+ * range-checks, on the device, every index its kernels read from a caller-visible
+ * table before using it to address memory: worklist col_idx entries against
+ * [0, r] of their row (bsa_attention_fwd, bsa_attention_bwd, bsa_attention_chunk),
+ * chunk block-table entries against [0, num_phys_pages), and decode selections
+ * against [0, max_pages_per_req).  An index outside its range sets
+ * BSA_ERR_INDEX_RANGE in dev_status and is clamped into the range, so the call
+ * completes without touching memory outside its buffers (its outputs are then
+ * meaningless).  The default build trusts these tables, which the library's own
+ * validated kernels produce.  Same ABI and results otherwise. */
+int32_t bsa_bounds_checked(void);
+
 #ifdef __cplusplus
 }
 #endif
