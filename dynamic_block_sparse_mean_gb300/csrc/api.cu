@@ -96,7 +96,7 @@ bool decode_ok(const bsa_decode_shape_t *s) {
 bool decode_supported(const bsa_decode_shape_t *s) {
   const int G = s->num_heads / s->num_kv_heads;
   return s->head_dim == 128 && s->page_size == 64 && s->top_k >= 1 && s->top_k <= 64 &&
-         (G == 1 || G == 2 || G == 4 || G == 8) && s->num_heads <= 256 &&
+         (G == 1 || G == 2 || G == 4 || G == 8) && s->num_heads <= 256 && s->num_reqs <= 65535 &&
          s->max_pages_per_req <= 16384 &&
          (long long)s->num_phys_pages * s->num_kv_heads < INT32_MAX;
 }

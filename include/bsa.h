@@ -302,6 +302,7 @@ bsa_status_t bsa_page_summaries_append(const bsa_decode_shape_t *shape, const vo
  *   sel      : [R, H_kv, top_k + 1] int32 logical pages, -1 padded.
  *   sel_counts : [R, H_kv] int32.
  *   ws       : at least bsa_decode_workspace_size() bytes, 256-byte aligned.
+ *   num_reqs <= 65535 (else BSA_ERR_UNSUPPORTED).
  *   Lengths and page ids are checked on the device before they index anything:
  *   - context_lens[rho] == 0 is an idle slot (a padded batch): sel row all -1,
  *     count 0, o = 0, lse = -inf, no error.
