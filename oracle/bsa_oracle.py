@@ -55,7 +55,9 @@ bound of [P2] §4; the online-softmax recurrences against the direct softmax;
 eq.(11) streaming means; the worked budget numbers of [P2] §2.2 (golden file);
 token recall against the dense top-t teacher worked by hand (ties, GQA, an
 empty row), equal to 1 at density 1 and to the explicit mask's key count when
-the teacher covers every visible key.
+the teacher covers every visible key; the backward against central differences,
+against autograd of the dense causal attention at density 1, and its one-row /
+one-key-block restriction against the whole-sequence backward.
 """
 from __future__ import annotations
 
@@ -397,6 +399,63 @@ def attention_backward(Q, K, V, cu_seqlens, b: int, G: int, J, counts, dO, scale
                 dK[h, s0:s0 + n] += gk.numpy()
                 dV[h, s0:s0 + n] += gv.numpy()
     return dQ, dK, dV
+
+
+def attention_backward_row(Q, K, V, cu_seqlens, b: int, G: int, J, counts, dO, row,
+                           scale=None):
+    """The backward of one router row (i, h_kv, r) alone, for sampled checks at sizes
+    where `attention_backward` cannot materialise a sequence: the same definition
+    (mask {s : block(s) in J_r, s <= t} before the softmax, O = softmax(S) V, torch
+    autograd of sum(O * dO)) over the row's query tokens of every query head of the
+    group.  The row's queries meet no other row, so its dQ [G, n_r, d] is exact; its
+    keys 0 .. t_max receive this row's share of dK and dV [t_max + 1, d] (summed over
+    the group's heads), which the rows selecting a key block add up to that block's
+    dK and dV (`attention_backward_key_block`)."""
+    i, h, r = row
+    d = Q.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s0, n, nb = seq_info(cu_seqlens, b)[i]
+    cnt = int(counts[i, h, r])
+    mult = block_multiplicity(J[i, h, r, :cnt], nb, r)
+    q_lo, q_hi = r * b, min(n, (r + 1) * b)
+    mask = torch.from_numpy(key_mask(q_lo, q_hi, mult, b))
+    k = torch.tensor(_f64(K[h, s0:s0 + q_hi]), requires_grad=True)
+    v = torch.tensor(_f64(V[h, s0:s0 + q_hi]), requires_grad=True)
+    dq = np.empty((G, q_hi - q_lo, d))
+    dk = np.zeros((q_hi, d))
+    dv = np.zeros((q_hi, d))
+    for g, hq in enumerate(range(h * G, (h + 1) * G)):
+        q = torch.tensor(_f64(Q[hq, s0 + q_lo:s0 + q_hi]), requires_grad=True)
+        sc = ((q @ k.T) * scale).masked_fill(~mask, float("-inf"))
+        o = torch.softmax(sc, dim=-1) @ v
+        gout = torch.from_numpy(_f64(dO[hq, s0 + q_lo:s0 + q_hi]))
+        gq, gk, gv = torch.autograd.grad((o * gout).sum(), (q, k, v))
+        dq[g] = gq.numpy()
+        dk += gk.numpy()
+        dv += gv.numpy()
+    return dq, dk, dv
+
+
+def attention_backward_key_block(Q, K, V, cu_seqlens, b: int, G: int, J, counts, dO, i: int,
+                                 h: int, j: int, scale=None):
+    """dK and dV [n_j, d] of key block j of sequence i and KV head h: the sum, over
+    every row r >= j whose selected SET holds j (an empty row holds {r}, R-7), of
+    that row's share from `attention_backward_row`."""
+    s0, n, nb = seq_info(cu_seqlens, b)[i]
+    lo, hi = j * b, min(n, (j + 1) * b)
+    dk = np.zeros((hi - lo, Q.shape[2]))
+    dv = np.zeros((hi - lo, Q.shape[2]))
+    for r in range(j, nb):
+        cnt = int(counts[i, h, r])
+        sel = {int(x) for x in J[i, h, r, :cnt]} or {r}
+        if j not in sel:
+            continue
+        _, gk, gv = attention_backward_row(Q, K, V, cu_seqlens, b, G, J, counts, dO, (i, h, r),
+                                           scale)
+        dk += gk[lo:hi]
+        dv += gv[lo:hi]
+    return dk, dv
 
 
 def causal_all_blocks(cu_seqlens, b: int, Hk: int):

@@ -107,3 +107,63 @@ def test_decode_workload_sampled_requests():
     d = np.abs(og - oo[reqs])
     assert d.max() <= BF16_MAX_ABS and d.mean() <= BF16_MEAN_ABS
     assert np.abs(lse.cpu().numpy()[reqs] - lo[reqs]).max() <= BF16_LSE_ABS
+
+
+BACKWARD = [(workloads.PROMPT_32K, 6, 3, 24), (workloads.LONG_128K, 3, 2, 10)]
+BWD_REL = 2e-2  # bf16 gradients: max |diff| / max |ref|, as in test_gpu_backward.py
+
+
+@pytest.mark.parametrize("w,n_rows,n_blocks,max_sel", BACKWARD, ids=[w.name for w, *_ in BACKWARD])
+def test_backward_workload_sampled(w, n_rows, n_blocks, max_sel):
+    """The backward at full size, launched as bench.py launches it (the forward's
+    worklist and lse), on sampled outputs the oracle computes one by one: dQ of
+    whole router rows, and dK / dV of key blocks selected by at most max_sel rows
+    (the oracle sums those rows' shares), on the index the GPU used."""
+    x = synth.make_prefill(w)
+    q, k, v = (dev_tensor(a, "bf16") for a in (x.q, x.k, x.v))
+    plan = bsa.PrefillPlan(x.cu_seqlens, w.num_heads, w.num_kv_heads, w.head_dim, w.block,
+                           bsa.RouteParams(w.mode, w.k_max, w.k_min, w.tau_delta, w.force_sink))
+    out, lse = plan.run(q, k, v)
+    rng = np.random.default_rng(w.seed + 7)
+    dO_bits = synth.f32_to_bf16_bits(rng.normal(size=x.q.shape).astype(np.float32))
+    do = dev_tensor(dO_bits, "bf16")
+    dq, dk, dv = bsa.attention_bwd(q, k, v, out, do, lse, plan.wl, plan.shape)
+    torch.cuda.synchronize()
+    bsa.check_status(plan.status)
+    J, cnt = plan.J.cpu().numpy(), plan.counts.cpu().numpy()
+    Q, K, V, dO = BF16View(x.q), BF16View(x.k), BF16View(x.v), BF16View(dO_bits)
+    G, b = w.group, w.block
+    info = oracle.seq_info(x.cu_seqlens, b)
+
+    def rel(got, ref):
+        return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+    rows = sample_rows(x.cu_seqlens, b, w.num_kv_heads, 0, seed=w.seed)
+    picked = [rows[int(e)] for e in rng.choice(len(rows), size=min(n_rows, len(rows)),
+                                              replace=False)]
+    for (i, h, r) in picked:
+        ref, _, _ = oracle.attention_backward_row(Q, K, V, x.cu_seqlens, b, G, J, cnt, dO,
+                                                  (i, h, r))
+        s0, n, _ = info[i]
+        t0, t1 = s0 + r * b, s0 + min(n, (r + 1) * b)
+        got = dq[h * G:(h + 1) * G, t0:t1].float().cpu().numpy()
+        assert rel(got, ref) <= BWD_REL, ("dQ", (i, h, r), rel(got, ref))
+    # key blocks with a few selecting rows, spread over sequences, heads and positions
+    nsel = {}
+    for i, (s0, n, nb) in enumerate(info):
+        for h in range(w.num_kv_heads):
+            for r in range(nb):
+                for j in {int(e) for e in J[i, h, r, :cnt[i, h, r]]} or {r}:
+                    nsel[(i, h, j)] = nsel.get((i, h, j), 0) + 1
+    cands = sorted(key for key, c in nsel.items() if 2 <= c <= max_sel)
+    assert cands
+    for e in rng.choice(len(cands), size=min(n_blocks, len(cands)), replace=False):
+        i, h, j = cands[int(e)]
+        ref_k, ref_v = oracle.attention_backward_key_block(Q, K, V, x.cu_seqlens, b, G, J, cnt,
+                                                           dO, i, h, j)
+        s0, n, _ = info[i]
+        t0, t1 = s0 + j * b, s0 + min(n, (j + 1) * b)
+        got_k = dk[h, t0:t1].float().cpu().numpy()
+        got_v = dv[h, t0:t1].float().cpu().numpy()
+        assert rel(got_k, ref_k) <= BWD_REL, ("dK", (i, h, j), rel(got_k, ref_k))
+        assert rel(got_v, ref_v) <= BWD_REL, ("dV", (i, h, j), rel(got_v, ref_v))

@@ -365,6 +365,33 @@ def test_backward_matches_central_differences():
             assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
 
 
+def test_backward_row_and_key_block_equal_the_full_backward():
+    # The sampled backward (one router row's dQ; one key block's dK / dV summed over
+    # the rows that selected it) against the whole-sequence backward, itself pinned to
+    # central differences and to the dense gradients above.  Rows include an empty
+    # one (R-7: it holds its diagonal) and ragged tails.
+    x, Q, K, V = _inputs([170, 75], 4, 2, 8, 32, seed=65)
+    G, b = 2, 32
+    Jo, co, _, _ = oracle.route(Q, K, x.cu_seqlens, b, G, oracle.TOPK, 3, force_sink=True)
+    co = co.copy()
+    co[0, 1, 3] = 0  # an empty row
+    dO = np.random.default_rng(66).normal(size=Q.shape)
+    dQ, dK, dV = oracle.attention_backward(Q, K, V, x.cu_seqlens, b, G, Jo, co, dO)
+    for i, (s0, n, nb) in enumerate(oracle.seq_info(x.cu_seqlens, b)):
+        for h in range(2):
+            for r in range(nb):
+                dq, _, _ = oracle.attention_backward_row(Q, K, V, x.cu_seqlens, b, G, Jo, co, dO,
+                                                         (i, h, r))
+                q_lo, q_hi = r * b, min(n, (r + 1) * b)
+                assert np.abs(dq - dQ[h * G:(h + 1) * G, s0 + q_lo:s0 + q_hi]).max() < 1e-12
+            for j in range(nb):
+                dk, dv = oracle.attention_backward_key_block(Q, K, V, x.cu_seqlens, b, G, Jo, co,
+                                                             dO, i, h, j)
+                lo, hi = j * b, min(n, (j + 1) * b)
+                assert np.abs(dk - dK[h, s0 + lo:s0 + hi]).max() < 1e-12
+                assert np.abs(dv - dV[h, s0 + lo:s0 + hi]).max() < 1e-12
+
+
 def test_backward_at_density_one_equals_sdpa_gradients():
     x, Q, K, V = _inputs([200, 90], 4, 2, 16, 32, seed=63)
     G, b = 2, 32
