@@ -37,6 +37,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // kind::f16 instruction descriptors: S / dP (A, B K-major, N = 64 keys); dQ
 // (A = dS K-major, B = K MN-major, N = d); dV^T / dK^T (A, B both MN-major).
 constexpr uint32_t kIdescS = idesc_bf16(128, 64, false);
+constexpr uint32_t kIdescS128 = idesc_bf16(128, 128, false);
 constexpr uint32_t kIdescDQ = idesc_bf16(128, kD, true);
 constexpr uint32_t kIdescKV = idesc_bf16(128, 64, true) | (1u << 15);
 
@@ -134,9 +135,14 @@ BSA_DEV uint64_t f2_mul(uint64_t a, uint64_t b) {
 // chains of different columns, which made this routine four times slower).
 // Keys past the query on the diagonal (key0 + column > tok), and invalid rows,
 // get P = dS = 0.
+// WAIT: the dS buffer may still be read by the previous dQ product; wait for its
+// release (bounded) before the first store, after the first 16 columns are computed.
+template <bool WAIT = false>
 BSA_DEV void tile_grad64(uint32_t tS, uint32_t tDP, uint32_t smP, uint32_t smDS, int rho,
                          bool valid, bool diag, int key0, int tok, float scale_log2, float lse2,
-                         float Drow) {
+                         float Drow, uint32_t wbar = 0u, uint32_t wparity = 0u,
+                         volatile int32_t *abort_flag = nullptr, int32_t *status = nullptr,
+                         bool *ok = nullptr) {
   uint32_t sb[2][16], db[2][16];
   const int lim = !valid ? 0 : (diag ? min(64, max(0, tok - key0 + 1)) : 64);  // first masked column
   const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
@@ -163,6 +169,13 @@ BSA_DEV void tile_grad64(uint32_t tS, uint32_t tDP, uint32_t smP, uint32_t smDS,
       pk[e] = pack_bf16x2(p0, p1);
       dk[e] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
     }
+    if (WAIT && c == 0) {
+      *ok = __all_sync(0xffffffffu, mbar_wait(wbar, wparity, abort_flag, status));
+      if (!*ok) {  // leave no TMEM load in flight
+        tmem_wait_ld16x2(sb[1], db[1]);
+        return;
+      }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // 16-byte chunk 2c + h of the 128-byte row
       const uint32_t off = rho * 128 + (((2 * c + h) ^ (rho & 7)) << 4);
@@ -182,6 +195,16 @@ BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
   for (int kk = 0; kk < kD / 16; ++kk)
     mma_ss_lo(d_tmem, xl + ((kk / 4) * 16384 + (kk % 4) * 32) / 16,
               yl + ((kk / 4) * 8192 + (kk % 4) * 32) / 16, kDescHi, kIdescS, kk > 0 ? 1u : 0u);
+}
+
+// S = X Y^T for one 128-row X tile and one 128-row Y tile (two 16 KB panels each),
+// K = d, N = 128.
+BSA_DEV void mma_xyT128(uint32_t d_tmem, uint32_t x, uint32_t y) {
+  const uint32_t xl = desc_lo(x, 16), yl = desc_lo(y, 16);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk)
+    mma_ss_lo(d_tmem, xl + ((kk / 4) * 16384 + (kk % 4) * 32) / 16,
+              yl + ((kk / 4) * 16384 + (kk % 4) * 32) / 16, kDescHi, kIdescS128, kk > 0 ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------- key-major index
@@ -249,32 +272,30 @@ __global__ void kt_emit_kernel(const uint32_t *__restrict__ bits,
 // ---------------------------------------------------------------- dQ pass
 
 // One CTA per (work row, M-tile), one per SM: Q and dO of the tile stay in shared
-// memory; the 64-key tiles of the row's blocks stream through a five-stage K ring
-// and a three-stage V ring (V of step s is free once dP(s) is done, K only after
-// dQ(s), two batches later; both rings keep two batches of loads ahead of the
-// MMAs, which hides the L2 / DRAM latency of a 16 KB tile).  Steps alternate between two halves of the CTA: warpgroup e (warps 4e ..
-// 4e + 3, one query row per thread) and MMA thread e (warp 9 + e) take the steps
-// s = e (mod 2), with S / dP buffer e in TMEM, dS buffer e in shared memory and
-// their own dQ accumulator dQ_e += dS K (fp32 in TMEM); the epilogue adds dQ_0 +
-// dQ_1 in that order, so the result is the same on every call.  The two MMA
-// threads alternate batches (S / dP of step s and dQ of step s - 2) through a
-// two-barrier ping-pong and check every barrier a batch needs before their turn:
-// a barrier check stalls its own thread's MMA issue (about a hundred cycles), so
-// each thread's checks run while the other's batch executes.  352 threads.
+// memory; the row's keys stream in steps of 128 (one 128-key block, or two 64-key
+// blocks side by side; an odd last block is loaded twice and its copy masked)
+// through two-stage K and V rings, so every S / dP product has N = 128 (the N = 64
+// form runs at 58 % of the N = 128 rate per FLOP).  S and dP of a step fill 256 TMEM
+// columns, so they are single-buffered: the MMA thread issues S / dP(s) as soon as
+// the softmax warps have turned S / dP(s - 1) into dS(s - 1), then dQ += dS(s - 1)
+// K(s - 1) (fp32 in TMEM), which runs while the softmax works on step s; the
+// softmax waits for that product to release the dS buffer only before its first
+// store.  Warpgroup g (warps 4 g .. 4 g + 3, one query row per thread) takes the
+// 64 keys 64 g .. 64 g + 63 of every step.  320 threads: warps 0-7 softmax, warp 8
+// TMA, warp 9 MMA.
 namespace dq {
-constexpr int kThreads = 352;
-constexpr int NK = 5, NV = 3;  // K and V ring stages (16 KB each)
-constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NK * 16384;
-constexpr int kOffDS = kOffV + NV * 16384;
-constexpr int kOffBar = kOffDS + 2 * 16384;
-constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK;
-constexpr int B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV;
-constexpr int B_SFREE = B_SFULL + 2, B_DSFULL = B_SFREE + 2, B_DSFREE = B_DSFULL + 2;
-constexpr int B_DQFULL = B_DSFREE + 2;  // one per MMA thread
-constexpr int B_TURN = B_DQFULL + 2;    // MMA thread e's batch is issued
-constexpr int kOffCtl = kOffBar + (B_TURN + 2) * 8;
+constexpr int kThreads = 320;
+constexpr int NR = 2;  // K and V ring stages (32 KB each: 128 keys x d)
+constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NR * 32768;
+constexpr int kOffDS = kOffV + NR * 32768;  // dS: two 16 KB panels (keys 0-63, 64-127)
+constexpr int kOffBar = kOffDS + 32768;
+constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NR, B_VFULL = B_KEMPTY + NR;
+constexpr int B_VEMPTY = B_VFULL + NR, B_SFULL = B_VEMPTY + NR;
+// DSFULL: the softmax has read S / dP of the step and written its dS (8 warps)
+constexpr int B_DSFULL = B_SFULL + 1, B_DSFREE = B_DSFULL + 1, B_DQFULL = B_DSFREE + 1;
+constexpr int kOffCtl = kOffBar + (B_DQFULL + 1) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;  // dQ_e at 256 + 128 e
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace dq
 
@@ -284,7 +305,7 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const BwdTcParams p) {
   using namespace dq;
-  constexpr int KT = BK / 64;  // 64-key tiles per block
+  constexpr int BPS = 128 / BK;  // key blocks per 128-key step
   const int u = blockIdx.x;
   if (u >= __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.mtiles) return;
   extern __shared__ uint8_t smem_raw[];
@@ -297,24 +318,16 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    for (int st = 0; st < NK; ++st) {
+    for (int st = 0; st < NR; ++st) {
       mbar_init(bar(B_KFULL + st), 1);
       mbar_init(bar(B_KEMPTY + st), 1);
-    }
-    for (int st = 0; st < NV; ++st) {
       mbar_init(bar(B_VFULL + st), 1);
       mbar_init(bar(B_VEMPTY + st), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_SFULL + b), 1);
-      mbar_init(bar(B_SFREE + b), 4);
-      mbar_init(bar(B_DSFULL + b), 4);
-      mbar_init(bar(B_DSFREE + b), 1);
-    }
-    for (int e = 0; e < 2; ++e) {
-      mbar_init(bar(B_DQFULL + e), 1);
-      mbar_init(bar(B_TURN + e), 1);
-    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_DSFULL), 8);
+    mbar_init(bar(B_DSFREE), 1);
+    mbar_init(bar(B_DQFULL), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -331,7 +344,8 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int row = __ldg(p.work + u / p.mtiles);
   const int r = row % p.Nq, h = (row / p.Nq) % p.Hk, i = row / (p.Nq * p.Hk);
   const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
-  const int kv0 = __ldg(p.row_ptr + row), nsteps = (__ldg(p.row_ptr + row + 1) - kv0) * KT;
+  const int kv0 = __ldg(p.row_ptr + row), nkv = __ldg(p.row_ptr + row + 1) - kv0;
+  const int nsteps = (nkv + BPS - 1) / BPS;
   const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
                  smV = sbase + kOffV, smDS = sbase + kOffDS;
 
@@ -339,136 +353,122 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int issued_k[NK], issued_v[NV];
-      for (int st = 0; st < NK; ++st) issued_k[st] = -1;
-      for (int st = 0; st < NV; ++st) issued_v[st] = -1;
+      int issued_k[NR], issued_v[NR];
+      for (int st = 0; st < NR; ++st) issued_k[st] = issued_v[st] = -1;
       const int hq0 = h * p.G + (t * 128) / BK;
       mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
       for (int pn = 0; pn < 2; ++pn) {
         tma_load_3d(smQ + pn * 16384, &tmQ, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
         tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
       }
+      // token row of 64-key half hf of step s (a missing second block repeats the first)
+      auto key_row = [&](int s, int hf) {
+        if (BPS == 1) return s0 + checked_index(__ldg(p.col_idx + kv0 + s), 0, r, p.status) * BK + hf * 64;
+        const int e = min(2 * s + hf, nkv - 1);
+        return s0 + checked_index(__ldg(p.col_idx + kv0 + e), 0, r, p.status) * BK;
+      };
       for (int s = 0; s < nsteps; ++s) {
-        const int y =
-            s0 + checked_index(__ldg(p.col_idx + kv0 + s / KT), 0, r, p.status) * BK + (s % KT) * 64;
-        const int sk = s % NK, sv = s % NV;
-        if (s >= NK &&
-            !(ok = mbar_wait(bar(B_KEMPTY + sk), ((s - NK) / NK) & 1, abort_flag, p.status)))
+        const int st = s % NR;
+        const int y0 = key_row(s, 0), y1 = key_row(s, 1);
+        if (s >= NR &&
+            !(ok = mbar_wait(bar(B_KEMPTY + st), ((s - NR) / NR) & 1, abort_flag, p.status)))
           break;
-        mbar_arrive_expect_tx(bar(B_KFULL + sk), 2 * 8192);
-        issued_k[sk] = (s / NK) & 1;
-        for (int pn = 0; pn < 2; ++pn)
-          tma_load_3d(smK + sk * 16384 + pn * 8192, &tmK, bar(B_KFULL + sk), pn * 64, y, h);
-        if (s >= NV &&
-            !(ok = mbar_wait(bar(B_VEMPTY + sv), ((s - NV) / NV) & 1, abort_flag, p.status)))
+        mbar_arrive_expect_tx(bar(B_KFULL + st), 4 * 8192);
+        issued_k[st] = (s / NR) & 1;
+        for (int pn = 0; pn < 2; ++pn) {  // panel pn: d columns 64 pn .. 64 pn + 63, 128 rows
+          tma_load_3d(smK + st * 32768 + pn * 16384, &tmK, bar(B_KFULL + st), pn * 64, y0, h);
+          tma_load_3d(smK + st * 32768 + pn * 16384 + 8192, &tmK, bar(B_KFULL + st), pn * 64, y1, h);
+        }
+        if (s >= NR &&
+            !(ok = mbar_wait(bar(B_VEMPTY + st), ((s - NR) / NR) & 1, abort_flag, p.status)))
           break;
-        mbar_arrive_expect_tx(bar(B_VFULL + sv), 2 * 8192);
-        issued_v[sv] = (s / NV) & 1;
-        for (int pn = 0; pn < 2; ++pn)
-          tma_load_3d(smV + sv * 16384 + pn * 8192, &tmV, bar(B_VFULL + sv), pn * 64, y, h);
+        mbar_arrive_expect_tx(bar(B_VFULL + st), 4 * 8192);
+        issued_v[st] = (s / NR) & 1;
+        for (int pn = 0; pn < 2; ++pn) {
+          tma_load_3d(smV + st * 32768 + pn * 16384, &tmV, bar(B_VFULL + st), pn * 64, y0, h);
+          tma_load_3d(smV + st * 32768 + pn * 16384 + 8192, &tmV, bar(B_VFULL + st), pn * 64, y1, h);
+        }
       }
       // every copy issued lands before the CTA leaves
       mbar_wait_drain(bar(B_QFULL), 0);
-      for (int st = 0; st < NK; ++st)
+      for (int st = 0; st < NR; ++st) {
         if (issued_k[st] >= 0) mbar_wait_drain(bar(B_KFULL + st), issued_k[st]);
-      for (int st = 0; st < NV; ++st)
         if (issued_v[st] >= 0) mbar_wait_drain(bar(B_VFULL + st), issued_v[st]);
+      }
       (void)ok;
     }
-  } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------------------ MMA threads
-    const int e = warp - 9;  // this thread's steps: s = e (mod 2)
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
-      auto dq_product = [&](int s) {  // dQ_e += dS(s) K(s): 64 keys in steps of 16
-        const uint32_t al = desc_lo(smDS + e * 16384, 16);
-        const uint32_t bl = desc_lo(smK + (s % NK) * 16384, 8192);
+      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 128 keys in steps of 16
+        const uint32_t al = desc_lo(smDS, 16);
+        const uint32_t bl = desc_lo(smK + (s % NR) * 32768, 16384);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss_lo(tmem + kColDQ + 128 * e, al + kk * 2, bl + kk * 128, kDescHi, kIdescDQ,
-                    (s >= 2 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_KEMPTY + s % NK));
-        mma_commit(bar(B_DSFREE + e));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_lo(tmem + kColDQ, al + (kk / 4) * (16384 / 16) + (kk % 4) * 2, bl + kk * 128,
+                    kDescHi, kIdescDQ, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_KEMPTY + s % NR));
+        mma_commit(bar(B_DSFREE));
       };
-      // Both threads run ceil(nsteps / 2) + 1 batches (thread 1 may have empty ones):
-      // batch k is S / dP of step 2k + e and dQ of step 2k + e - 2, each if present.
-      const int nbatch = (nsteps + 1) / 2 + 1;
-      for (int k = 0; ok && k < nbatch; ++k) {
-        const int s = 2 * k + e, sp = s - 2;
-        const bool has_s = s < nsteps, has_prev = sp >= 0 && sp < nsteps;
-        if (has_s) {
-          if (!(ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status)) ||
-              !(ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status)))
-            break;
-          if (s >= 2 &&
-              !(ok = mbar_wait(bar(B_SFREE + e), ((s - 2) >> 1) & 1, abort_flag, p.status)))
-            break;
-        }
-        if (has_prev &&
-            !(ok = mbar_wait(bar(B_DSFULL + e), (sp >> 1) & 1, abort_flag, p.status)))
+      for (int s = 0; ok && s < nsteps; ++s) {
+        const int st = s % NR;
+        if (!(ok = mbar_wait(bar(B_KFULL + st), (s / NR) & 1, abort_flag, p.status)) ||
+            !(ok = mbar_wait(bar(B_VFULL + st), (s / NR) & 1, abort_flag, p.status)))
           break;
-        // thread 0's batch k follows thread 1's batch k - 1, thread 1's batch k thread 0's
-        if (!(e == 0 && k == 0) &&
-            !(ok = mbar_wait(bar(B_TURN + (1 - e)), (e == 0 ? k - 1 : k) & 1, abort_flag,
-                             p.status)))
-          break;
+        // S / dP(s - 1) read and dS(s - 1) written (the single S / dP buffer is free)
+        if (s >= 1 && !(ok = mbar_wait(bar(B_DSFULL), (s - 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        if (has_s) {
-          mma_xyT(tmem + kColS + 64 * e, smQ, smK + (s % NK) * 16384);
-          mma_xyT(tmem + kColDP + 64 * e, smDO, smV + (s % NV) * 16384);
-          mma_commit(bar(B_SFULL + e));
-          mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
-        }
-        if (has_prev) dq_product(sp);
-        mbar_arrive(bar(B_TURN + e));
+        mma_xyT128(tmem + kColS, smQ, smK + st * 32768);
+        mma_xyT128(tmem + kColDP, smDO, smV + st * 32768);
+        mma_commit(bar(B_SFULL));
+        mma_commit(bar(B_VEMPTY + st));  // V(s) has no other reader
+        if (s >= 1) dq_product(s - 1);
       }
-      mma_commit(bar(B_DQFULL + e));
-      mbar_wait_drain(bar(B_DQFULL + e), 0);  // MMAs done before TMEM is freed
+      if (ok && nsteps > 0 &&
+          (ok = mbar_wait(bar(B_DSFULL), (nsteps - 1) & 1, abort_flag, p.status))) {
+        tc_fence_after();
+        dq_product(nsteps - 1);
+      }
+      mma_commit(bar(B_DQFULL));
+      mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int g = warp / 4, wq = warp % 4;  // warpgroup g takes the steps s = g (mod 2)
+    const int g = warp / 4, wq = warp % 4;  // warpgroup g: keys 64 g .. 64 g + 63 of a step
     const int rho = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
     const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
     const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
     bool ok = true;
-    int j_next = g < nsteps ? __ldg(p.col_idx + kv0 + g / KT) : 0;
-    for (int s = g; s < nsteps; s += 2) {
-      const int b = s & 1;
-      const bool diag = j_next == r;
-      if (s + 2 < nsteps) j_next = __ldg(p.col_idx + kv0 + (s + 2) / KT);
-      if (!(ok = mbar_wait(bar(B_SFULL + b), (s >> 1) & 1, abort_flag, p.status))) break;
-      if (s >= 2 && !(ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
-        break;
+    for (int s = 0; s < nsteps; ++s) {
+      // this warpgroup's 64 keys: half g of the step's 128-key block, or its 64-key
+      // block (absent past the row's last block)
+      const int e = BPS == 1 ? s : 2 * s + g;
+      const bool present = e < nkv;
+      const int j = present ? __ldg(p.col_idx + kv0 + e) : -1;
+      const int key0 = BPS == 1 ? 64 * g : 0;
+      if (!(ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      tile_grad64(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b, 0u,
-                  smDS + b * 16384, rho, q.valid, diag, (s % KT) * 64, q.tok, p.scale_log2, lse2,
-                  Drow);
+      tile_grad64<true>(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g, 0u,
+                        smDS + g * 16384, rho, q.valid && present, j == r, key0, q.tok,
+                        p.scale_log2, lse2, Drow, bar(B_DSFREE), (s - 1) & 1, abort_flag, p.status,
+                        &ok);
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_SFREE + b));
-        mbar_arrive(bar(B_DSFULL + b));
-      }
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
     }
-    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ =
-    // dQ_0 + dQ_1 (dQ_1 holds the odd steps; there are none when nsteps == 1)
-    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status) &&
-        mbar_wait(bar(B_DQFULL + 1), 0, abort_flag, p.status)) {
+    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
+    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
       tc_fence_after();
       uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32], r1[32];
+        uint32_t rr[32];
         tmem_ld32(tmem + lane_base + kColDQ + 64 * g + c0, rr);
-        tmem_ld32(tmem + lane_base + kColDQ + 128 + 64 * g + c0, r1);
-        if (nsteps >= 2)
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            rr[c] = __float_as_uint(__uint_as_float(rr[c]) + __uint_as_float(r1[c]));
         uint32_t o[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
