@@ -197,6 +197,71 @@ BSA_DEV void mma_xyT(uint32_t d_tmem, uint32_t x, uint32_t y) {
               yl + ((kk / 4) * 8192 + (kk % 4) * 32) / 16, kDescHi, kIdescS, kk > 0 ? 1u : 0u);
 }
 
+// D += A B with A (bf16 pairs, row = lane) read from tensor memory.
+BSA_DEV void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi)
+      : "memory");
+}
+
+// 8 TMEM columns of this thread's lane, not waited.
+BSA_DEV void tmem_st8_nowait(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+               "r"(r[7])
+               : "memory");
+}
+
+// dS of the 64 keys of one TMEM S / dP tile row written back to tensor memory as
+// bf16 pairs (32 columns at tDS, key 2 c and 2 c + 1 in column c: the layout of a
+// tensor-memory A operand), 16 columns at a time as tile_grad64 does.  Once the
+// last S / dP columns are loaded the warp arrives on `sread` (the S / dP buffer may
+// then be overwritten); the stores are waited before returning.
+BSA_DEV void tile_grad64_tmem(uint32_t tS, uint32_t tDP, uint32_t tDS, bool valid, bool diag,
+                              int key0, int tok, float scale_log2, float lse2, float Drow,
+                              uint32_t sread) {
+  uint32_t sb[2][16], db[2][16];
+  const int lim = !valid ? 0 : (diag ? min(64, max(0, tok - key0 + 1)) : 64);  // first masked column
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
+  const uint64_t nd2 = f2_pack(-Drow, -Drow);
+  tmem_ld16_async(tS, sb[0]);
+  tmem_ld16_async(tDP, db[0]);
+  tmem_wait_ld16x2(sb[0], db[0]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (c < 3) {
+      tmem_ld16_async(tS + 16 * (c + 1), sb[(c + 1) & 1]);
+      tmem_ld16_async(tDP + 16 * (c + 1), db[(c + 1) & 1]);
+    }
+    const uint32_t(&sv)[16] = sb[c & 1];
+    const uint32_t(&dv)[16] = db[c & 1];
+    uint32_t dk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int col = 16 * c + 2 * e;
+      const uint64_t z = f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sc2, nl2);
+      const float p0 = col < lim ? fast_exp2(f2_lo(z)) : 0.f;
+      const float p1 = col + 1 < lim ? fast_exp2(f2_hi(z)) : 0.f;
+      const uint64_t ds = f2_mul(f2_pack(p0, p1), f2_add(f2_pack(dv[2 * e], dv[2 * e + 1]), nd2));
+      dk[e] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+    }
+    tmem_st8_nowait(tDS + 8 * c, dk);
+    if (c < 3) tmem_wait_ld16x2(sb[(c + 1) & 1], db[(c + 1) & 1]);
+    if (c == 2) {  // every S / dP column of this warp is in registers
+      tc_fence_before();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(sread);
+    }
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // S = X Y^T for one 128-row X tile and one 128-row Y tile (two 16 KB panels each),
 // K = d, N = 128.
 BSA_DEV void mma_xyT128(uint32_t d_tmem, uint32_t x, uint32_t y) {
@@ -274,28 +339,30 @@ __global__ void kt_emit_kernel(const uint32_t *__restrict__ bits,
 // One CTA per (work row, M-tile), one per SM: Q and dO of the tile stay in shared
 // memory; the row's keys stream in steps of 128 (one 128-key block, or two 64-key
 // blocks side by side; an odd last block is loaded twice and its copy masked)
-// through two-stage K and V rings, so every S / dP product has N = 128 (the N = 64
-// form runs at 58 % of the N = 128 rate per FLOP).  S and dP of a step fill 256 TMEM
-// columns, so they are single-buffered: the MMA thread issues S / dP(s) as soon as
-// the softmax warps have turned S / dP(s - 1) into dS(s - 1), then dQ += dS(s - 1)
-// K(s - 1) (fp32 in TMEM), which runs while the softmax works on step s; the
-// softmax waits for that product to release the dS buffer only before its first
-// store.  Warpgroup g (warps 4 g .. 4 g + 3, one query row per thread) takes the
-// 64 keys 64 g .. 64 g + 63 of every step.  320 threads: warps 0-7 softmax, warp 8
-// TMA, warp 9 MMA.
+// through a three-stage K ring and a two-stage V ring, so every S / dP product has
+// N = 128 (the N = 64 form runs at 58 % of the N = 128 rate per FLOP).  TMEM holds
+// S and dP of one step (256 columns, single-buffered), the dQ accumulator (128) and
+// two dS buffers (64 each): the softmax warps write dS back to tensor memory as
+// bf16 pairs and dQ += dS K reads it as the A operand, so no shared-memory dS
+// buffer has to be released before the next step's dS is written.  The MMA thread
+// issues S / dP(s) as soon as the softmax warps have loaded S / dP(s - 1) (before
+// they finish dS(s - 1)), then dQ += dS(s - 1) K(s - 1).  Warpgroup g (warps 4 g ..
+// 4 g + 3, one query row per thread) takes the 64 keys 64 g .. 64 g + 63 of every
+// step.  320 threads: warps 0-7 softmax, warp 8 TMA, warp 9 MMA.
 namespace dq {
 constexpr int kThreads = 320;
-constexpr int NR = 2;  // K and V ring stages (32 KB each: 128 keys x d)
-constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NR * 32768;
-constexpr int kOffDS = kOffV + NR * 32768;  // dS: two 16 KB panels (keys 0-63, 64-127)
-constexpr int kOffBar = kOffDS + 32768;
-constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NR, B_VFULL = B_KEMPTY + NR;
-constexpr int B_VEMPTY = B_VFULL + NR, B_SFULL = B_VEMPTY + NR;
-// DSFULL: the softmax has read S / dP of the step and written its dS (8 warps)
-constexpr int B_DSFULL = B_SFULL + 1, B_DSFREE = B_DSFULL + 1, B_DQFULL = B_DSFREE + 1;
+constexpr int NK = 3, NV = 2;  // K and V ring stages (32 KB each: 128 keys x d)
+constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NK * 32768;
+constexpr int kOffBar = kOffV + NV * 32768;
+constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK;
+constexpr int B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV;
+// SREAD: the softmax has loaded S / dP of the step (8 warps); DSFULL / DSFREE per
+// dS buffer
+constexpr int B_SREAD = B_SFULL + 1, B_DSFULL = B_SREAD + 1, B_DSFREE = B_DSFULL + 2;
+constexpr int B_DQFULL = B_DSFREE + 2;
 constexpr int kOffCtl = kOffBar + (B_DQFULL + 1) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384, kTmemCols = 512;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace dq
 
@@ -318,15 +385,20 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    for (int st = 0; st < NR; ++st) {
+    for (int st = 0; st < NK; ++st) {
       mbar_init(bar(B_KFULL + st), 1);
       mbar_init(bar(B_KEMPTY + st), 1);
+    }
+    for (int st = 0; st < NV; ++st) {
       mbar_init(bar(B_VFULL + st), 1);
       mbar_init(bar(B_VEMPTY + st), 1);
     }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_DSFULL), 8);
-    mbar_init(bar(B_DSFREE), 1);
+    mbar_init(bar(B_SREAD), 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_DSFULL + b), 8);
+      mbar_init(bar(B_DSFREE + b), 1);
+    }
     mbar_init(bar(B_DQFULL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -347,14 +419,15 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int kv0 = __ldg(p.row_ptr + row), nkv = __ldg(p.row_ptr + row + 1) - kv0;
   const int nsteps = (nkv + BPS - 1) / BPS;
   const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
-                 smV = sbase + kOffV, smDS = sbase + kOffDS;
+                 smV = sbase + kOffV;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int issued_k[NR], issued_v[NR];
-      for (int st = 0; st < NR; ++st) issued_k[st] = issued_v[st] = -1;
+      int issued_k[NK], issued_v[NV];
+      for (int st = 0; st < NK; ++st) issued_k[st] = -1;
+      for (int st = 0; st < NV; ++st) issued_v[st] = -1;
       const int hq0 = h * p.G + (t * 128) / BK;
       mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
       for (int pn = 0; pn < 2; ++pn) {
@@ -368,67 +441,74 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
         return s0 + checked_index(__ldg(p.col_idx + kv0 + e), 0, r, p.status) * BK;
       };
       for (int s = 0; s < nsteps; ++s) {
-        const int st = s % NR;
+        const int sk = s % NK, sv = s % NV;
         const int y0 = key_row(s, 0), y1 = key_row(s, 1);
-        if (s >= NR &&
-            !(ok = mbar_wait(bar(B_KEMPTY + st), ((s - NR) / NR) & 1, abort_flag, p.status)))
+        if (s >= NK &&
+            !(ok = mbar_wait(bar(B_KEMPTY + sk), ((s - NK) / NK) & 1, abort_flag, p.status)))
           break;
-        mbar_arrive_expect_tx(bar(B_KFULL + st), 4 * 8192);
-        issued_k[st] = (s / NR) & 1;
+        mbar_arrive_expect_tx(bar(B_KFULL + sk), 4 * 8192);
+        issued_k[sk] = (s / NK) & 1;
         for (int pn = 0; pn < 2; ++pn) {  // panel pn: d columns 64 pn .. 64 pn + 63, 128 rows
-          tma_load_3d(smK + st * 32768 + pn * 16384, &tmK, bar(B_KFULL + st), pn * 64, y0, h);
-          tma_load_3d(smK + st * 32768 + pn * 16384 + 8192, &tmK, bar(B_KFULL + st), pn * 64, y1, h);
+          tma_load_3d(smK + sk * 32768 + pn * 16384, &tmK, bar(B_KFULL + sk), pn * 64, y0, h);
+          tma_load_3d(smK + sk * 32768 + pn * 16384 + 8192, &tmK, bar(B_KFULL + sk), pn * 64, y1, h);
         }
-        if (s >= NR &&
-            !(ok = mbar_wait(bar(B_VEMPTY + st), ((s - NR) / NR) & 1, abort_flag, p.status)))
+        if (s >= NV &&
+            !(ok = mbar_wait(bar(B_VEMPTY + sv), ((s - NV) / NV) & 1, abort_flag, p.status)))
           break;
-        mbar_arrive_expect_tx(bar(B_VFULL + st), 4 * 8192);
-        issued_v[st] = (s / NR) & 1;
+        mbar_arrive_expect_tx(bar(B_VFULL + sv), 4 * 8192);
+        issued_v[sv] = (s / NV) & 1;
         for (int pn = 0; pn < 2; ++pn) {
-          tma_load_3d(smV + st * 32768 + pn * 16384, &tmV, bar(B_VFULL + st), pn * 64, y0, h);
-          tma_load_3d(smV + st * 32768 + pn * 16384 + 8192, &tmV, bar(B_VFULL + st), pn * 64, y1, h);
+          tma_load_3d(smV + sv * 32768 + pn * 16384, &tmV, bar(B_VFULL + sv), pn * 64, y0, h);
+          tma_load_3d(smV + sv * 32768 + pn * 16384 + 8192, &tmV, bar(B_VFULL + sv), pn * 64, y1, h);
         }
       }
       // every copy issued lands before the CTA leaves
       mbar_wait_drain(bar(B_QFULL), 0);
-      for (int st = 0; st < NR; ++st) {
+      for (int st = 0; st < NK; ++st)
         if (issued_k[st] >= 0) mbar_wait_drain(bar(B_KFULL + st), issued_k[st]);
+      for (int st = 0; st < NV; ++st)
         if (issued_v[st] >= 0) mbar_wait_drain(bar(B_VFULL + st), issued_v[st]);
-      }
       (void)ok;
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
-      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 128 keys in steps of 16
-        const uint32_t al = desc_lo(smDS, 16);
-        const uint32_t bl = desc_lo(smK + (s % NR) * 32768, 16384);
+      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 128 keys in steps of 16, dS from TMEM
+        const int b = s & 1;
+        const uint32_t bl = desc_lo(smK + (s % NK) * 32768, 16384);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss_lo(tmem + kColDQ, al + (kk / 4) * (16384 / 16) + (kk % 4) * 2, bl + kk * 128,
-                    kDescHi, kIdescDQ, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_KEMPTY + s % NR));
-        mma_commit(bar(B_DSFREE));
+          mma_ts_lo(tmem + kColDQ, tmem + kColDS + 64 * b + 8 * kk, bl + kk * 128, kDescHi,
+                    kIdescDQ, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_KEMPTY + s % NK));
+        mma_commit(bar(B_DSFREE + b));
       };
       for (int s = 0; ok && s < nsteps; ++s) {
-        const int st = s % NR;
-        if (!(ok = mbar_wait(bar(B_KFULL + st), (s / NR) & 1, abort_flag, p.status)) ||
-            !(ok = mbar_wait(bar(B_VFULL + st), (s / NR) & 1, abort_flag, p.status)))
+        if (!(ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status)) ||
+            !(ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status)))
           break;
-        // S / dP(s - 1) read and dS(s - 1) written (the single S / dP buffer is free)
-        if (s >= 1 && !(ok = mbar_wait(bar(B_DSFULL), (s - 1) & 1, abort_flag, p.status))) break;
+        // S / dP(s - 1) loaded by the softmax: the single S / dP buffer is free
+        if (s >= 1 && !(ok = mbar_wait(bar(B_SREAD), (s - 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        mma_xyT128(tmem + kColS, smQ, smK + st * 32768);
-        mma_xyT128(tmem + kColDP, smDO, smV + st * 32768);
+        mma_xyT128(tmem + kColS, smQ, smK + (s % NK) * 32768);
+        mma_xyT128(tmem + kColDP, smDO, smV + (s % NV) * 32768);
         mma_commit(bar(B_SFULL));
-        mma_commit(bar(B_VEMPTY + st));  // V(s) has no other reader
-        if (s >= 1) dq_product(s - 1);
+        mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
+        if (s >= 1) {
+          const int sp = s - 1;
+          if (!(ok = mbar_wait(bar(B_DSFULL + (sp & 1)), (sp >> 1) & 1, abort_flag, p.status)))
+            break;
+          tc_fence_after();
+          dq_product(sp);
+        }
       }
-      if (ok && nsteps > 0 &&
-          (ok = mbar_wait(bar(B_DSFULL), (nsteps - 1) & 1, abort_flag, p.status))) {
-        tc_fence_after();
-        dq_product(nsteps - 1);
+      if (ok && nsteps > 0) {
+        const int sp = nsteps - 1;
+        if ((ok = mbar_wait(bar(B_DSFULL + (sp & 1)), (sp >> 1) & 1, abort_flag, p.status))) {
+          tc_fence_after();
+          dq_product(sp);
+        }
       }
       mma_commit(bar(B_DQFULL));
       mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
@@ -443,6 +523,7 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
+      const int b = s & 1;
       // this warpgroup's 64 keys: half g of the step's 128-key block, or its 64-key
       // block (absent past the row's last block)
       const int e = BPS == 1 ? s : 2 * s + g;
@@ -450,16 +531,16 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       const int j = present ? __ldg(p.col_idx + kv0 + e) : -1;
       const int key0 = BPS == 1 ? 64 * g : 0;
       if (!(ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status))) break;
+      // dS buffer b was read by dQ(s - 2) (issued one step ago)
+      if (s >= 2 && !(ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
+        break;
       tc_fence_after();
-      tile_grad64<true>(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g, 0u,
-                        smDS + g * 16384, rho, q.valid && present, j == r, key0, q.tok,
-                        p.scale_log2, lse2, Drow, bar(B_DSFREE), (s - 1) & 1, abort_flag, p.status,
-                        &ok);
-      if (!ok) break;
-      fence_proxy_async_smem();
+      tile_grad64_tmem(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g,
+                       tmem + lane_base + kColDS + 64 * b + 32 * g, q.valid && present, j == r,
+                       key0, q.tok, p.scale_log2, lse2, Drow, bar(B_SREAD));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+      if (lane == 0) mbar_arrive(bar(B_DSFULL + b));
     }
     // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
     if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
