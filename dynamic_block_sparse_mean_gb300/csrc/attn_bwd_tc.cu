@@ -824,6 +824,265 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
   }
 }
 
+// ---------------------------------------------------------------- dK / dV pass, 128-key blocks
+
+// b = 128: one CTA per key block with its 128 keys on the TMEM lanes (M = 128), so
+// P and dS never leave tensor memory: S^T = K Q^T and dP^T = V dO^T (N = 64 query
+// rows of one head and half a query block per tile), the softmax warps turn them
+// into P^T and dS^T (bf16 pairs written over the S^T / dP^T columns they read:
+// the A operand layout), and dV += P^T dO, dK += dS^T Q run as TS products with
+// N = d.  Shared memory holds K, V and a four-stage ring of Q / dO tiles (no P / dS
+// buffers).  Per key lane, the query columns a tile may use are [lo, hi): the
+// causal triangle on the diagonal block (key <= query), the sequence end, and keys
+// past the sequence end use none.  The query-row statistics (lse, D) of a tile are
+// staged per warp in shared memory and read as broadcasts.  320 threads: two
+// softmax warpgroups on alternate tiles (warpgroup 0 writes dV, 1 dK at the end),
+// warp 8 TMA, warp 9 MMA.
+namespace kv128 {
+constexpr int kThreads = 320;
+constexpr int NQ = 4;  // Q / dO stages (Q 16 KB | dO 16 KB)
+constexpr int kOffK = 0, kOffV = 32768, kOffQ = 65536;
+constexpr int kStage = 32768;
+constexpr int kOffStat = kOffQ + NQ * kStage;  // per softmax warp: lse2[64] | D[64]
+constexpr int kOffBar = kOffStat + 8 * 512;
+constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + NQ, B_SFULL = B_QEMPTY + NQ;
+constexpr int B_PDS = B_SFULL + 2, B_DONE = B_PDS + 2;
+constexpr int kOffCtl = kOffBar + (B_DONE + 1) * 8;
+constexpr int kSmemBytes = kOffCtl + 16 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384, kTmemCols = 512;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+}  // namespace kv128
+
+// P^T and dS^T of one 64-column S^T / dP^T tile row (this key lane, 64 query columns)
+// written back over the columns read (chunk c -> columns 8 c .. 8 c + 7), 16 columns
+// at a time with the next chunk's loads in flight.  Columns outside [lo, hi) get
+// P = dS = 0; st = this warp's staged lse2 / D.
+BSA_DEV void tile_grad64_t(uint32_t tS, uint32_t tDP, const float *st, int lo, int hi,
+                           float scale_log2) {
+  uint32_t sb[2][16], db[2][16];
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+  tmem_ld16_async(tS, sb[0]);
+  tmem_ld16_async(tDP, db[0]);
+  tmem_wait_ld16x2(sb[0], db[0]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (c < 3) {
+      tmem_ld16_async(tS + 16 * (c + 1), sb[(c + 1) & 1]);
+      tmem_ld16_async(tDP + 16 * (c + 1), db[(c + 1) & 1]);
+    }
+    const uint32_t(&sv)[16] = sb[c & 1];
+    const uint32_t(&dv)[16] = db[c & 1];
+    uint32_t pk[8], dk[8];
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4) {  // four columns: two packed pairs
+      const float4 l4 = *reinterpret_cast<const float4 *>(st + 16 * c + 4 * e4);
+      const float4 d4 = *reinterpret_cast<const float4 *>(st + 64 + 16 * c + 4 * e4);
+#pragma unroll
+      for (int hp = 0; hp < 2; ++hp) {
+        const int e = 2 * e4 + hp, col = 16 * c + 2 * e;
+        const float la = hp ? l4.z : l4.x, lb = hp ? l4.w : l4.y;
+        const float da = hp ? d4.z : d4.x, db_ = hp ? d4.w : d4.y;
+        const uint64_t z = f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), sc2, f2_pack(-la, -lb));
+        const float p0 = col >= lo && col < hi ? fast_exp2(f2_lo(z)) : 0.f;
+        const float p1 = col + 1 >= lo && col + 1 < hi ? fast_exp2(f2_hi(z)) : 0.f;
+        const uint64_t ds =
+            f2_mul(f2_pack(p0, p1), f2_add(f2_pack(dv[2 * e], dv[2 * e + 1]), f2_pack(-da, -db_)));
+        pk[e] = pack_bf16x2(p0, p1);
+        dk[e] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+      }
+    }
+    tmem_st8_nowait(tS + 8 * c, pk);
+    tmem_st8_nowait(tDP + 8 * c, dk);
+    if (c < 3) tmem_wait_ld16x2(sb[(c + 1) & 1], db[(c + 1) & 1]);
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    const BwdTcParams p) {
+  using namespace kv128;
+  constexpr int BK = 128;
+  const int u = blockIdx.x;
+  if (u >= __ldg(p.kt_bucket + BSA_NUM_BUCKETS)) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (sbase - raw);
+  auto bar = [&](int k) { return sbase + kOffBar + 8u * (uint32_t)k; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffCtl);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + kOffCtl + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_KVFULL), 1);
+    for (int st = 0; st < NQ; ++st) {
+      mbar_init(bar(B_QFULL + st), 1);
+      mbar_init(bar(B_QEMPTY + st), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_PDS + b), 4);
+    }
+    mbar_init(bar(B_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int kb = __ldg(p.kt_work + u);  // (i * H_kv + h) * N_q + j
+  const int j = kb % p.Nq, h = (kb / p.Nq) % p.Hk, i = kb / (p.Nq * p.Hk);
+  const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
+  const int tpr = 2 * p.G;  // 64-row query tiles per selecting row: G heads x 2 halves
+  const int l0 = __ldg(p.kt_ptr + kb), ntiles = (__ldg(p.kt_ptr + kb + 1) - l0) * tpr;
+  const uint32_t smK = sbase + kOffK, smV = sbase + kOffV, smQ = sbase + kOffQ;
+  auto row_of = [&](int nt) { return __ldg(p.kt_rows + l0 + nt / tpr); };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      int issued[NQ];
+      for (int st = 0; st < NQ; ++st) issued[st] = -1;
+      mbar_arrive_expect_tx(bar(B_KVFULL), 8 * 8192);
+      for (int pn = 0; pn < 2; ++pn)
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(smK + pn * 16384 + hf * 8192, &tmK, bar(B_KVFULL), pn * 64,
+                      s0 + j * BK + hf * 64, h);
+          tma_load_3d(smV + pn * 16384 + hf * 8192, &tmV, bar(B_KVFULL), pn * 64,
+                      s0 + j * BK + hf * 64, h);
+        }
+      for (int nt = 0; nt < ntiles; ++nt) {
+        const int st = nt % NQ;
+        if (nt >= NQ &&
+            !(ok = mbar_wait(bar(B_QEMPTY + st), ((nt - NQ) / NQ) & 1, abort_flag, p.status)))
+          break;
+        const int r = row_of(nt), tt = nt % tpr;
+        const int y = s0 + r * BK + 64 * (tt & 1), hq = h * p.G + (tt >> 1);
+        mbar_arrive_expect_tx(bar(B_QFULL + st), 4 * 8192);
+        issued[st] = (nt / NQ) & 1;
+        for (int pn = 0; pn < 2; ++pn) {  // Q | dO, each two 8 KB panels of 64 rows
+          tma_load_3d(smQ + st * kStage + pn * 8192, &tmQ, bar(B_QFULL + st), pn * 64, y, hq);
+          tma_load_3d(smQ + st * kStage + 16384 + pn * 8192, &tmDO, bar(B_QFULL + st), pn * 64,
+                      y, hq);
+        }
+      }
+      mbar_wait_drain(bar(B_KVFULL), 0);
+      for (int st = 0; st < NQ; ++st)
+        if (issued[st] >= 0) mbar_wait_drain(bar(B_QFULL + st), issued[st]);
+      (void)ok;
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
+      // dV += P^T dO, dK += dS^T Q of tile nt (64 query rows in steps of 16)
+      auto kv_products = [&](int nt) {
+        const int b = nt & 1, st = nt % NQ;
+        const uint32_t ql = desc_lo(smQ + st * kStage, 8192);
+        const uint32_t dol = desc_lo(smQ + st * kStage + 16384, 8192);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts_lo(tmem + kColDV, tmem + kColS + 64 * b + 8 * kk, dol + kk * 128, kDescHi,
+                    kIdescDQ, (nt > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts_lo(tmem + kColDK, tmem + kColDP + 64 * b + 8 * kk, ql + kk * 128, kDescHi,
+                    kIdescDQ, (nt > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_QEMPTY + st));
+      };
+      for (int nt = 0; ok && nt < ntiles; ++nt) {
+        const int b = nt & 1, st = nt % NQ;
+        if (!(ok = mbar_wait(bar(B_QFULL + st), (nt / NQ) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // buffer b was last read by kv_products(nt - 2), issued before this by this thread
+        mma_xyT(tmem + kColS + 64 * b, smK, smQ + st * kStage);
+        mma_xyT(tmem + kColDP + 64 * b, smV, smQ + st * kStage + 16384);
+        mma_commit(bar(B_SFULL + b));
+        if (nt >= 1) {
+          if (!(ok = mbar_wait(bar(B_PDS + (b ^ 1)), ((nt - 1) >> 1) & 1, abort_flag, p.status)))
+            break;
+          tc_fence_after();
+          kv_products(nt - 1);
+        }
+      }
+      if (ok && ntiles > 0 &&
+          (ok = mbar_wait(bar(B_PDS + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, abort_flag,
+                          p.status))) {
+        tc_fence_after();
+        kv_products(ntiles - 1);
+      }
+      mma_commit(bar(B_DONE));
+      mbar_wait_drain(bar(B_DONE), 0);  // MMAs done before TMEM is freed
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int g = warp / 4, wq = warp % 4;  // warpgroup g takes the tiles nt = g (mod 2)
+    const int kin = wq * 32 + lane;         // this lane's key within the block
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const bool key_ok = j * BK + kin < n;
+    float *stat = reinterpret_cast<float *>(sm + kOffStat) + warp * 128;
+    bool ok = true;
+    for (int nt = g; nt < ntiles; nt += 2) {
+      const int b = nt & 1;
+      const int r = row_of(nt), tt = nt % tpr;
+      const int qtok0 = 64 * (tt & 1);                  // first query of the tile in block r
+      const size_t q0 = (size_t)(h * p.G + (tt >> 1)) * p.T + s0 + r * BK + qtok0;
+      const int nq = min(64, n - (r * BK + qtok0));     // valid query columns
+      // stage this tile's lse2 / D (columns past the sequence end read as 0)
+      for (int c = lane; c < 64; c += 32) {
+        stat[c] = c < nq ? __ldg(p.lse + q0 + c) * kLog2e : 0.f;
+        stat[64 + c] = c < nq ? __ldg(p.Dv + q0 + c) : 0.f;
+      }
+      __syncwarp();
+      const int lo = (j == r) ? max(0, kin - qtok0) : 0;  // causal: key <= query
+      const int hi = key_ok ? nq : 0;
+      if (!(ok = mbar_wait(bar(B_SFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      tile_grad64_t(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b, stat, lo,
+                    hi, p.scale_log2);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PDS + b));
+    }
+    // epilogue: TMEM lane = key, 128 columns = d; warpgroup 0 writes dV, 1 dK
+    if (ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status)) {
+      tc_fence_after();
+      uint16_t *out = g == 0 ? p.dV : p.dK;
+      const float mul = g == 0 ? 1.f : p.scale;
+      const uint32_t col = g == 0 ? kColDV : kColDK;
+      uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)h * p.T + s0 + j * BK + kin) * kD);
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + col + c0, rr);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          o[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * mul, __uint_as_float(rr[2 * e + 1]) * mul);
+        if (key_ok)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[c0 / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 template <int BK>
@@ -838,16 +1097,31 @@ cudaError_t launch_bk(const bsa_shape_t &s, const void *Q, const void *K, const 
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel<BK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kv::kSmemBytes);
+  if constexpr (BK == 64) {
+    e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kv::kSmemBytes);
+  } else {
+    e = cudaFuncSetAttribute(bwd_dkdv128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kv128::kSmemBytes);
+  }
   if (e != cudaSuccess) return e;
   const long long rows = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks;
   bwd_dq_tc_kernel<BK><<<(unsigned)(rows * p.mtiles), dq::kThreads, dq::kSmemBytes, st>>>(
       mq, mdo, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dkdv_tc_kernel<BK><<<(unsigned)(rows * (BK / 64)), kv::kThreads, kv::kSmemBytes, st>>>(
-      mq, mdo, mk, mv, p);
+  if constexpr (BK == 64) {
+    bwd_dkdv_tc_kernel<BK><<<(unsigned)rows, kv::kThreads, kv::kSmemBytes, st>>>(mq, mdo, mk, mv,
+                                                                                 p);
+  } else {
+    // query tiles of 64 rows of one head: their own tensor maps
+    CUtensorMap mq64, mdo64;
+    if (!make_tmap_3d_bf16(&mq64, Q, kD, s.total_tokens, s.num_heads, 64, 64, 1) ||
+        !make_tmap_3d_bf16(&mdo64, dO, kD, s.total_tokens, s.num_heads, 64, 64, 1))
+      return cudaErrorInvalidValue;
+    bwd_dkdv128_kernel<<<(unsigned)rows, kv128::kThreads, kv128::kSmemBytes, st>>>(mq64, mdo64, mk,
+                                                                                 mv, p);
+  }
   return cudaGetLastError();
 }
 
