@@ -832,21 +832,26 @@ __global__ void __launch_bounds__(kv::kThreads, 1) bwd_dkdv_tc_kernel(
 // into P^T and dS^T (bf16 pairs written over the S^T / dP^T columns they read:
 // the A operand layout), and dV += P^T dO, dK += dS^T Q run as TS products with
 // N = d.  Shared memory holds K, V and a four-stage ring of Q / dO tiles (no P / dS
-// buffers).  Per key lane, the query columns a tile may use are [lo, hi): the
+// buffers).  The MMA warp hears from the softmax warps and of landed copies through
+// named barriers: an mbarrier check costs it a few hundred cycles while the MMAs
+// stream operands from shared memory, and the MMA queue runs dry meanwhile.  Per key lane, the query columns a tile may use are [lo, hi): the
 // causal triangle on the diagonal block (key <= query), the sequence end, and keys
 // past the sequence end use none.  The query-row statistics (lse, D) of a tile are
-// staged per warp in shared memory and read as broadcasts.  320 threads: two
+// staged per warp in shared memory and read as broadcasts.  352 threads: two
 // softmax warpgroups on alternate tiles (warpgroup 0 writes dV, 1 dK at the end),
-// warp 8 TMA, warp 9 MMA.
+// warp 8 TMA, warp 9 MMA, warp 10 turns the copies' mbarriers into named barriers.
 namespace kv128 {
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int NQ = 4;  // Q / dO stages (Q 16 KB | dO 16 KB)
 constexpr int kOffK = 0, kOffV = 32768, kOffQ = 65536;
 constexpr int kStage = 32768;
 constexpr int kOffStat = kOffQ + NQ * kStage;  // per softmax warp: lse2[64] | D[64]
 constexpr int kOffBar = kOffStat + 8 * 512;
 constexpr int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = B_QFULL + NQ, B_SFULL = B_QEMPTY + NQ;
-constexpr int B_PDS = B_SFULL + 2, B_DONE = B_PDS + 2;
+constexpr int B_DONE = B_SFULL + 2;
+// named barriers: softmax warpgroup g done with its tile (4 warps + the MMA warp), and
+// Q / dO stage st landed (the watcher warp + the MMA warp)
+constexpr uint32_t kNbPDS = 1, kNbQ = 3, kPdsThreads = 160, kQThreads = 64;
 constexpr int kOffCtl = kOffBar + (B_DONE + 1) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384, kTmemCols = 512;
@@ -920,10 +925,7 @@ __global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
       mbar_init(bar(B_QFULL + st), 1);
       mbar_init(bar(B_QEMPTY + st), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_SFULL + b), 1);
-      mbar_init(bar(B_PDS + b), 4);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(bar(B_SFULL + b), 1);
     mbar_init(bar(B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -937,6 +939,9 @@ __global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Synchronisation: mbarrier waits are bounded and made warp-uniform; every named
+  // barrier is reached once per tile by each of its warps whether or not a wait gave
+  // up, so none of them can be left waiting.
   const int kb = __ldg(p.kt_work + u);  // (i * H_kv + h) * N_q + j
   const int j = kb % p.Nq, h = (kb / p.Nq) % p.Hk, i = kb / (p.Nq * p.Hk);
   const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
@@ -981,8 +986,9 @@ __global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
+    {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, p.status);
       // dV += P^T dO, dK += dS^T Q of tile nt (64 query rows in steps of 16)
       auto kv_products = [&](int nt) {
         const int b = nt & 1, st = nt % NQ;
@@ -998,29 +1004,48 @@ __global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
                     kIdescDQ, (nt > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_QEMPTY + st));
       };
-      for (int nt = 0; ok && nt < ntiles; ++nt) {
+      // S^T / dP^T of tile nt into buffer nt & 1 (its last reader, kv_products(nt - 2),
+      // was issued before by this thread)
+      auto s_products = [&](int nt) {
         const int b = nt & 1, st = nt % NQ;
-        if (!(ok = mbar_wait(bar(B_QFULL + st), (nt / NQ) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // buffer b was last read by kv_products(nt - 2), issued before this by this thread
         mma_xyT(tmem + kColS + 64 * b, smK, smQ + st * kStage);
         mma_xyT(tmem + kColDP + 64 * b, smV, smQ + st * kStage + 16384);
         mma_commit(bar(B_SFULL + b));
-        if (nt >= 1) {
-          if (!(ok = mbar_wait(bar(B_PDS + (b ^ 1)), ((nt - 1) >> 1) & 1, abort_flag, p.status)))
-            break;
+      };
+      // lane 0 issues; the whole warp takes the named barriers.  Tile nt's products
+      // and tile nt + 2's S^T / dP^T go out back to back after one pair of checks.
+      for (int nt = 0; nt < 2 && nt < ntiles; ++nt) {
+        nbar_sync(kNbQ + nt, kQThreads);
+        if (lane == 0 && ok) {
           tc_fence_after();
-          kv_products(nt - 1);
+          s_products(nt);
         }
+        __syncwarp();
       }
-      if (ok && ntiles > 0 &&
-          (ok = mbar_wait(bar(B_PDS + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, abort_flag,
-                          p.status))) {
-        tc_fence_after();
-        kv_products(ntiles - 1);
+      for (int nt = 0; nt < ntiles; ++nt) {
+        const bool next = nt + 2 < ntiles;
+        nbar_sync(kNbPDS + (nt & 1), kPdsThreads);
+        if (next) nbar_sync(kNbQ + (nt + 2) % NQ, kQThreads);
+        if (lane == 0 && ok) {
+          tc_fence_after();
+          kv_products(nt);
+          if (next) s_products(nt + 2);
+        }
+        __syncwarp();
       }
-      mma_commit(bar(B_DONE));
-      mbar_wait_drain(bar(B_DONE), 0);  // MMAs done before TMEM is freed
+      if (lane == 0) {
+        mma_commit(bar(B_DONE));
+        mbar_wait_drain(bar(B_DONE), 0);  // MMAs done before TMEM is freed
+      }
+      __syncwarp();
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ copy watcher
+    bool ok = true;
+    for (int nt = 0; nt < ntiles; ++nt) {
+      if (ok) ok = mbar_wait(bar(B_QFULL + nt % NQ), (nt / NQ) & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      nbar_sync(kNbQ + nt % NQ, kQThreads);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -1029,31 +1054,51 @@ __global__ void __launch_bounds__(kv128::kThreads, 1) bwd_dkdv128_kernel(
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const bool key_ok = j * BK + kin < n;
     float *stat = reinterpret_cast<float *>(sm + kOffStat) + warp * 128;
+    // lse / D of query columns lane and lane + 32 of tile nt (0 past the sequence
+    // end), loaded one tile of this warpgroup ahead of their use
+    auto stat_load = [&](int nt, float(&v)[4]) {
+      if (nt >= ntiles) return;
+      const int r = row_of(nt), tt = nt % tpr;
+      const int qtok0 = 64 * (tt & 1);
+      const size_t q0 = (size_t)(h * p.G + (tt >> 1)) * p.T + s0 + r * BK + qtok0;
+      const int nq = min(64, n - (r * BK + qtok0));
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = lane + 32 * e;
+        v[e] = c < nq ? __ldg(p.lse + q0 + c) : 0.f;
+        v[2 + e] = c < nq ? __ldg(p.Dv + q0 + c) : 0.f;
+      }
+    };
+    float nxt[4] = {0.f, 0.f, 0.f, 0.f};
+    stat_load(g, nxt);
     bool ok = true;
     for (int nt = g; nt < ntiles; nt += 2) {
       const int b = nt & 1;
       const int r = row_of(nt), tt = nt % tpr;
       const int qtok0 = 64 * (tt & 1);                  // first query of the tile in block r
-      const size_t q0 = (size_t)(h * p.G + (tt >> 1)) * p.T + s0 + r * BK + qtok0;
       const int nq = min(64, n - (r * BK + qtok0));     // valid query columns
-      // stage this tile's lse2 / D (columns past the sequence end read as 0)
-      for (int c = lane; c < 64; c += 32) {
-        stat[c] = c < nq ? __ldg(p.lse + q0 + c) * kLog2e : 0.f;
-        stat[64 + c] = c < nq ? __ldg(p.Dv + q0 + c) : 0.f;
-      }
+      // stage this tile's lse2 / D for the broadcasts, then start the next tile's loads
+      stat[lane] = nxt[0] * kLog2e;
+      stat[lane + 32] = nxt[1] * kLog2e;
+      stat[64 + lane] = nxt[2];
+      stat[96 + lane] = nxt[3];
       __syncwarp();
+      stat_load(nt + 2, nxt);
       const int lo = (j == r) ? max(0, kin - qtok0) : 0;  // causal: key <= query
       const int hi = key_ok ? nq : 0;
-      if (!(ok = mbar_wait(bar(B_SFULL + b), (nt >> 1) & 1, abort_flag, p.status))) break;
-      tc_fence_after();
-      tile_grad64_t(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b, stat, lo,
-                    hi, p.scale_log2);
+      if (ok) ok = mbar_wait(bar(B_SFULL + b), (nt >> 1) & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        tile_grad64_t(tmem + lane_base + kColS + 64 * b, tmem + lane_base + kColDP + 64 * b, stat,
+                      lo, hi, p.scale_log2);
+      }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PDS + b));
+      nbar_sync(kNbPDS + g, kPdsThreads);
     }
     // epilogue: TMEM lane = key, 128 columns = d; warpgroup 0 writes dV, 1 dK
-    if (ok && mbar_wait(bar(B_DONE), 0, abort_flag, p.status)) {
+    if (ok) ok = mbar_wait(bar(B_DONE), 0, abort_flag, p.status);
+    if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       uint16_t *out = g == 0 ? p.dV : p.dK;
       const float mul = g == 0 ? 1.f : p.scale;

@@ -140,6 +140,14 @@ BSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_fl
   }
 }
 
+// Named barrier `id` (1 .. 15; 0 is __syncthreads) over `count` threads (a multiple of
+// 32), blocking, warp-collective.  It does not touch shared memory, so it stays cheap
+// while MMAs stream their operands from there.  Every participant must reach it the
+// same number of times: a phase then holds exactly the warps meant for it.
+BSA_DEV void nbar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Wait bounded only by time (used while draining copies / MMAs after an abort).
 BSA_DEV void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
