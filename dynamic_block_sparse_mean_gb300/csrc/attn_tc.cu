@@ -26,8 +26,9 @@
 //     QK_t(s+1) [after K(s+1)]      S_t  = Q_t K(s+1)^T
 // tcgen05.mma operations of one thread execute in issue order, so QK_t(s+1)
 // overwrites S_t only after PV_t(s) has read P_t(s).  Each M-tile has its own
-// issuing thread, and the two alternate batch by batch (a ping-pong of two
-// barriers), so the tensor pipe sees PV_0 QK_0 | PV_1 QK_1 | PV_0 ... and the two
+// issuing thread, and the two alternate batch by batch (a ping-pong of two named
+// barriers, which unlike an mbarrier do not wait behind the MMAs' shared-memory
+// operand reads), so the tensor pipe sees PV_0 QK_0 | PV_1 QK_1 | PV_0 ... and the two
 // tiles' softmaxes stay half a step apart.  A barrier check stalls its own
 // thread's MMA issue for about a hundred cycles, even on a completed phase
 // (measured on GB300: four checks per 32 MMAs of one thread slow the pipe from 64
@@ -54,6 +55,8 @@ constexpr int kTmemCols = 512;
 constexpr int kStep = 128;  // keys per step
 constexpr int kPrefetch = 2;  // steps of K / V prefetched into L2 ahead of their stage load
 constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kNbTurn = 1;  // named barriers 1, 2: the issuers' turns
+constexpr uint32_t kNbP = 3;     // named barriers 3, 4: P_t written (warpgroup t + issuer t)
 
 template <int D, int BK>
 struct Cfg {
@@ -73,14 +76,13 @@ struct Cfg {
   static constexpr int B_QFULL = 0, B_QEMPTY = 1;
   static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + NS;
   static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
-  static constexpr int B_SFULL = B_VEMPTY + NS, B_PFULL = B_SFULL + 2;
-  static constexpr int B_OFREE = B_PFULL + 2;
+  static constexpr int B_SFULL = B_VEMPTY + NS;
+  static constexpr int B_OFREE = B_SFULL + 2;
   static constexpr int B_OFINAL = B_OFREE + 2;    // all PV of a unit done (once per unit)
   static constexpr int B_OSTAGED = B_OFINAL + 2;  // a staged output half is complete (4 warps)
   static constexpr int B_OSFREE = B_OSTAGED + 2;  // the staging buffer was read by its store
   static constexpr int B_FINAL = B_OSFREE + 2;    // one per issuer
-  static constexpr int B_TURN = B_FINAL + 2;      // issuer t's batch is issued (one per issuer)
-  static constexpr int kNumBars = B_TURN + 2;
+  static constexpr int kNumBars = B_FINAL + 2;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemUsed = kOffCtl + 16;
   // 1 KB for base alignment; at least 120 KB so that exactly one CTA (which owns
@@ -341,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
-      mbar_init(bar(C::B_PFULL + t), 4);
       mbar_init(bar(C::B_OFREE + t), 4);
       mbar_init(bar(C::B_OFINAL + t), 1);
     }
@@ -351,8 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::B_FINAL), 1);
     mbar_init(bar(C::B_FINAL + 1), 1);
-    mbar_init(bar(C::B_TURN), 1);
-    mbar_init(bar(C::B_TURN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -457,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers
-    const int t = warp - kMmaWarp;  // the M-tile this thread issues for
-    if (lane == 0) {
+    const int t = warp - kMmaWarp;  // the M-tile this warp's lane 0 issues for
+    {
+      const bool lead = lane == 0;  // waits and issues; the whole warp takes the turns
       int stp = 0, ucount = 0;
       int ks = 0;   // steps of this tile (S / P phases)
       int ut = 0;   // units of this tile (O-free / O-final phases)
@@ -489,71 +489,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (acc || kk > 0) ? 1u : 0u);
       };
       // Batches alternate between the issuers: issuer 0's batch b follows issuer 1's
-      // batch b - 1, issuer 1's batch b follows issuer 0's batch b.
+      // batch b - 1, issuer 1's batch b follows issuer 0's batch b.  The turn passes
+      // through two named barriers (issuer 0 -> 1, issuer 1 -> 0) that both warps
+      // take once per batch, blocking: a named barrier does not go through shared
+      // memory, where an mbarrier check waits behind the MMAs' operand reads.  Both
+      // issuers walk every batch of every unit, after a failed wait too (they then
+      // skip the waits and the MMAs), so the two barriers always pair up.
       int nb = 0;
       auto my_turn = [&]() {
-        if (t == 0 && nb == 0) return true;
-        const int other = 1 - t, k = t == 0 ? nb - 1 : nb;
-        return mbar_wait(bar(C::B_TURN + other), k & 1, abort_flag, p.status);
+        __syncwarp();
+        if (t == 1) nbar_sync(kNbTurn, 64);
+        else if (nb > 0) nbar_sync(kNbTurn + 1, 64);
       };
       auto turn_done = [&]() {
-        mbar_arrive(bar(C::B_TURN + t));
+        __syncwarp();
+        nbar_sync(kNbTurn + t, 64);
         ++nb;
+      };
+      auto wait = [&](int b, uint32_t parity) {
+        if (lead && ok) ok = mbar_wait(bar(b), parity, abort_flag, p.status);
       };
       Unit nx;
       if (blockIdx.x < total_units) nx = decode_unit<CHUNK>(p, blockIdx.x);
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ucount) {
+      for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++ucount) {
         const Unit x = nx;
         if (u + (int)gridDim.x < total_units) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
         const int nsteps = (x.nkv + BPS - 1) / BPS;
         const bool active = t < x.nt;
         // Every barrier a batch needs is checked before the issuer takes its turn,
-        // while the other tile's batch runs; the turn check is then the only wait
-        // between the two threads' batches.
-        if (!(ok = mbar_wait(bar(C::B_QFULL), ucount & 1, abort_flag, p.status))) break;
+        // while the other tile's batch runs; the turn is then the only wait between
+        // the two warps' batches.
+        wait(C::B_QFULL, ucount & 1);
         {  // QK of step 0
           const int st = stp % C::NS;
-          if (!(ok = mbar_wait(bar(C::B_KFULL + st), (stp / C::NS) & 1, abort_flag, p.status)))
-            break;
-          if (!(ok = my_turn())) break;
-          tc_fence_after();
-          if (active) {
-            issue_qk(st);
-            mma_commit(bar(C::B_SFULL + t));
+          wait(C::B_KFULL + st, (stp / C::NS) & 1);
+          my_turn();
+          if (lead && ok) {
+            tc_fence_after();
+            if (active) {
+              issue_qk(st);
+              mma_commit(bar(C::B_SFULL + t));
+            }
+            mma_commit(bar(C::B_KEMPTY + st));
+            if (nsteps == 1) mma_commit(bar(C::B_QEMPTY));
           }
-          mma_commit(bar(C::B_KEMPTY + st));
-          if (nsteps == 1) mma_commit(bar(C::B_QEMPTY));
           turn_done();
         }
-        for (int s = 0; ok && s < nsteps; ++s) {
+        for (int s = 0; s < nsteps; ++s) {
           const int g = stp + s, st = g % C::NS;
           const int g1 = g + 1, st1 = g1 % C::NS;
           const bool more = s + 1 < nsteps;
-          if (!(ok = mbar_wait(bar(C::B_VFULL + st), (g / C::NS) & 1, abort_flag, p.status)))
-            break;
+          wait(C::B_VFULL + st, (g / C::NS) & 1);
           if (active) {
-            if (!(ok = mbar_wait(bar(C::B_PFULL + t), (ks + s) & 1, abort_flag, p.status))) break;
-            if (s == 0 &&
-                !(ok = mbar_wait(bar(C::B_OFREE + t), (ut & 1) ^ 1, abort_flag, p.status)))
-              break;
+            __syncwarp();
+            nbar_sync(kNbP + t, 160);  // P_t(s) is in tensor memory
+            if (s == 0) wait(C::B_OFREE + t, (ut & 1) ^ 1);
           }
-          if (more &&
-              !(ok = mbar_wait(bar(C::B_KFULL + st1), (g1 / C::NS) & 1, abort_flag, p.status)))
-            break;
-          if (!(ok = my_turn())) break;
-          tc_fence_after();
-          if (active) {
-            issue_pv(st, s > 0);
-            if (!more) mma_commit(bar(C::B_OFINAL + t));
-          }
-          mma_commit(bar(C::B_VEMPTY + st));
-          if (more) {
+          if (more) wait(C::B_KFULL + st1, (g1 / C::NS) & 1);
+          my_turn();
+          if (lead && ok) {
+            tc_fence_after();
             if (active) {
-              issue_qk(st1);
-              mma_commit(bar(C::B_SFULL + t));
+              issue_pv(st, s > 0);
+              if (!more) mma_commit(bar(C::B_OFINAL + t));
             }
-            mma_commit(bar(C::B_KEMPTY + st1));
-            if (s + 2 == nsteps) mma_commit(bar(C::B_QEMPTY));
+            mma_commit(bar(C::B_VEMPTY + st));
+            if (more) {
+              if (active) {
+                issue_qk(st1);
+                mma_commit(bar(C::B_SFULL + t));
+              }
+              mma_commit(bar(C::B_KEMPTY + st1));
+              if (s + 2 == nsteps) mma_commit(bar(C::B_QEMPTY));
+            }
           }
           turn_done();
         }
@@ -563,9 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stp += nsteps;
       }
+      // issuer 1's last batch hands the turn to issuer 0 once more
+      if (t == 0 && nb > 0) {
+        __syncwarp();
+        nbar_sync(kNbTurn + 1, 64);
+      }
       // Every MMA this thread issued completes before TMEM is released.
-      mma_commit(bar(C::B_FINAL + t));
-      mbar_wait_drain(bar(C::B_FINAL + t), 0);
+      if (lead) {
+        mma_commit(bar(C::B_FINAL + t));
+        mbar_wait_drain(bar(C::B_FINAL + t), 0);
+      }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -598,7 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       nx = decode_unit<CHUNK>(p, blockIdx.x);
       nx_diag = diag_of(nx);
     }
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+    // Every step of every unit of this tile takes the P barrier with issuer t, after a
+    // failed wait too (the work is then skipped), so the two sides always pair up.
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
       const Unit x = nx;
       const int diag_j = nx_diag;
       const bool has_next = u + (int)gridDim.x < total_units;
@@ -625,7 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jb >= x.nkv) lim[hh] = 0;
           else if (jb == diag_j) lim[hh] = max(0, min(64, tok_in_blk - key0 + 1));
         }
-        if (!(ok = mbar_wait(bar(C::B_SFULL + t), kstep & 1, abort_flag, p.status))) break;
+        if (ok) ok = mbar_wait(bar(C::B_SFULL + t), kstep & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          __syncwarp();
+          nbar_sync(kNbP + t, 160);
+          if (s == 0 && has_next) nx_diag = diag_of(nx);
+          continue;
+        }
         tc_fence_after();
         float mx;
         // tcgen05 loads are warp-collective: the path must be the same for every
@@ -668,13 +693,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += exp_step<true>(tS, scale2, negm, lim);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
+        nbar_sync(kNbP + t, 160);
         // The next unit's diagonal position: its load overlaps the wait for S(1).
         if (s == 0 && has_next) nx_diag = diag_of(nx);
       }
-      if (!ok) break;
+      if (!ok) continue;
       // epilogue: O = u / l, lse = (m + log2 l) ln 2
-      if (!(ok = mbar_wait(bar(C::B_OFINAL + t), units & 1, abort_flag, p.status))) break;
+      ok = mbar_wait(bar(C::B_OFINAL + t), units & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        continue;
+      }
       ++units;
       tc_fence_after();
       const bool store = row_valid && tq < x.n;
@@ -708,8 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < C::kPanels; ++hh, ++ostage) {
           // the previous store out of this buffer has finished reading it
-          if (!(ok = mbar_wait(bar(C::B_OSFREE + t), (ostage & 1) ^ 1, abort_flag, p.status)))
+          if (!__all_sync(0xffffffffu, ok = mbar_wait(bar(C::B_OSFREE + t), (ostage & 1) ^ 1,
+                                                      abort_flag, p.status))) {
+            ok = false;
             break;
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             st_shared_v4(stg + rho * 128 + ((c ^ (rho & 7)) << 4), ob[hh * 32 + 4 * c],
@@ -718,15 +750,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::B_OSTAGED + t));
           if (elected) {
-            if (!(ok = mbar_wait(bar(C::B_OSTAGED + t), ostage & 1, abort_flag, p.status))) break;
-            tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
-                         x.h * p.G + ((2 * x.pair + t) * 128) / BK);
-            bulk_commit();
-            bulk_wait_read();
-            mbar_arrive(bar(C::B_OSFREE + t));
+            ok = mbar_wait(bar(C::B_OSTAGED + t), ostage & 1, abort_flag, p.status);
+            if (ok) {
+              tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
+                           x.h * p.G + ((2 * x.pair + t) * 128) / BK);
+              bulk_commit();
+              bulk_wait_read();
+              mbar_arrive(bar(C::B_OSFREE + t));
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);  // the elected thread's outcome, warp-wide
+          if (!ok) break;
         }
-        if (!ok) break;
+        if (!ok) continue;
       } else if (store) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.O + ((size_t)hq * p.T + x.s0 + tq) * D);
 #pragma unroll
