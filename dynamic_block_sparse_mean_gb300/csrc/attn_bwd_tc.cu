@@ -221,11 +221,12 @@ BSA_DEV void tmem_st8_nowait(uint32_t taddr, const uint32_t (&r)[8]) {
 // dS of the 64 keys of one TMEM S / dP tile row written back to tensor memory as
 // bf16 pairs (32 columns at tDS, key 2 c and 2 c + 1 in column c: the layout of a
 // tensor-memory A operand), 16 columns at a time as tile_grad64 does.  Once the
-// last S / dP columns are loaded the warp arrives on `sread` (the S / dP buffer may
-// then be overwritten); the stores are waited before returning.
+// last S / dP columns are loaded the warp takes named barrier `sread` (over
+// `sread_threads` threads: the S / dP buffer may then be overwritten); the stores
+// are waited before returning.
 BSA_DEV void tile_grad64_tmem(uint32_t tS, uint32_t tDP, uint32_t tDS, bool valid, bool diag,
                               int key0, int tok, float scale_log2, float lse2, float Drow,
-                              uint32_t sread) {
+                              uint32_t sread, uint32_t sread_threads) {
   uint32_t sb[2][16], db[2][16];
   const int lim = !valid ? 0 : (diag ? min(64, max(0, tok - key0 + 1)) : 64);  // first masked column
   const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
@@ -256,7 +257,7 @@ BSA_DEV void tile_grad64_tmem(uint32_t tS, uint32_t tDP, uint32_t tDS, bool vali
     if (c == 2) {  // every S / dP column of this warp is in registers
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(sread);
+      nbar_sync(sread, sread_threads);
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -350,16 +351,18 @@ __global__ void kt_emit_kernel(const uint32_t *__restrict__ bits,
 // 4 g + 3, one query row per thread) takes the 64 keys 64 g .. 64 g + 63 of every
 // step.  320 threads: warps 0-7 softmax, warp 8 TMA, warp 9 MMA.
 namespace dq {
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int NK = 3, NV = 2;  // K and V ring stages (32 KB each: 128 keys x d)
 constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NK * 32768;
 constexpr int kOffBar = kOffV + NV * 32768;
 constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK;
 constexpr int B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV;
-// SREAD: the softmax has loaded S / dP of the step (8 warps); DSFULL / DSFREE per
-// dS buffer
-constexpr int B_SREAD = B_SFULL + 1, B_DSFULL = B_SREAD + 1, B_DSFREE = B_DSFULL + 2;
-constexpr int B_DQFULL = B_DSFREE + 2;
+// DSFREE per dS buffer: dQ(s) has read it
+constexpr int B_DSFREE = B_SFULL + 1, B_DQFULL = B_DSFREE + 2;
+// named barriers, each taken once per step by all of its warps: K / V of the step
+// landed (watcher + MMA warp), S / dP loaded by the softmax and dS written (8 softmax
+// warps + MMA warp)
+constexpr uint32_t kNbKV = 1, kNbSR = 2, kNbDS = 3, kKVThreads = 64, kSoftThreads = 288;
 constexpr int kOffCtl = kOffBar + (B_DQFULL + 1) * 8;
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384, kTmemCols = 512;
@@ -394,11 +397,7 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       mbar_init(bar(B_VEMPTY + st), 1);
     }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SREAD), 8);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_DSFULL + b), 8);
-      mbar_init(bar(B_DSFREE + b), 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(bar(B_DSFREE + b), 1);
     mbar_init(bar(B_DQFULL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -472,8 +471,11 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
+    // Lane 0 issues; the whole warp takes the named barriers, once per step each
+    // whether or not a wait gave up, so none of them can be left waiting.
+    {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
       auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 128 keys in steps of 16, dS from TMEM
         const int b = s & 1;
         const uint32_t bl = desc_lo(smK + (s % NK) * 32768, 16384);
@@ -484,34 +486,51 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
         mma_commit(bar(B_KEMPTY + s % NK));
         mma_commit(bar(B_DSFREE + b));
       };
-      for (int s = 0; ok && s < nsteps; ++s) {
-        if (!(ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status)) ||
-            !(ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status)))
-          break;
-        // S / dP(s - 1) loaded by the softmax: the single S / dP buffer is free
-        if (s >= 1 && !(ok = mbar_wait(bar(B_SREAD), (s - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        mma_xyT128(tmem + kColS, smQ, smK + (s % NK) * 32768);
-        mma_xyT128(tmem + kColDP, smDO, smV + (s % NV) * 32768);
-        mma_commit(bar(B_SFULL));
-        mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
+      for (int s = 0; s < nsteps; ++s) {
+        // S / dP(s - 1) loaded by the softmax: the single S / dP buffer is free (taken
+        // first: the softmax waits on this barrier in the middle of its step)
+        if (s >= 1) nbar_sync(kNbSR, kSoftThreads);
+        nbar_sync(kNbKV, kKVThreads);
+        if (lane == 0 && ok) {
+          tc_fence_after();
+          mma_xyT128(tmem + kColS, smQ, smK + (s % NK) * 32768);
+          mma_xyT128(tmem + kColDP, smDO, smV + (s % NV) * 32768);
+          mma_commit(bar(B_SFULL));
+          mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
+        }
+        __syncwarp();
         if (s >= 1) {
-          const int sp = s - 1;
-          if (!(ok = mbar_wait(bar(B_DSFULL + (sp & 1)), (sp >> 1) & 1, abort_flag, p.status)))
-            break;
-          tc_fence_after();
-          dq_product(sp);
+          nbar_sync(kNbDS, kSoftThreads);  // dS(s - 1) written
+          if (lane == 0 && ok) {
+            tc_fence_after();
+            dq_product(s - 1);
+          }
+          __syncwarp();
         }
       }
-      if (ok && nsteps > 0) {
-        const int sp = nsteps - 1;
-        if ((ok = mbar_wait(bar(B_DSFULL + (sp & 1)), (sp >> 1) & 1, abort_flag, p.status))) {
+      if (nsteps > 0) {
+        nbar_sync(kNbSR, kSoftThreads);
+        nbar_sync(kNbDS, kSoftThreads);
+        if (lane == 0 && ok) {
           tc_fence_after();
-          dq_product(sp);
+          dq_product(nsteps - 1);
         }
+        __syncwarp();
       }
-      mma_commit(bar(B_DQFULL));
-      mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
+      if (lane == 0) {
+        mma_commit(bar(B_DQFULL));
+        mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
+      }
+      __syncwarp();
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ copy watcher
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      if (ok) ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status);
+      if (ok) ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      nbar_sync(kNbKV, kKVThreads);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -530,20 +549,24 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       const bool present = e < nkv;
       const int j = present ? __ldg(p.col_idx + kv0 + e) : -1;
       const int key0 = BPS == 1 ? 64 * g : 0;
-      if (!(ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status))) break;
+      if (ok) ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status);
       // dS buffer b was read by dQ(s - 2) (issued one step ago)
-      if (s >= 2 && !(ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status)))
-        break;
-      tc_fence_after();
-      tile_grad64_tmem(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g,
-                       tmem + lane_base + kColDS + 64 * b + 32 * g, q.valid && present, j == r,
-                       key0, q.tok, p.scale_log2, lse2, Drow, bar(B_SREAD));
+      if (ok && s >= 2) ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        tile_grad64_tmem(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g,
+                         tmem + lane_base + kColDS + 64 * b + 32 * g, q.valid && present, j == r,
+                         key0, q.tok, p.scale_log2, lse2, Drow, kNbSR, kSoftThreads);
+      } else {
+        nbar_sync(kNbSR, kSoftThreads);
+      }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSFULL + b));
+      nbar_sync(kNbDS, kSoftThreads);
     }
     // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
-    if (ok && mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status)) {
+    if (ok) ok = mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status);
+    if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
 #pragma unroll
