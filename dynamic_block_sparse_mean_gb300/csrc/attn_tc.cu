@@ -594,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kstep = 0;                    // steps of this tile (S / P / O-done phases)
     int units = 0;                    // units of this tile (O-final phases)
     int ostage = 0;                   // output staging uses of this tile
+    bool store_pending = false;       // elected thread: the last staged store is not yet waited
     bool ok = true;
     const uint64_t scale2 = pack2(p.scale_log2, p.scale_log2);
     // Position of the diagonal block r in a unit's row (the token-level triangle),
@@ -736,6 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool elected = wq == 0 && lane == 0;
 #pragma unroll
         for (int hh = 0; hh < C::kPanels; ++hh, ++ostage) {
+          // the last half of the previous unit is waited for only now, when the buffer
+          // is needed again
+          if (elected && store_pending) {
+            bulk_wait_read();
+            mbar_arrive(bar(C::B_OSFREE + t));
+            store_pending = false;
+          }
           // the previous store out of this buffer has finished reading it
           if (!__all_sync(0xffffffffu, ok = mbar_wait(bar(C::B_OSFREE + t), (ostage & 1) ^ 1,
                                                       abort_flag, p.status))) {
@@ -755,8 +763,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
                            x.h * p.G + ((2 * x.pair + t) * 128) / BK);
               bulk_commit();
-              bulk_wait_read();
-              mbar_arrive(bar(C::B_OSFREE + t));
+              if (hh + 1 < C::kPanels) {
+                bulk_wait_read();
+                mbar_arrive(bar(C::B_OSFREE + t));
+              } else {
+                store_pending = true;
+              }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);  // the elected thread's outcome, warp-wide
