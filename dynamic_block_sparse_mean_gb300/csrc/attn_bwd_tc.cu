@@ -355,7 +355,8 @@ constexpr int kThreads = 352;
 constexpr int NK = 3, NV = 2;  // K and V ring stages (32 KB each: 128 keys x d)
 constexpr int kOffQ = 0, kOffDO = 32768, kOffK = 65536, kOffV = kOffK + NK * 32768;
 constexpr int kOffBar = kOffV + NV * 32768;
-constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NK;
+constexpr int B_VFULL = B_KEMPTY + NK;
 constexpr int B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV;
 // DSFREE per dS buffer: dQ(s) has read it
 constexpr int B_DSFREE = B_SFULL + 1, B_DQFULL = B_DSFREE + 2;
@@ -369,6 +370,11 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384, kTmemCol
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 }  // namespace dq
 
+// Persistent: one CTA per SM walks the work items (router row, 128-row M-tile) of the
+// worklist's longest-first order with a stride of the grid.  Ring stages, barrier phases
+// and dS buffers follow step and item counters that run on across items, so the next
+// item's Q / dO load starts once the current item's last S / dP products have read
+// theirs, and its first steps overlap the current item's last dQ products and dQ store.
 template <int BK>
 __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -376,8 +382,8 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     const BwdTcParams p) {
   using namespace dq;
   constexpr int BPS = 128 / BK;  // key blocks per 128-key step
-  const int u = blockIdx.x;
-  if (u >= __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.mtiles) return;
+  const int total = __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.mtiles;  // work items
+  if ((int)blockIdx.x >= total) return;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -388,6 +394,7 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
     for (int st = 0; st < NK; ++st) {
       mbar_init(bar(B_KFULL + st), 1);
       mbar_init(bar(B_KEMPTY + st), 1);
@@ -410,59 +417,86 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  const int t = u % p.mtiles;
-  const int row = __ldg(p.work + u / p.mtiles);
-  const int r = row % p.Nq, h = (row / p.Nq) % p.Hk, i = row / (p.Nq * p.Hk);
-  const int s0 = __ldg(p.cu + i), n = __ldg(p.cu + i + 1) - s0;
-  const int kv0 = __ldg(p.row_ptr + row), nkv = __ldg(p.row_ptr + row + 1) - kv0;
-  const int nsteps = (nkv + BPS - 1) / BPS;
   const uint32_t smQ = sbase + kOffQ, smDO = sbase + kOffDO, smK = sbase + kOffK,
                  smV = sbase + kOffV;
+
+  struct Item {
+    int t, r, h, s0, n, kv0, nkv, nsteps;
+  };
+  auto item_of = [&](int u) {
+    Item w;
+    w.t = u % p.mtiles;
+    const int row = __ldg(p.work + u / p.mtiles);
+    w.r = row % p.Nq;
+    w.h = (row / p.Nq) % p.Hk;
+    const int i = row / (p.Nq * p.Hk);
+    w.s0 = __ldg(p.cu + i);
+    w.n = __ldg(p.cu + i + 1) - w.s0;
+    w.kv0 = __ldg(p.row_ptr + row);
+    w.nkv = __ldg(p.row_ptr + row + 1) - w.kv0;
+    w.nsteps = (w.nkv + BPS - 1) / BPS;
+    return w;
+  };
+  // every role walks the same items; the next item is decoded one ahead
+  const int stride = (int)gridDim.x;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      int issued_k[NK], issued_v[NV];
+      int issued_k[NK], issued_v[NV], issued_q = -1;
       for (int st = 0; st < NK; ++st) issued_k[st] = -1;
       for (int st = 0; st < NV; ++st) issued_v[st] = -1;
-      const int hq0 = h * p.G + (t * 128) / BK;
-      mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
-      for (int pn = 0; pn < 2; ++pn) {
-        tma_load_3d(smQ + pn * 16384, &tmQ, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
-        tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, s0 + r * BK, hq0);
-      }
-      // token row of 64-key half hf of step s (a missing second block repeats the first)
-      auto key_row = [&](int s, int hf) {
-        if (BPS == 1) return s0 + checked_index(__ldg(p.col_idx + kv0 + s), 0, r, p.status) * BK + hf * 64;
-        const int e = min(2 * s + hf, nkv - 1);
-        return s0 + checked_index(__ldg(p.col_idx + kv0 + e), 0, r, p.status) * BK;
-      };
-      for (int s = 0; s < nsteps; ++s) {
-        const int sk = s % NK, sv = s % NV;
-        const int y0 = key_row(s, 0), y1 = key_row(s, 1);
-        if (s >= NK &&
-            !(ok = mbar_wait(bar(B_KEMPTY + sk), ((s - NK) / NK) & 1, abort_flag, p.status)))
+      int gs = 0, it = 0;
+      Item nx = item_of(blockIdx.x);
+      for (int u = blockIdx.x; ok && u < total; u += stride, ++it) {
+        const Item w = nx;
+        if (u + stride < total) nx = item_of(u + stride);
+        const int hq0 = w.h * p.G + (w.t * 128) / BK;
+        // the previous item's last S / dP products have read its Q / dO
+        if (it >= 1 && !(ok = mbar_wait(bar(B_QEMPTY), (it - 1) & 1, abort_flag, p.status)))
           break;
-        mbar_arrive_expect_tx(bar(B_KFULL + sk), 4 * 8192);
-        issued_k[sk] = (s / NK) & 1;
-        for (int pn = 0; pn < 2; ++pn) {  // panel pn: d columns 64 pn .. 64 pn + 63, 128 rows
-          tma_load_3d(smK + sk * 32768 + pn * 16384, &tmK, bar(B_KFULL + sk), pn * 64, y0, h);
-          tma_load_3d(smK + sk * 32768 + pn * 16384 + 8192, &tmK, bar(B_KFULL + sk), pn * 64, y1, h);
-        }
-        if (s >= NV &&
-            !(ok = mbar_wait(bar(B_VEMPTY + sv), ((s - NV) / NV) & 1, abort_flag, p.status)))
-          break;
-        mbar_arrive_expect_tx(bar(B_VFULL + sv), 4 * 8192);
-        issued_v[sv] = (s / NV) & 1;
+        mbar_arrive_expect_tx(bar(B_QFULL), 4 * 16384);
+        issued_q = it & 1;
         for (int pn = 0; pn < 2; ++pn) {
-          tma_load_3d(smV + sv * 32768 + pn * 16384, &tmV, bar(B_VFULL + sv), pn * 64, y0, h);
-          tma_load_3d(smV + sv * 32768 + pn * 16384 + 8192, &tmV, bar(B_VFULL + sv), pn * 64, y1, h);
+          tma_load_3d(smQ + pn * 16384, &tmQ, bar(B_QFULL), pn * 64, w.s0 + w.r * BK, hq0);
+          tma_load_3d(smDO + pn * 16384, &tmDO, bar(B_QFULL), pn * 64, w.s0 + w.r * BK, hq0);
+        }
+        // token row of 64-key half hf of step s (a missing second block repeats the first)
+        auto key_row = [&](int s, int hf) {
+          if (BPS == 1)
+            return w.s0 + checked_index(__ldg(p.col_idx + w.kv0 + s), 0, w.r, p.status) * BK +
+                   hf * 64;
+          const int e = min(2 * s + hf, w.nkv - 1);
+          return w.s0 + checked_index(__ldg(p.col_idx + w.kv0 + e), 0, w.r, p.status) * BK;
+        };
+        for (int s = 0; s < w.nsteps; ++s, ++gs) {
+          const int sk = gs % NK, sv = gs % NV;
+          const int y0 = key_row(s, 0), y1 = key_row(s, 1);
+          if (gs >= NK &&
+              !(ok = mbar_wait(bar(B_KEMPTY + sk), ((gs - NK) / NK) & 1, abort_flag, p.status)))
+            break;
+          mbar_arrive_expect_tx(bar(B_KFULL + sk), 4 * 8192);
+          issued_k[sk] = (gs / NK) & 1;
+          for (int pn = 0; pn < 2; ++pn) {  // panel pn: d columns 64 pn .. 64 pn + 63, 128 rows
+            tma_load_3d(smK + sk * 32768 + pn * 16384, &tmK, bar(B_KFULL + sk), pn * 64, y0, w.h);
+            tma_load_3d(smK + sk * 32768 + pn * 16384 + 8192, &tmK, bar(B_KFULL + sk), pn * 64,
+                        y1, w.h);
+          }
+          if (gs >= NV &&
+              !(ok = mbar_wait(bar(B_VEMPTY + sv), ((gs - NV) / NV) & 1, abort_flag, p.status)))
+            break;
+          mbar_arrive_expect_tx(bar(B_VFULL + sv), 4 * 8192);
+          issued_v[sv] = (gs / NV) & 1;
+          for (int pn = 0; pn < 2; ++pn) {
+            tma_load_3d(smV + sv * 32768 + pn * 16384, &tmV, bar(B_VFULL + sv), pn * 64, y0, w.h);
+            tma_load_3d(smV + sv * 32768 + pn * 16384 + 8192, &tmV, bar(B_VFULL + sv), pn * 64,
+                        y1, w.h);
+          }
         }
       }
       // every copy issued lands before the CTA leaves
-      mbar_wait_drain(bar(B_QFULL), 0);
+      if (issued_q >= 0) mbar_wait_drain(bar(B_QFULL), issued_q);
       for (int st = 0; st < NK; ++st)
         if (issued_k[st] >= 0) mbar_wait_drain(bar(B_KFULL + st), issued_k[st]);
       for (int st = 0; st < NV; ++st)
@@ -471,117 +505,142 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Lane 0 issues; the whole warp takes the named barriers, once per step each
-    // whether or not a wait gave up, so none of them can be left waiting.
+    // Lane 0 issues; the whole warp takes the named barriers, once per step each, so
+    // none of them can be left waiting.
     {
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status);
-      auto dq_product = [&](int s) {  // dQ += dS(s) K(s): 128 keys in steps of 16, dS from TMEM
-        const int b = s & 1;
-        const uint32_t bl = desc_lo(smK + (s % NK) * 32768, 16384);
+      // dQ += dS(g) K(g): 128 keys in steps of 16, dS from TMEM; `first` starts the
+      // item's accumulator
+      auto dq_product = [&](int g, bool first) {
+        const int b = g & 1;
+        const uint32_t bl = desc_lo(smK + (g % NK) * 32768, 16384);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts_lo(tmem + kColDQ, tmem + kColDS + 64 * b + 8 * kk, bl + kk * 128, kDescHi,
-                    kIdescDQ, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_KEMPTY + s % NK));
+                    kIdescDQ, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_KEMPTY + g % NK));
         mma_commit(bar(B_DSFREE + b));
       };
-      for (int s = 0; s < nsteps; ++s) {
-        // S / dP(s - 1) loaded by the softmax: the single S / dP buffer is free (taken
-        // first: the softmax waits on this barrier in the middle of its step)
-        if (s >= 1) nbar_sync(kNbSR, kSoftThreads);
-        nbar_sync(kNbKV, kKVThreads);
-        if (lane == 0 && ok) {
-          tc_fence_after();
-          mma_xyT128(tmem + kColS, smQ, smK + (s % NK) * 32768);
-          mma_xyT128(tmem + kColDP, smDO, smV + (s % NV) * 32768);
-          mma_commit(bar(B_SFULL));
-          mma_commit(bar(B_VEMPTY + s % NV));  // V(s) has no other reader
-        }
-        __syncwarp();
-        if (s >= 1) {
-          nbar_sync(kNbDS, kSoftThreads);  // dS(s - 1) written
-          if (lane == 0 && ok) {
+      int gs = 0, it = 0;
+      Item nx = item_of(blockIdx.x);
+      for (int u = blockIdx.x; u < total; u += stride, ++it) {
+        const Item w = nx;
+        if (u + stride < total) nx = item_of(u + stride);
+        for (int s = 0; s < w.nsteps; ++s) {
+          const int g = gs + s;
+          // S / dP(g - 1) loaded by the softmax: the single S / dP buffer is free (the
+          // previous item's last step was waited for below; this one is taken first:
+          // the softmax waits on it in the middle of its step)
+          if (s >= 1) nbar_sync(kNbSR, kSoftThreads);
+          nbar_sync(kNbKV, kKVThreads);  // K / V(g) landed (and the item's Q / dO at s = 0)
+          if (lane == 0) {
             tc_fence_after();
-            dq_product(s - 1);
+            mma_xyT128(tmem + kColS, smQ, smK + (g % NK) * 32768);
+            mma_xyT128(tmem + kColDP, smDO, smV + (g % NV) * 32768);
+            mma_commit(bar(B_SFULL));
+            mma_commit(bar(B_VEMPTY + g % NV));  // V(g) has no other reader
+            if (s + 1 == w.nsteps) mma_commit(bar(B_QEMPTY));  // the item's Q / dO are read
           }
           __syncwarp();
+          if (s >= 1) {
+            // dS(g - 1) written; at s = 1 the softmax warps have also finished reading
+            // the previous item's dQ, which this item's first product overwrites
+            nbar_sync(kNbDS, kSoftThreads);
+            if (lane == 0) {
+              tc_fence_after();
+              dq_product(g - 1, s == 1);
+            }
+            __syncwarp();
+          }
         }
-      }
-      if (nsteps > 0) {
         nbar_sync(kNbSR, kSoftThreads);
         nbar_sync(kNbDS, kSoftThreads);
-        if (lane == 0 && ok) {
+        if (lane == 0) {
           tc_fence_after();
-          dq_product(nsteps - 1);
+          dq_product(gs + w.nsteps - 1, w.nsteps == 1);
+          mma_commit(bar(B_DQFULL));
         }
         __syncwarp();
+        gs += w.nsteps;
       }
-      if (lane == 0) {
-        mma_commit(bar(B_DQFULL));
-        mbar_wait_drain(bar(B_DQFULL), 0);  // MMAs done before TMEM is freed
-      }
+      if (lane == 0 && it > 0) mbar_wait_drain(bar(B_DQFULL), (it - 1) & 1);  // before TMEM is freed
       __syncwarp();
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ copy watcher
     bool ok = true;
-    for (int s = 0; s < nsteps; ++s) {
-      if (ok) ok = mbar_wait(bar(B_KFULL + s % NK), (s / NK) & 1, abort_flag, p.status);
-      if (ok) ok = mbar_wait(bar(B_VFULL + s % NV), (s / NV) & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      nbar_sync(kNbKV, kKVThreads);
+    int gs = 0, it = 0;
+    Item nx = item_of(blockIdx.x);
+    for (int u = blockIdx.x; u < total; u += stride, ++it) {
+      const Item w = nx;
+      if (u + stride < total) nx = item_of(u + stride);
+      for (int s = 0; s < w.nsteps; ++s, ++gs) {
+        if (ok && s == 0) ok = mbar_wait(bar(B_QFULL), it & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait(bar(B_KFULL + gs % NK), (gs / NK) & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait(bar(B_VFULL + gs % NV), (gs / NV) & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        nbar_sync(kNbKV, kKVThreads);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int g = warp / 4, wq = warp % 4;  // warpgroup g: keys 64 g .. 64 g + 63 of a step
     const int rho = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const QRow q = qrow<BK>(p, t, rho, h, r, s0, n);
-    const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
-    const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
     bool ok = true;
-    for (int s = 0; s < nsteps; ++s) {
-      const int b = s & 1;
-      // this warpgroup's 64 keys: half g of the step's 128-key block, or its 64-key
-      // block (absent past the row's last block)
-      const int e = BPS == 1 ? s : 2 * s + g;
-      const bool present = e < nkv;
-      const int j = present ? __ldg(p.col_idx + kv0 + e) : -1;
-      const int key0 = BPS == 1 ? 64 * g : 0;
-      if (ok) ok = mbar_wait(bar(B_SFULL), s & 1, abort_flag, p.status);
-      // dS buffer b was read by dQ(s - 2) (issued one step ago)
-      if (ok && s >= 2) ok = mbar_wait(bar(B_DSFREE + b), ((s - 2) >> 1) & 1, abort_flag, p.status);
+    int gs = 0, it = 0;
+    Item nx = item_of(blockIdx.x);
+    for (int u = blockIdx.x; u < total; u += stride, ++it) {
+      const Item w = nx;
+      if (u + stride < total) nx = item_of(u + stride);
+      const QRow q = qrow<BK>(p, w.t, rho, w.h, w.r, w.s0, w.n);
+      const float lse2 = q.valid ? __ldg(p.lse + q.idx) * kLog2e : 0.f;
+      const float Drow = q.valid ? __ldg(p.Dv + q.idx) : 0.f;
+      for (int s = 0; s < w.nsteps; ++s) {
+        const int gg = gs + s, b = gg & 1;
+        // this warpgroup's 64 keys: half g of the step's 128-key block, or its 64-key
+        // block (absent past the row's last block)
+        const int e = BPS == 1 ? s : 2 * s + g;
+        const bool present = e < w.nkv;
+        const int j = present ? __ldg(p.col_idx + w.kv0 + e) : -1;
+        const int key0 = BPS == 1 ? 64 * g : 0;
+        if (ok) ok = mbar_wait(bar(B_SFULL), gg & 1, abort_flag, p.status);
+        // dS buffer b was read by dQ(gg - 2) (issued one step ago)
+        if (ok && gg >= 2)
+          ok = mbar_wait(bar(B_DSFREE + b), ((gg - 2) >> 1) & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          tile_grad64_tmem(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g,
+                           tmem + lane_base + kColDS + 64 * b + 32 * g, q.valid && present,
+                           j == w.r, key0, q.tok, p.scale_log2, lse2, Drow, kNbSR,
+                           kSoftThreads);
+        } else {
+          nbar_sync(kNbSR, kSoftThreads);
+        }
+        tc_fence_before();
+        nbar_sync(kNbDS, kSoftThreads);
+      }
+      gs += w.nsteps;
+      // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
+      if (ok) ok = mbar_wait(bar(B_DQFULL), it & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        tile_grad64_tmem(tmem + lane_base + kColS + 64 * g, tmem + lane_base + kColDP + 64 * g,
-                         tmem + lane_base + kColDS + 64 * b + 32 * g, q.valid && present, j == r,
-                         key0, q.tok, p.scale_log2, lse2, Drow, kNbSR, kSoftThreads);
-      } else {
-        nbar_sync(kNbSR, kSoftThreads);
-      }
-      tc_fence_before();
-      nbar_sync(kNbDS, kSoftThreads);
-    }
-    // epilogue: warpgroup g writes columns 64 g .. 64 g + 63 of its rows' dQ
-    if (ok) ok = mbar_wait(bar(B_DQFULL), 0, abort_flag, p.status);
-    if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-      uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + q.idx * kD + 64 * g);
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + kColDQ + 64 * g + c0, rr);
-        uint32_t o[16];
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + kColDQ + 64 * g + c0, rr);
+          uint32_t o[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          o[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale,
-                             __uint_as_float(rr[2 * e + 1]) * p.scale);
-        if (q.valid)
+          for (int e = 0; e < 16; ++e)
+            o[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale,
+                               __uint_as_float(rr[2 * e + 1]) * p.scale);
+          if (q.valid)
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[c0 / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              dst[c0 / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
       }
     }
   }
@@ -1174,8 +1233,8 @@ cudaError_t launch_bk(const bsa_shape_t &s, const void *Q, const void *K, const 
   }
   if (e != cudaSuccess) return e;
   const long long rows = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks;
-  bwd_dq_tc_kernel<BK><<<(unsigned)(rows * p.mtiles), dq::kThreads, dq::kSmemBytes, st>>>(
-      mq, mdo, mk, mv, p);
+  const unsigned dq_grid = (unsigned)std::min<long long>(rows * p.mtiles, num_sms());
+  bwd_dq_tc_kernel<BK><<<dq_grid, dq::kThreads, dq::kSmemBytes, st>>>(mq, mdo, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (BK == 64) {
