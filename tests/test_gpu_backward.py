@@ -22,6 +22,11 @@ CASES = [
     # eight (four M-tiles per row)
     ("bwd_bf16_g1_d128_b64_sink", [500, 70], 2, 2, 128, 64, 4, True, "bf16", 2e-2),
     ("bwd_bf16_gqa8_d128_b64", [600, 1], 16, 2, 128, 64, 3, False, "bf16", 2e-2),
+    # more work items than SMs (440 and 752 (row, M-tile) items): each persistent dQ
+    # CTA walks several items, carrying ring stages, barrier phases and the dS buffer
+    # across them; the 128-key case also runs 94 key-major dK / dV CTAs
+    ("bwd_bf16_gqa4_d128_b64_multi", [4000, 3000], 8, 2, 128, 64, 6, True, "bf16", 2e-2),
+    ("bwd_bf16_gqa8_d128_b128_multi", [6000], 16, 2, 128, 128, 4, True, "bf16", 2e-2),
 ]
 
 
