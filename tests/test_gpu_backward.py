@@ -27,6 +27,10 @@ CASES = [
     # across them; the 128-key case also runs 94 key-major dK / dV CTAs
     ("bwd_bf16_gqa4_d128_b64_multi", [4000, 3000], 8, 2, 128, 64, 6, True, "bf16", 2e-2),
     ("bwd_bf16_gqa8_d128_b128_multi", [6000], 16, 2, 128, 128, 4, True, "bf16", 2e-2),
+    # 128-key blocks with one and two query heads per KV head (2 and 4 query tiles of
+    # 64 rows per selecting row in the key-major pass), ragged tails
+    ("bwd_bf16_g1_d128_b128", [700, 129], 2, 2, 128, 128, 3, True, "bf16", 2e-2),
+    ("bwd_bf16_g2_d128_b128", [900, 60], 4, 2, 128, 128, 3, False, "bf16", 2e-2),
 ]
 
 
