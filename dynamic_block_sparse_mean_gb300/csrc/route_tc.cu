@@ -22,7 +22,10 @@
 //              write / max-merge into S
 //   warp 4     TMA producer: query chunks (G*b rows, <= 256 per chunk) and
 //              16 KB panels of the split summaries, through rings of 2 and 4
-//   warp 5     MMA issuer (one thread), double-buffered accumulators in TMEM
+//   warp 5     MMA issuer (lane 0), double-buffered accumulators in TMEM
+//   warp 6     watcher: waits on the copies' mbarriers and meets the MMA warp on
+//              named barriers (an mbarrier check would cost the issuing thread a few
+//              hundred cycles while the MMAs stream their operands from shared memory)
 // Work order: rows with the longest history first (r descending).
 #include "common.cuh"
 #include "kernels.h"
@@ -32,9 +35,12 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kWatchWarp = 6;
+// named barriers (watcher + MMA warp, taken by both once per query chunk / panel)
+constexpr uint32_t kNbQ = 1, kNbA = 2, kNbThreads = 64;
 constexpr int kQStages = 2;
 constexpr int kAStages = 4;
 constexpr int kAStage = 128 * 128;  // one 128-byte panel of one split part, 128 summaries
@@ -194,31 +200,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      int qi = 0, ai = 0, di = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-        const RUnit x = runit(p, u);
-        if (!x.valid) continue;
-        const int nmt = (x.r + 127) / 128;
-        for (int ch = 0; ok && ch < p.nch; ++ch, ++qi) {
-          const int qs = qi % kQStages;
-          const uint32_t idesc = idesc_bf16(128, chunk_cols(p, ch), false);
-          if (!(ok = mbar_wait(bar(C::B_QFULL + qs), (qi / kQStages) & 1, abort_flag, p.status)))
-            break;
-          tc_fence_after();
-          for (int mt = 0; ok && mt < nmt; ++mt, ++di) {
-            const int db = di % 2;
-            if (!(ok = mbar_wait(bar(C::B_DEMPTY + db), ((di / 2) & 1) ^ 1, abort_flag, p.status)))
-              break;
-            tc_fence_after();
-            bool first = true;
-            for (int part = p.parts - 1; ok && part >= 0; --part)
-              for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
-                const int as = ai % kAStages;
-                if (!(ok = mbar_wait(bar(C::B_AFULL + as), (ai / kAStages) & 1, abort_flag,
-                                     p.status)))
-                  break;
+    // Lane 0 issues; the whole warp takes the named barriers, once per chunk and panel
+    // whether or not a wait gave up, so the watcher's and its own always pair up.
+    int qi = 0, ai = 0, di = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const RUnit x = runit(p, u);
+      if (!x.valid) continue;
+      const int nmt = (x.r + 127) / 128;
+      for (int ch = 0; ch < p.nch; ++ch, ++qi) {
+        const int qs = qi % kQStages;
+        const uint32_t idesc = idesc_bf16(128, chunk_cols(p, ch), false);
+        nbar_sync(kNbQ, kNbThreads);  // the query chunk landed
+        for (int mt = 0; mt < nmt; ++mt, ++di) {
+          const int db = di % 2;
+          if (lane == 0 && ok)
+            ok = mbar_wait(bar(C::B_DEMPTY + db), ((di / 2) & 1) ^ 1, abort_flag, p.status);
+          __syncwarp();
+          bool first = true;
+          for (int part = p.parts - 1; part >= 0; --part)
+            for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
+              const int as = ai % kAStages;
+              nbar_sync(kNbA, kNbThreads);  // the summary panel landed
+              if (lane == 0 && ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -230,15 +234,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar(C::B_AEMPTY + as));
               }
-            if (!ok) break;
-            mma_commit(bar(C::B_DFULL + db));
-          }
-          if (!ok) break;
-          mma_commit(bar(C::B_QEMPTY + qs));
+              __syncwarp();
+            }
+          if (lane == 0 && ok) mma_commit(bar(C::B_DFULL + db));
+          __syncwarp();
         }
+        if (lane == 0 && ok) mma_commit(bar(C::B_QEMPTY + qs));
+        __syncwarp();
       }
+    }
+    if (lane == 0) {
       mma_commit(bar(C::B_FINAL));
       mbar_wait_drain(bar(C::B_FINAL), 0);
+    }
+    __syncwarp();
+  } else if (warp == kWatchWarp) {
+    // ------------------------------------------------------------ copy watcher
+    int qi = 0, ai = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const RUnit x = runit(p, u);
+      if (!x.valid) continue;
+      const int nmt = (x.r + 127) / 128;
+      for (int ch = 0; ch < p.nch; ++ch, ++qi) {
+        const int qs = qi % kQStages;
+        if (lane == 0 && ok)
+          ok = mbar_wait(bar(C::B_QFULL + qs), (qi / kQStages) & 1, abort_flag, p.status);
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        nbar_sync(kNbQ, kNbThreads);
+        for (int mt = 0; mt < nmt; ++mt)
+          for (int part = p.parts - 1; part >= 0; --part)
+            for (int pn = 0; pn < C::kPanels; ++pn, ++ai) {
+              const int as = ai % kAStages;
+              if (lane == 0 && ok)
+                ok = mbar_wait(bar(C::B_AFULL + as), (ai / kAStages) & 1, abort_flag, p.status);
+              __syncwarp();
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              nbar_sync(kNbA, kNbThreads);
+            }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-3)
