@@ -26,7 +26,7 @@
 //   warp 6     watcher: waits on the copies' mbarriers and meets the MMA warp on
 //              named barriers (an mbarrier check would cost the issuing thread a few
 //              hundred cycles while the MMAs stream their operands from shared memory)
-// Work order: rows with the longest history first (r descending).
+// Work order: rows with the longest and the shortest history alternately.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -86,7 +86,12 @@ struct RUnit {
 BSA_DEV RUnit runit(const RouteTcParams &p, int u) {
   RUnit x;
   const int BH = p.B * p.Hk;
-  x.qb = p.Nq - 1 - u / BH;
+  // Rank k of the longest-first order, taken alternately from its two ends (0, N-1, 1,
+  // N-2, ...): along a CTA's stride long rows (tensor-bound) and short ones (bound by
+  // their query copies) alternate, so the copies overlap the products.
+  const int k = u / BH;
+  const int kk = (k & 1) ? p.Nq - 1 - (k >> 1) : (k >> 1);
+  x.qb = p.Nq - 1 - kk;
   const int ih = u % BH;
   x.i = ih / p.Hk;
   x.h = ih % p.Hk;
