@@ -149,15 +149,26 @@ __global__ void __launch_bounds__(kThreads) chunk_append_kernel(
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  for (int row = rg; row < 64; row += rgroups) {
-    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+  // this thread's rows (d / 32 of them, at most 4): every load goes out before the
+  // first store, so a thread keeps all of its copies in flight
+  uint4 kv[4], vv[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int row = rg + t * rgroups;
+    kv[t] = vv[t] = make_uint4(0u, 0u, 0u, 0u);
     if (row < nrows) {
-      kv = __ldg(reinterpret_cast<const uint4 *>(K + src + (size_t)row * d) + vec);
-      vv = __ldg(reinterpret_cast<const uint4 *>(V + src + (size_t)row * d) + vec);
-      Vec16<uint16_t>::add(kv, acc);
+      kv[t] = __ldg(reinterpret_cast<const uint4 *>(K + src + (size_t)row * d) + vec);
+      vv[t] = __ldg(reinterpret_cast<const uint4 *>(V + src + (size_t)row * d) + vec);
     }
-    reinterpret_cast<uint4 *>(kc + dst + (size_t)row * d)[vec] = kv;
-    reinterpret_cast<uint4 *>(vc + dst + (size_t)row * d)[vec] = vv;
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int row = rg + t * rgroups;
+    if (row < 64) {
+      if (row < nrows) Vec16<uint16_t>::add(kv[t], acc);
+      reinterpret_cast<uint4 *>(kc + dst + (size_t)row * d)[vec] = kv[t];
+      reinterpret_cast<uint4 *>(vc + dst + (size_t)row * d)[vec] = vv[t];
+    }
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[rg * d + vec * 8 + e] = acc[e];
