@@ -12,11 +12,19 @@
 // twice and its copy masked).  Every MMA therefore has N = 128, the shape at
 // which tcgen05 runs at its full rate (N = 64 runs at two thirds).
 //
-// Warp roles (352 threads):
-//   warps 0-3  softmax / epilogue for M-tile 0 (thread = one query row = one TMEM lane)
-//   warps 4-7  softmax / epilogue for M-tile 1
-//   warp 8     TMA producer: Q tiles, then the K and V rows of each key step
-//   warps 9-10 MMA issuers, one thread each: warp 9 + t issues M-tile t's products
+// Warp roles (512 threads):
+//   warps 0-3   softmax for M-tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7   softmax for M-tile 1
+//   warp 8      TMA producer: Q tiles, then the K and V rows of each key step
+//   warps 9-10  MMA issuers, one thread each: warp 9 + t issues M-tile t's products
+//   warp 11     idle (completes the warpgroup of warps 8-10)
+//   warps 12-15 output epilogue of both M-tiles (warp 12 + q reads TMEM lane quarter q)
+// A unit's last softmax step hands each row's 1 / l to the epilogue warpgroup through
+// shared memory and goes straight on to the next unit; the epilogue reads O out of
+// tensor memory, releases it to the next unit's PV and writes the tile out while the
+// softmax already works on the next unit.  The warpgroups split the register file
+// (setmaxnreg): the softmax takes more than the 128 registers a thread has at launch,
+// the TMA / MMA warps and the epilogue give theirs up.
 // TMEM (512 columns): O_0, O_1 (d columns each), S_0, S_1 (128 columns each).  The
 // softmax overwrites the first 64 columns of S_t with P (bf16 pairs) and the PV
 // product reads P straight from tensor memory.
@@ -48,9 +56,16 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 512;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;    // M-tile 0's issuer; M-tile 1's is kMmaWarp + 1; owns TMEM
+constexpr int kEpiWarp = 12;   // first of the four epilogue warps
+// Registers per thread after the split, for the softmax warpgroups, the warpgroup of
+// the TMA and MMA warps, and the epilogue warpgroup.  The four warpgroups hold
+// 4 x 128 x 128 registers at launch, and the split must stay within them (an
+// increase waits until other warpgroups have released enough).
+constexpr uint32_t kRegSoftmax = 176, kRegIssue = 56, kRegEpi = 104;
+static_assert(2 * kRegSoftmax + kRegIssue + kRegEpi <= 4 * 128, "register split");
 constexpr int kTmemCols = 512;
 constexpr int kStep = 128;  // keys per step
 constexpr int kPrefetch = 2;  // steps of K / V prefetched into L2 ahead of their stage load
@@ -82,9 +97,12 @@ struct Cfg {
   static constexpr int B_OSTAGED = B_OFINAL + 2;  // a staged output half is complete (4 warps)
   static constexpr int B_OSFREE = B_OSTAGED + 2;  // the staging buffer was read by its store
   static constexpr int B_FINAL = B_OSFREE + 2;    // one per issuer
-  static constexpr int kNumBars = B_FINAL + 2;
+  static constexpr int B_STATS = B_FINAL + 2;     // a unit's 1 / l of tile t staged (4 warps)
+  static constexpr int B_STATSFREE = B_STATS + 2; // ... and read by the epilogue (4 warps)
+  static constexpr int kNumBars = B_STATSFREE + 2;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemUsed = kOffCtl + 16;
+  static constexpr int kOffStat = kOffCtl + 16;           // 1 / l of each tile's 128 rows
+  static constexpr int kSmemUsed = kOffStat + 2 * 128 * 4;
   // 1 KB for base alignment; at least 120 KB so that exactly one CTA (which owns
   // all 512 TMEM columns) is resident per SM.
   static constexpr int kSmemBytes = kSmemUsed + 1024 < 120 * 1024 ? 120 * 1024 : kSmemUsed + 1024;
@@ -315,6 +333,17 @@ BSA_DEV float exp_step(uint32_t tS, uint64_t scale2, uint64_t negm, const int (&
   return lo_of(acc) + hi_of(acc);
 }
 
+// Warpgroup-wide change of this warp's register allocation (every warp of the
+// warpgroup executes the same one).
+template <uint32_t R>
+BSA_DEV void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+BSA_DEV void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 template <int D, int BK, bool CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -349,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_OSTAGED + t), 4);
       mbar_init(bar(C::B_OSFREE + t), 1);
+      mbar_init(bar(C::B_STATS + t), 4);
+      mbar_init(bar(C::B_STATSFREE + t), 4);
     }
     mbar_init(bar(C::B_FINAL), 1);
     mbar_init(bar(C::B_FINAL + 1), 1);
@@ -373,8 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_units = __ldg(p.bucket_off + BSA_NUM_BUCKETS) * p.npairs;
   const uint32_t smQ = sbase + C::kOffQ, smK = sbase + C::kOffK, smV = sbase + C::kOffV;
 
+  // Each role changes its register allocation first (warps 8-11 together, each
+  // softmax warpgroup, the epilogue warpgroup).
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
+    reg_dealloc<kRegIssue>();
     if (lane == 0) {
       int stp = 0, ucount = 0;   // global step counter (stage ring), units
       int issuedK[C::NS], issuedV[C::NS], issuedQ = -1;
@@ -456,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers
+    reg_dealloc<kRegIssue>();
     const int t = warp - kMmaWarp;  // the M-tile this warp's lane 0 issues for
     {
       const bool lead = lane == 0;  // waits and issues; the whole warp takes the turns
@@ -583,8 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    reg_alloc<kRegSoftmax>();
     const int t = warp / 4;           // M-tile of this warpgroup
     const int wq = warp % 4;          // TMEM lane quarter
     const int rho = wq * 32 + lane;   // row of the M-tile
@@ -592,9 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + C::colO(t);
     const uint32_t tS = tmem + lane_base + C::colS(t);
     int kstep = 0;                    // steps of this tile (S / P / O-done phases)
-    int units = 0;                    // units of this tile (O-final phases)
-    int ostage = 0;                   // output staging uses of this tile
-    bool store_pending = false;       // elected thread: the last staged store is not yet waited
+    int units = 0;                    // units of this tile (row statistics handed over)
+    float *stat_inv_l = reinterpret_cast<float *>(sm + C::kOffStat) + t * 128;
     bool ok = true;
     const uint64_t scale2 = pack2(p.scale_log2, p.scale_log2);
     // Position of the diagonal block r in a unit's row (the token-level triangle),
@@ -699,92 +734,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s == 0 && has_next) nx_diag = diag_of(nx);
       }
       if (!ok) continue;
-      // epilogue: O = u / l, lse = (m + log2 l) ln 2
-      ok = mbar_wait(bar(C::B_OFINAL + t), units & 1, abort_flag, p.status);
+      // Hand the row's 1 / l to the epilogue warpgroup (its slot is free once the
+      // epilogue has read the previous unit's) and write lse = (m + log2 l) ln 2.
+      if (units > 0) ok = mbar_wait(bar(C::B_STATSFREE + t), (units - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         continue;
       }
-      ++units;
-      tc_fence_after();
-      const bool store = row_valid && tq < x.n;
-      const float inv_l = 1.f / l;
-      // Read the whole O row as bf16 pairs first, release O to the next unit's PV,
-      // and only then write the row out.
-      uint32_t ob[D / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ro[32];
-        tmem_ld32(tO + c0, ro);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ob[c0 / 2 + e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv_l,
-                                       __uint_as_float(ro[2 * e + 1]) * inv_l);
-      }
-      tc_fence_before();
+      stat_inv_l[rho] = 1.f / l;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_OFREE + t));
-      if (store && p.lse != nullptr)
+      if (lane == 0) mbar_arrive(bar(C::B_STATS + t));
+      ++units;
+      if (row_valid && tq < x.n && p.lse != nullptr)
         p.lse[(size_t)hq * p.T + x.s0 + tq] = (m_used + fast_log2(l)) * 0.6931471805599453f;
-      // A tile whose 128 rows are all valid query rows of a full block goes out
-      // through shared memory and tensor stores (one 64-column half at a time, in
-      // the 128-byte-swizzled layout of the store box); other tiles (sequence
-      // tails, partial groups) store their valid rows directly.
-      const bool via_tma =
-          (2 * x.pair + t + 1) * 128 <= p.G * BK && (qblock<CHUNK>(x) + 1) * BK <= x.n;
-      if (via_tma) {
-        const uint32_t stg = sbase + C::kOffStageO + t * C::kStageO;
-        const bool elected = wq == 0 && lane == 0;
+    }
+  } else if (warp >= kEpiWarp) {
+    // ------------------------------------------------------------ epilogue, both M-tiles
+    reg_dealloc<kRegEpi>();
+    const int wq = warp % 4;          // TMEM lane quarter
+    const int rho = wq * 32 + lane;   // row of the M-tile
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float *stat_inv_l = reinterpret_cast<const float *>(sm + C::kOffStat);
+    const bool elected = wq == 0 && lane == 0;  // issues the tensor stores
+    int ut[2] = {0, 0};               // units of each tile (O-final / statistics phases)
+    int ostage[2] = {0, 0};           // output staging uses of each tile
+    bool store_pending[2] = {false, false};  // elected: a tile's last staged store not yet waited
+    bool ok = true;
+    Unit nx;
+    if (blockIdx.x < total_units) nx = decode_unit<CHUNK>(p, blockIdx.x);
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      const Unit x = nx;
+      if (u + (int)gridDim.x < total_units) nx = decode_unit<CHUNK>(p, u + gridDim.x);  // prefetch
+      for (int t = 0; ok && t < x.nt; ++t) {
+        // O = u / l once the unit's last PV of tile t is done and its 1 / l is staged
+        ok = mbar_wait(bar(C::B_OFINAL + t), ut[t] & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait(bar(C::B_STATS + t), ut[t] & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++ut[t];
+        tc_fence_after();
+        const int grow = (2 * x.pair + t) * 128 + rho;   // row within the group's G*b rows
+        const int tq = qblock<CHUNK>(x) * BK + grow % BK;  // query position in the packed Q
+        const bool store = grow < p.G * BK && tq < x.n;
+        const int hq = x.h * p.G + grow / BK;
+        const float inv_l = stat_inv_l[t * 128 + rho];
+        const uint32_t tO = tmem + lane_base + C::colO(t);
+        // Read the whole O row as bf16 pairs first, release O (to the next unit's PV)
+        // and the statistics slot, and only then write the row out.
+        uint32_t ob[D / 2];
 #pragma unroll
-        for (int hh = 0; hh < C::kPanels; ++hh, ++ostage) {
-          // the last half of the previous unit is waited for only now, when the buffer
-          // is needed again
-          if (elected && store_pending) {
-            bulk_wait_read();
-            mbar_arrive(bar(C::B_OSFREE + t));
-            store_pending = false;
-          }
-          // the previous store out of this buffer has finished reading it
-          if (!__all_sync(0xffffffffu, ok = mbar_wait(bar(C::B_OSFREE + t), (ostage & 1) ^ 1,
-                                                      abort_flag, p.status))) {
-            ok = false;
-            break;
-          }
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ro[32];
+          tmem_ld32(tO + c0, ro);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(stg + rho * 128 + ((c ^ (rho & 7)) << 4), ob[hh * 32 + 4 * c],
-                         ob[hh * 32 + 4 * c + 1], ob[hh * 32 + 4 * c + 2], ob[hh * 32 + 4 * c + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(C::B_OSTAGED + t));
-          if (elected) {
-            ok = mbar_wait(bar(C::B_OSTAGED + t), ostage & 1, abort_flag, p.status);
-            if (ok) {
-              tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
-                           x.h * p.G + ((2 * x.pair + t) * 128) / BK);
-              bulk_commit();
-              if (hh + 1 < C::kPanels) {
-                bulk_wait_read();
-                mbar_arrive(bar(C::B_OSFREE + t));
-              } else {
-                store_pending = true;
+          for (int e = 0; e < 16; ++e)
+            ob[c0 / 2 + e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv_l,
+                                         __uint_as_float(ro[2 * e + 1]) * inv_l);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(C::B_OFREE + t));
+          mbar_arrive(bar(C::B_STATSFREE + t));
+        }
+        // A tile whose 128 rows are all valid query rows of a full block goes out
+        // through shared memory and tensor stores (one 64-column half at a time, in
+        // the 128-byte-swizzled layout of the store box); other tiles (sequence
+        // tails, partial groups) store their valid rows directly.
+        const bool via_tma =
+            (2 * x.pair + t + 1) * 128 <= p.G * BK && (qblock<CHUNK>(x) + 1) * BK <= x.n;
+        if (via_tma) {
+          const uint32_t stg = sbase + C::kOffStageO + t * C::kStageO;
+#pragma unroll
+          for (int hh = 0; hh < C::kPanels; ++hh, ++ostage[t]) {
+            // the last half of the tile's previous unit is waited for only now, when
+            // the buffer is needed again
+            if (elected && store_pending[t]) {
+              bulk_wait_read();
+              mbar_arrive(bar(C::B_OSFREE + t));
+              store_pending[t] = false;
+            }
+            // the previous store out of this buffer has finished reading it
+            if (!__all_sync(0xffffffffu, ok = mbar_wait(bar(C::B_OSFREE + t), (ostage[t] & 1) ^ 1,
+                                                        abort_flag, p.status))) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(stg + rho * 128 + ((c ^ (rho & 7)) << 4), ob[hh * 32 + 4 * c],
+                           ob[hh * 32 + 4 * c + 1], ob[hh * 32 + 4 * c + 2], ob[hh * 32 + 4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_OSTAGED + t));
+            if (elected) {
+              ok = mbar_wait(bar(C::B_OSTAGED + t), ostage[t] & 1, abort_flag, p.status);
+              if (ok) {
+                tma_store_3d(&tmO, stg, hh * 64, x.s0 + qblock<CHUNK>(x) * BK,
+                             x.h * p.G + ((2 * x.pair + t) * 128) / BK);
+                bulk_commit();
+                if (hh + 1 < C::kPanels) {
+                  bulk_wait_read();
+                  mbar_arrive(bar(C::B_OSFREE + t));
+                } else {
+                  store_pending[t] = true;
+                }
               }
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);  // the elected thread's outcome, warp-wide
+            if (!ok) break;
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);  // the elected thread's outcome, warp-wide
-          if (!ok) break;
-        }
-        if (!ok) continue;
-      } else if (store) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.O + ((size_t)hq * p.T + x.s0 + tq) * D);
+        } else if (store) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.O + ((size_t)hq * p.T + x.s0 + tq) * D);
 #pragma unroll
-        for (int q4 = 0; q4 < D / 8; ++q4)
-          dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+          for (int q4 = 0; q4 < D / 8; ++q4)
+            dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+        }
       }
     }
+  } else {
+    reg_dealloc<kRegIssue>();  // warp 11: no role
   }
 
-  if (warp < 8 && (warp % 4) == 0 && lane == 0) bulk_wait_all();  // output stores done
+  if (warp == kEpiWarp && lane == 0) bulk_wait_all();  // output stores done
   grid_dep_launch();  // the next launch may be scheduled; it waits for this grid
   tc_fence_before();
   __syncthreads();
