@@ -97,6 +97,15 @@ __global__ void __launch_bounds__(kScoreThreads) dec_score_kernel(
   const int ngrp = (npg + 7) / 8;
   for (int item = warp; item < Hk * ngrp; item += kScoreThreads / 32) {
     const int h = item / ngrp, p0 = (item - h * ngrp) * 8;
+    {  // this warp's next item towards L2: lane = (page, 128-byte line of its summary row)
+      const int nitem = item + kScoreThreads / 32;
+      if (nitem < Hk * ngrp) {
+        const int nh = nitem / ngrp, np0 = (nitem - nh * ngrp) * 8 + (lane >> 2);
+        const int ph = np0 < npg ? phys_s[np0] : -1;
+        if (ph >= 0)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(ps + ((size_t)ph * Hk + nh) * kD + (lane & 3) * 32));
+      }
+    }
     float4 c[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {  // a missing page of the last group repeats the first
@@ -289,14 +298,20 @@ __global__ void __launch_bounds__(kSelThreads) dec_select_kernel(
 //   O^T = V^T P^T M = d = 128,   N = 16,                                K = 128 keys
 // A unit holding one page only reads the second page at an out-of-range page
 // coordinate, which the tensor copy fills with zeros, and masks its keys.
-// Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue: thread = one key row of S^T (TMEM lane), then
-//              one d row of O^T
+// Warp roles (320 threads):
+//   warps 0-3  softmax: thread = one key row of S^T (TMEM lane)
 //   warp 4     producer: resolves the page indices of 32 units at a time, then
 //              stages K, V (two 64-column panels x two pages) and Q by TMA
 //   warp 5     MMA issuer (one thread); owns the TMEM allocation
+//   warps 6-9  epilogue: thread = one d row of O^T (warp 6 + q reads TMEM lane
+//              quarter (q + 2) mod 4), writes the unit's partial (m, l, u)
+// The softmax warps hand a unit to the epilogue warps once its P and row sums are
+// written and go on to the next unit while the unit's PV runs and its partial is
+// written out; a buffer (b = unit parity) is reused two units later only after the
+// epilogue has released it.
 // TMEM (64 columns): S_0, S_1, O_0, O_1 (16 columns each), double-buffered by unit.
-constexpr int kDecThreads = 192;
+constexpr int kDecThreads = 320;
+constexpr int kDecEpi = 6;       // first of the four epilogue warps
 constexpr int kDecProducer = 4;
 constexpr int kDecMma = 5;
 constexpr int kNS = 3;                       // K/V/Q stages
@@ -311,10 +326,13 @@ constexpr int kOffStages = 0;
 constexpr int kOffP = kOffStages + kNS * kStageBytes;
 constexpr int kOffHdr = kOffP + 2 * kPBytes;        // per stage: unit, valid A, valid B
 constexpr int kOffRed = kOffHdr + kNS * 16;          // [2][4][16] max, [2][4][16] sum
-constexpr int kOffBar = kOffRed + 2 * 2 * 4 * 16 * 4;
-// barriers: FULL[kNS], EMPTY[kNS], SFULL[2], PFULL[2], OFULL[2], MX[2], LS[2], FINAL
+constexpr int kOffEpi = kOffRed + 2 * 2 * 4 * 16 * 4; // [2] unit handed to the epilogue
+constexpr int kOffBar = kOffEpi + 16;
+// barriers: FULL[kNS], EMPTY[kNS], SFULL[2], PFULL[2], OFULL[2], MX[2], EPI[2] (a unit
+// handed to the epilogue), EPIFREE[2] (its buffer released by the epilogue), FINAL
 constexpr int B_FULL = 0, B_EMPTY = kNS, B_SFULL = 2 * kNS, B_PFULL = B_SFULL + 2,
-              B_OFULL = B_PFULL + 2, B_MX = B_OFULL + 2, B_LS = B_MX + 2, B_FIN = B_LS + 2;
+              B_OFULL = B_PFULL + 2, B_MX = B_OFULL + 2, B_EPI = B_MX + 2,
+              B_EPIFREE = B_EPI + 2, B_FIN = B_EPIFREE + 2;
 constexpr int kNumBars = B_FIN + 1;
 constexpr int kOffCtl = kOffBar + kNumBars * 8;     // tmem base, abort flag
 constexpr int kDecSmem = kOffCtl + 16 + 1024;
@@ -373,6 +391,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   int32_t *hdr = reinterpret_cast<int32_t *>(sm + kOffHdr);
   float *red_m = reinterpret_cast<float *>(sm + kOffRed);
   float *red_l = red_m + 2 * 4 * 16;
+  int32_t *epi_u = reinterpret_cast<int32_t *>(sm + kOffEpi);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffCtl);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(sm + kOffCtl + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -387,7 +406,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_init(bar(B_PFULL + b), 4);
       mbar_init(bar(B_OFULL + b), 1);
       mbar_init(bar(B_MX + b), 4);
-      mbar_init(bar(B_LS + b), 4);
+      mbar_init(bar(B_EPI + b), 4);
+      mbar_init(bar(B_EPIFREE + b), 4);
     }
     mbar_init(bar(B_FIN), 1);
     *abort_flag = 0;
@@ -542,9 +562,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mma_commit(bar(B_FIN));
       mbar_wait_drain(bar(B_FIN), 0);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int t = warp * 32 + lane;  // key row of S^T, then d row of O^T
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp * 32 + lane;  // key row of S^T
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     // byte offset of P^T[g][t] inside one P buffer (128-byte swizzle, 8-row atoms)
     const uint32_t t_panel = (uint32_t)(t >> 6) * kQPanel, t_chunk = (uint32_t)((t & 63) >> 3),
@@ -555,7 +575,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       bar_warps_wait(bar(B_FULL + st), (i / kNS) & 1, abort_flag, p.status, ok);
       if (!ok) break;
       const int u = hdr[st * 4 + 0];
-      if (u < 0) break;
+      // buffer b (row statistics, unit slot, O_b) was released by the epilogue for
+      // unit i - 2
+      if (i >= 2) bar_warps_wait(bar(B_EPIFREE + b), ((i - 2) / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      if (u < 0) {  // end of work, passed on to the epilogue
+        if (t == 0) epi_u[b] = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_EPI + b));
+        break;
+      }
       const int va = hdr[st * 4 + 1], vb = hdr[st * 4 + 2];
       const bool valid = t < kPage ? t < va : t - kPage < vb;
       bar_warps_wait(bar(B_SFULL + b), (i / 2) & 1, abort_flag, p.status, ok);
@@ -576,13 +605,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_MX + b));
       bar_warps_wait(bar(B_MX + b), (i / 2) & 1, abort_flag, p.status, ok);
       if (!ok) break;
-      float M[G], l[G];
+      float l[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        M[g] = fmaxf(fmaxf(red_m[(b * 4 + 0) * 16 + g], red_m[(b * 4 + 1) * 16 + g]),
-                     fmaxf(red_m[(b * 4 + 2) * 16 + g], red_m[(b * 4 + 3) * 16 + g]));
+        const float M = fmaxf(fmaxf(red_m[(b * 4 + 0) * 16 + g], red_m[(b * 4 + 1) * 16 + g]),
+                              fmaxf(red_m[(b * 4 + 2) * 16 + g], red_m[(b * 4 + 3) * 16 + g]));
         // a unit's first page always holds a valid key, so M is finite
-        const float pg = fast_exp2(x[g] - M[g]);
+        const float pg = fast_exp2(x[g] - M);
         l[g] = pg;
         const __nv_bfloat16 pb = __float2bfloat16_rn(pg);
         const uint32_t off = t_panel + (uint32_t)g * 128u + ((t_chunk ^ (uint32_t)(g & 7)) << 4) + t_in;
@@ -601,18 +630,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         if (lane == 0) red_l[(b * 4 + warp) * 16 + g] = sum;
       }
+      if (t == 0) epi_u[b] = u;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_LS + b));
-      // epilogue: O^T row t of this unit
+      if (lane == 0) mbar_arrive(bar(B_EPI + b));
+    }
+  } else if (warp >= kDecEpi) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp % 4;            // TMEM lane quarter
+    const int t = q * 32 + lane;       // d row of O^T
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    bool ok = true;
+    for (int i = 0;; ++i) {
+      const int b = i & 1;
+      bar_warps_wait(bar(B_EPI + b), (i / 2) & 1, abort_flag, p.status, ok);
+      if (!ok) break;
+      const int u = epi_u[b];
+      if (u < 0) break;
       bar_warps_wait(bar(B_OFULL + b), (i / 2) & 1, abort_flag, p.status, ok);
       if (!ok) break;
       tc_fence_after();
+      uint32_t r[16];
       tmem_ld16(tmem + lane_base + kColO + 16 * b, r);
       float *po = p.part_o + (size_t)u * G * kD;
 #pragma unroll
       for (int g = 0; g < G; ++g) po[g * kD + t] = __uint_as_float(r[g]);
-      bar_warps_wait(bar(B_LS + b), (i / 2) & 1, abort_flag, p.status, ok);
-      if (!ok) break;
       if (t < G) {
         float lsum = 0.f, mt = 0.f;
 #pragma unroll
@@ -620,12 +661,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (g == t) {
             lsum = red_l[(b * 4 + 0) * 16 + g] + red_l[(b * 4 + 1) * 16 + g] +
                    red_l[(b * 4 + 2) * 16 + g] + red_l[(b * 4 + 3) * 16 + g];
-            mt = M[g];
+            mt = fmaxf(fmaxf(red_m[(b * 4 + 0) * 16 + g], red_m[(b * 4 + 1) * 16 + g]),
+                       fmaxf(red_m[(b * 4 + 2) * 16 + g], red_m[(b * 4 + 3) * 16 + g]));
           }
         p.part_ml[((size_t)u * G + t) * 2] = mt;
         p.part_ml[((size_t)u * G + t) * 2 + 1] = lsum;
       }
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_EPIFREE + b));
     }
   }
 
