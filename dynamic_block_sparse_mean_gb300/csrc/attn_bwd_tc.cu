@@ -32,6 +32,7 @@ namespace bsa {
 namespace {
 
 constexpr int kD = 128;
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // kind::f16 instruction descriptors: S / dP (A, B K-major, N = 64 keys); dQ
@@ -574,9 +575,9 @@ __global__ void __launch_bounds__(dq::kThreads, 1) bwd_dq_tc_kernel(
       const Item w = nx;
       if (u + stride < total) nx = item_of(u + stride);
       for (int s = 0; s < w.nsteps; ++s, ++gs) {
-        if (ok && s == 0) ok = mbar_wait(bar(B_QFULL), it & 1, abort_flag, p.status);
-        if (ok) ok = mbar_wait(bar(B_KFULL + gs % NK), (gs / NK) & 1, abort_flag, p.status);
-        if (ok) ok = mbar_wait(bar(B_VFULL + gs % NV), (gs / NV) & 1, abort_flag, p.status);
+        if (ok && s == 0) ok = mbar_wait_poll(bar(B_QFULL), it & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait_poll(bar(B_KFULL + gs % NK), (gs / NK) & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait_poll(bar(B_VFULL + gs % NV), (gs / NV) & 1, abort_flag, p.status);
         ok = __all_sync(0xffffffffu, ok);
         nbar_sync(kNbKV, kKVThreads);
       }

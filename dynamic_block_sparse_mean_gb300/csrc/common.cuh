@@ -140,6 +140,32 @@ BSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_fl
   }
 }
 
+// Like mbar_wait, but polling with the non-blocking test_wait: the warp is never
+// suspended between checks, so it sees a completed phase at once.  For a warp whose
+// only work is to wait (a copy watcher).
+BSA_DEV bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int32_t *abort_flag,
+                            int32_t *status) {
+  const long long t0 = clock64();
+#pragma unroll 1
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      set_status(status, BSA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // Named barrier `id` (1 .. 15; 0 is __syncthreads) over `count` threads (a multiple of
 // 32), blocking, warp-collective.  It does not touch shared memory, so it stays cheap
 // while MMAs stream their operands from there.  Every participant must reach it the
