@@ -3,7 +3,8 @@
 // rows grouped into length buckets and handed to one persistent launch).
 //   1. rows kernel   validates each row and records its length (grid-wide)
 //   2. scan kernel   row_ptr by prefix sum, and the work list: a stable counting
-//                    sort of rows by capacity bucket, largest first (one CTA)
+//                    sort of rows by length, longest first (one CTA); the
+//                    capacity buckets are contiguous ranges of it
 //   3. fill kernel   copies the block ids into col_idx (grid-wide)
 #include <cudaTypedefs.h>
 
@@ -79,15 +80,6 @@ __global__ void wl_rows_kernel(const int32_t *__restrict__ J, const int32_t *__r
   grid_dep_launch();
 }
 
-BSA_DEV int bucket_of(int len) {  // capacity max(4, pow2 >= len): 256 -> 0, ..., 4 -> 6
-  int cap = 4, s = 6;
-  while (cap < len && s > 0) {
-    cap <<= 1;
-    --s;
-  }
-  return s;
-}
-
 // Exclusive scan over the block of N values per thread at once (warp shuffles,
 // then a scan of the 32 warp totals): v becomes each thread's exclusive prefix,
 // tot the block totals.
@@ -129,61 +121,96 @@ BSA_DEV void block_scan_n(int (&v)[N], int (&tot)[N], int (*wsum)[N]) {
   }
 }
 
-// One CTA: row_ptr by prefix sum of the row lengths, and the work list: a stable
-// counting sort of rows by capacity bucket, largest bucket first.  Thread t owns
-// a contiguous chunk of rows.
+// One CTA: row_ptr by prefix sum of the row lengths, and the work list: the rows
+// with at least one block, longest first (lengths above 256 count as 256), rows of
+// equal length in row-id order: a stable counting sort on the length.  A persistent
+// launch that hands out the list round-robin then ends within about one unit of the
+// ideal; capacity buckets alone left the rows inside a bucket unordered.  The
+// capacity buckets are contiguous ranges of the list: bucket s (capacity 256 >> s)
+// starts after the rows longer than its capacity.  For the row_ptr scan thread t owns
+// a contiguous chunk of rows; for the sort warp w does, walking it 32 rows at a time
+// (equal lengths inside a group of 32 ranked by lane).
 __global__ void __launch_bounds__(kScanThreads) wl_scan_kernel(
     const int32_t *__restrict__ code, int32_t *__restrict__ row_ptr, int32_t *__restrict__ work,
     int32_t *__restrict__ bucket_off, int nrows) {
   grid_dep_wait();  // the row codes come from the previous launch
   constexpr int NB = BSA_NUM_BUCKETS;
-  __shared__ int wsum[33][NB + 1];
-  const int t = threadIdx.x;
-  const int chunk = (nrows + kScanThreads - 1) / kScanThreads;
-  const int lo = min(nrows, t * chunk), hi = min(nrows, lo + chunk);
-  int v[NB + 1];  // v[0]: length sum; v[1 + s]: rows in bucket s
-#pragma unroll
-  for (int k = 0; k <= NB; ++k) v[k] = 0;
-  for (int row = lo; row < hi; ++row) {
+  constexpr int NK = 256;                 // sort keys 0 .. 255: 256 - min(length, 256)
+  constexpr int NW = kScanThreads / 32;   // warps
+  __shared__ int wsum[33][1];
+  __shared__ int hist[NK][NW];  // per (key, warp): rows, then the first position
+  const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  // row_ptr: prefix sum of the lengths (an error row, code -1, holds one block)
+  {
+    const int chunk = (nrows + kScanThreads - 1) / kScanThreads;
+    const int lo = min(nrows, t * chunk), hi = min(nrows, lo + chunk);
+    int v[1] = {0}, tot[1];
+    for (int row = lo; row < hi; ++row) {
+      const int c = code[row];
+      v[0] += c < 0 ? 1 : c;
+    }
+    block_scan_n<1>(v, tot, wsum);
+    int off = v[0];
+    for (int row = lo; row < hi; ++row) {
+      const int c = code[row];
+      row_ptr[row] = off;
+      off += c < 0 ? 1 : c;
+    }
+    if (t == 0) row_ptr[nrows] = tot[0];
+  }
+  for (int k = t; k < NK * NW; k += kScanThreads) (&hist[0][0])[k] = 0;
+  __syncthreads();
+  const int wchunk = (nrows + NW - 1) / NW;
+  const int wlo = min(nrows, warp * wchunk), whi = min(nrows, wlo + wchunk);
+  auto key_of = [&](int row) {  // -1: an empty row, not listed
+    if (row >= whi) return -1;
     const int c = code[row];
     const int len = c < 0 ? 1 : c;
-    v[0] += len;
-    if (len > 0) {
-      const int sb = bucket_of(len);
-#pragma unroll
-      for (int q = 0; q < NB; ++q) v[1 + q] += (q == sb) ? 1 : 0;
-    }
+    return len > 0 ? NK - min(len, NK) : -1;
+  };
+  // rows per (key, warp)
+  for (int r0 = wlo; r0 < whi; r0 += 32) {
+    const int key = key_of(r0 + lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && lane == __ffs(peers) - 1) hist[key][warp] += __popc(peers);
+    __syncwarp();
   }
-  int tot[NB + 1];
-  block_scan_n<NB + 1>(v, tot, wsum);
-  int bstart[NB];
-  int acc = 0;
+  __syncthreads();
+  // first position of each (key, warp): exclusive scan in key-major order, 8 entries
+  // per thread
+  constexpr int PER = NK * NW / kScanThreads;
+  static_assert(PER * kScanThreads == NK * NW, "scan split");
+  int *flat = &hist[0][0];
+  int loc[PER], v[1] = {0}, tot[1];
 #pragma unroll
-  for (int q = 0; q < NB; ++q) {
-    bstart[q] = acc;
-    acc += tot[1 + q];
+  for (int i = 0; i < PER; ++i) {
+    loc[i] = flat[PER * t + i];
+    v[0] += loc[i];
   }
+  __syncthreads();
+  block_scan_n<1>(v, tot, wsum);
+  int acc = v[0];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    flat[PER * t + i] = acc;
+    acc += loc[i];
+  }
+  __syncthreads();
   if (t == 0) {
-    row_ptr[nrows] = tot[0];
+    bucket_off[0] = 0;
 #pragma unroll
-    for (int q = 0; q < NB; ++q) bucket_off[q] = bstart[q];
-    bucket_off[NB] = acc;
+    for (int q = 1; q < NB; ++q) bucket_off[q] = hist[NK - (256 >> q)][0];  // rows longer than 256 >> q
+    bucket_off[NB] = tot[0];
   }
-  int off = v[0];
-  int pos[NB];
-#pragma unroll
-  for (int q = 0; q < NB; ++q) pos[q] = bstart[q] + v[1 + q];
-  for (int row = lo; row < hi; ++row) {
-    const int c = code[row];
-    const int len = c < 0 ? 1 : c;
-    row_ptr[row] = off;
-    off += len;
-    if (len > 0) {
-      const int sb = bucket_of(len);
-#pragma unroll
-      for (int q = 0; q < NB; ++q)
-        if (q == sb) work[pos[q]++] = row;
-    }
+  // placement: the (key, warp) start, plus the rows of the same key before this one
+  for (int r0 = wlo; r0 < whi; r0 += 32) {
+    const int row = r0 + lane, key = key_of(row);
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int base = key >= 0 ? hist[key][warp] : 0;
+    if (key >= 0) work[base + __popc(peers & ((1u << lane) - 1u))] = row;
+    __syncwarp();
+    if (key >= 0 && lane == __ffs(peers) - 1) hist[key][warp] = base + __popc(peers);
+    __syncwarp();
   }
   grid_dep_launch();
 }

@@ -126,16 +126,17 @@ def expected_csr(Jo, co, cu, b):
 
 
 def check_buckets(wl, rp):
-    """Every non-empty row appears once in `work`, in the bucket of its capacity
-    max(4, next power of two of its length), row-id order inside a bucket."""
+    """`work` lists every non-empty row once, longest first (lengths above 256 count
+    as 256), rows of equal length in row-id order; each row lies in the bucket of its
+    capacity max(4, next power of two of its length)."""
     bo = wl.bucket_off.cpu().numpy()
     work = wl.work.cpu().numpy()[:bo[-1]]
     lens = np.diff(rp)
-    assert sorted(work.tolist()) == sorted(np.nonzero(lens)[0].tolist())
+    rows = np.nonzero(lens)[0].tolist()
+    assert work.tolist() == sorted(rows, key=lambda w: (-min(int(lens[w]), 256), w))
     for s in range(7):
         seg = work[bo[s]:bo[s + 1]]
         assert all(max(4, 1 << int(np.ceil(np.log2(max(1, lens[w]))))) == 256 >> s for w in seg)
-        assert list(seg) == sorted(seg)
 
 
 def rows_token_mask(cu, b, G, rows, H, T):
