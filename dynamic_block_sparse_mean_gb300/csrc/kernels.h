@@ -87,7 +87,8 @@ cudaError_t launch_worklist(const bsa_shape_t &s, int32_t k_max, const int32_t *
                             int32_t *work, int32_t *bucket_off, int32_t *dev_status, void *ws,
                             cudaStream_t st, const bsa_kv_cache_t *cache = nullptr);
 // Row lengths (>= 0; a negative entry counts as 1) -> CSR offsets, and the rows of
-// non-zero length grouped by capacity bucket, largest first (worklist.cu).
+// non-zero length, those above 128 in exact order of length, the others grouped by
+// capacity bucket, longest first (worklist.cu).
 cudaError_t launch_length_scan(const int32_t *len, int32_t *row_ptr, int32_t *work,
                                int32_t *bucket_off, int nrows, cudaStream_t st);
 // Tensor-core backward, BF16 with head_dim 128 (attn_bwd_tc.cu): workspace of

@@ -181,9 +181,11 @@ bsa_status_t bsa_route(const bsa_shape_t *shape, const bsa_route_params_t *param
  *                sequence's end are empty.
  *   col_idx    : [B * H_kv * N_q * k_max] int32 capacity, CSR block ids.
  *   work       : [B * H_kv * N_q] int32 capacity: flattened row ids
- *                (i * H_kv + h) * N_q + r of the non-empty rows, longest first
- *                (lengths above 256 count as 256), rows of equal length in
- *                row-id order; so grouped by capacity bucket, largest first.
+ *                (i * H_kv + h) * N_q + r of the non-empty rows: rows longer
+ *                than 32 blocks first, longest first (lengths above 256 count
+ *                as 256), then the others by capacity bucket, largest first;
+ *                row-id order among rows of equal key.  So grouped by
+ *                capacity bucket, largest first.
  *   bucket_off : [BSA_NUM_BUCKETS + 1] int32: rows of capacity 256 >> s occupy
  *                work[bucket_off[s] .. bucket_off[s+1]); bucket_off[7] is the
  *                number of rows.  A row's capacity is max(4, next power of 2

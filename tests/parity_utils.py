@@ -125,18 +125,29 @@ def expected_csr(Jo, co, cu, b):
     return np.array(rp), np.array(ci)
 
 
+def capacity(n):
+    """A row's capacity bucket: max(4, next power of two of its length)."""
+    return max(4, 1 << int(np.ceil(np.log2(max(1, n)))))
+
+
 def check_buckets(wl, rp):
-    """`work` lists every non-empty row once, longest first (lengths above 256 count
-    as 256), rows of equal length in row-id order; each row lies in the bucket of its
-    capacity max(4, next power of two of its length)."""
+    """`work` lists every non-empty row once: rows longer than 32 blocks first,
+    longest first (lengths above 256 count as 256), then the others by capacity,
+    largest first, row-id order among equal keys; each row lies in the bucket of its
+    capacity."""
     bo = wl.bucket_off.cpu().numpy()
     work = wl.work.cpu().numpy()[:bo[-1]]
     lens = np.diff(rp)
     rows = np.nonzero(lens)[0].tolist()
-    assert work.tolist() == sorted(rows, key=lambda w: (-min(int(lens[w]), 256), w))
+
+    def key(w):
+        n = int(lens[w])
+        return (0, -min(n, 256), w) if n > 32 else (1, -capacity(n), w)
+
+    assert work.tolist() == sorted(rows, key=key)
     for s in range(7):
         seg = work[bo[s]:bo[s + 1]]
-        assert all(max(4, 1 << int(np.ceil(np.log2(max(1, lens[w]))))) == 256 >> s for w in seg)
+        assert all(capacity(lens[w]) == 256 >> s for w in seg)
 
 
 def rows_token_mask(cu, b, G, rows, H, T):
