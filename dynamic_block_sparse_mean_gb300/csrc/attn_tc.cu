@@ -68,7 +68,6 @@ constexpr uint32_t kRegSoftmax = 176, kRegIssue = 56, kRegEpi = 104;
 static_assert(2 * kRegSoftmax + kRegIssue + kRegEpi <= 4 * 128, "register split");
 constexpr int kTmemCols = 512;
 constexpr int kStep = 128;  // keys per step
-constexpr int kPrefetch = 2;  // steps of K / V prefetched into L2 ahead of their stage load
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kNbTurn = 1;  // named barriers 1, 2: the issuers' turns
 constexpr uint32_t kNbP = 3;     // named barriers 3, 4: P_t written (warpgroup t + issuer t)
@@ -435,27 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_prefetch_l2_3d(&tmQ, pn * 64, nx.s0 + qblock<CHUNK>(nx) * BK,
                                  nx.h * p.G + ((2 * nx.pair + t) * 128) / BK);
         const int nsteps = (x.nkv + BPS - 1) / BPS;
-        const int nsteps_next = has_next ? (nx.nkv + BPS - 1) / BPS : 0;
-        // K / V of the step kPrefetch ahead (possibly in the next unit) go to L2 first,
-        // so the stage loads below hit L2 instead of waiting on HBM.
-        auto prefetch_step = [&](const Unit &w, int s) {
-#pragma unroll
-          for (int e = 0; e < BPS; ++e) {
-            const int jb = min(s * BPS + e, w.nkv - 1);
-            const int2 y = kv_coord<CHUNK, BK>(p, w, jb);
-            for (int pn = 0; pn < C::kPanels; ++pn) {
-              tma_prefetch_l2_3d(&tmK, pn * 64, y.x, y.y);
-              tma_prefetch_l2_3d(&tmV, pn * 64, y.x, y.y);
-            }
-          }
-        };
-        if (u == (int)blockIdx.x)
-          for (int s = 0; s < kPrefetch && s < nsteps; ++s) prefetch_step(x, s);
+        // The K / V stage loads go straight to HBM / L2: prefetching them into L2 one
+        // or two steps ahead made the launch slower (128k workload 7.10 ms without,
+        // 7.19 one step ahead, 7.30 two; the 2-stage ring already keeps a step ahead).
         for (int s = 0; s < nsteps; ++s, ++stp) {
-          if (s + kPrefetch < nsteps)
-            prefetch_step(x, s + kPrefetch);
-          else if (s + kPrefetch - nsteps < nsteps_next)
-            prefetch_step(nx, s + kPrefetch - nsteps);
           int2 y[BPS];
 #pragma unroll
           for (int e = 0; e < BPS; ++e)  // a missing block repeats the last one
