@@ -427,16 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smQ + t * C::kQTile + pn * 16384, &tmQ, bar(C::B_QFULL), pn * 64,
                         x.s0 + qblock<CHUNK>(x) * BK, hq0);
         }
-        const bool has_next = u + (int)gridDim.x < total_units;
-        if (has_next)  // the next unit's queries come from HBM: start them towards L2 now
-          for (int t = 0; t < nx.nt; ++t)
-            for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_prefetch_l2_3d(&tmQ, pn * 64, nx.s0 + qblock<CHUNK>(nx) * BK,
-                                 nx.h * p.G + ((2 * nx.pair + t) * 128) / BK);
         const int nsteps = (x.nkv + BPS - 1) / BPS;
-        // The K / V stage loads go straight to HBM / L2: prefetching them into L2 one
-        // or two steps ahead made the launch slower (128k workload 7.10 ms without,
-        // 7.19 one step ahead, 7.30 two; the 2-stage ring already keeps a step ahead).
+        // No copy is prefetched into L2: prefetching the K / V steps one or two steps
+        // ahead made the launch slower (128k workload 7.10 ms without, 7.19 one step
+        // ahead, 7.30 two; the 2-stage ring already keeps a step ahead), and so did
+        // prefetching the next unit's Q tiles at the start of a unit (6.98 ms without).
         for (int s = 0; s < nsteps; ++s, ++stp) {
           int2 y[BPS];
 #pragma unroll
