@@ -891,6 +891,18 @@ cudaError_t launch_tc(const bsa_shape_t &s, const void *Q, const void *K, const 
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, BK, CHUNK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The softmax warpgroups' setmaxnreg increase waits, without a bound, until the
+  // other warpgroups have released enough registers: refuse to launch a build whose
+  // per-thread launch count cannot cover the split (checked once per instantiation).
+  static const cudaError_t regs_ok = [] {
+    cudaFuncAttributes fa;
+    const cudaError_t r = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, BK, CHUNK>);
+    if (r != cudaSuccess) return r;
+    return fa.numRegs * kThreads >= (int)(2 * kRegSoftmax + kRegIssue + kRegEpi) * 128
+               ? cudaSuccess
+               : cudaErrorInvalidConfiguration;
+  }();
+  if (regs_ok != cudaSuccess) return regs_ok;
   const long long max_units = (long long)s.num_seqs * s.num_kv_heads * s.max_blocks * p.npairs;
   const int grid = (int)std::min<long long>(num_sms(), std::max<long long>(1, max_units));
   return launch_dependent(attn_tc_kernel<D, BK, CHUNK>, dim3(grid), dim3(kThreads),
